@@ -1,0 +1,204 @@
+/*
+ * gsr.h -- C ABI of the GB300 (sm_103a) shard-reduction GEMM.
+ *
+ * A BF16 linear projection whose cross-shard reduction is fused into the GEMM,
+ * stated for one GPU: the R "ranks" of a tensor-parallel group are R shard
+ * buffers in this GPU's memory, and one kernel launch reads them all in place.
+ *
+ *   gemm_ar  Y   = sum_r X_r . W_r^T                (all-reduce over K-shards)
+ *   gemm_rs  Y_s = rows [s*rps, min(M,(s+1)*rps)) of sum_r X_r . W_r^T
+ *                  with rps = ceil(M / R)           (reduce-scatter by rows)
+ *   gemm_ag  Y   = concat_r(A_r) . W^T              (all-gather of M-shards)
+ *
+ * Sources of the definitions: vLLM PR #53053 summary ("Extend GEMM-RS to
+ * GEMM-AR"), implementation breakdown step 1 (one kernel serves RS and AR;
+ * AR accepts any M with no padding or input copy; flags handled inside the
+ * kernel) and the test's `_reference` (torch.mm(x, weight.T) per rank, then
+ * dist.all_reduce, or dist.reduce_scatter_single over rows padded to
+ * ceil(M/R)*R); vLLM PR #54151 "[Kimi-K3] AG-GEMM for Sequence Parallelism",
+ * Purpose (GEMM over the gathered activation shards).
+ *
+ * Conventions shared by every call
+ *   - Element type: bf16 in and out; products accumulate in fp32; the output
+ *     is rounded once, to nearest even.
+ *   - Layout: dense row-major, leading dimension = last dimension. Every GEMM
+ *     operand is K-major like an nn.Linear weight: X_r is M x K_r, W_r is
+ *     N x K_r, A_r is M_r x K, W is N x K. Outputs are rows x N.
+ *   - Alignment: every pointer 16-byte aligned; N and every K_r (AR/RS) or K
+ *     (AG) a multiple of 8, so that each row starts on a 16-byte boundary.
+ *   - Ownership: the caller owns every device buffer (shards, outputs,
+ *     workspace) and the stream. The library owns only the plan, a host
+ *     object; it allocates no device memory. Host pointer arrays are read
+ *     during the call only.
+ *   - Streams: calls are stream-ordered and asynchronous. Nothing synchronises
+ *     except gemm_shard_check_status. One workspace must not be used by two
+ *     calls that may run at the same time.
+ *   - Errors: argument errors are detected before any launch and return
+ *     GSR_ERR_INVALID_VALUE / GSR_ERR_WORKSPACE without touching the GPU. A
+ *     failed launch returns GSR_ERR_CUDA. Every wait inside the kernel is
+ *     bounded; a wait that runs out records GSR_ERR_TIMEOUT in the workspace
+ *     status word, the kernel returns cleanly, and gemm_shard_check_status
+ *     reports it. The library never aborts the process and never traps.
+ *     gsr_last_error_string() describes the last failure on this thread.
+ */
+#ifndef GSR_H
+#define GSR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream; NULL is the legacy default stream. */
+typedef struct CUstream_st *gsr_stream_t;
+
+typedef struct gemm_shard_plan gemm_shard_plan;
+
+typedef enum {
+    GSR_OK = 0,
+    GSR_ERR_INVALID_VALUE = 1, /* bad pointer, shape, alignment or option      */
+    GSR_ERR_UNSUPPORTED = 2,   /* device is not a GB300-class sm_103 part      */
+    GSR_ERR_WORKSPACE = 3,     /* workspace missing, misaligned or too small   */
+    GSR_ERR_CUDA = 4,          /* a CUDA runtime or driver call failed         */
+    GSR_ERR_TIMEOUT = 5        /* a bounded in-kernel wait ran out             */
+} gsr_status;
+
+/* Largest number of shards (ranks) one call accepts; the pages' gating allows
+ * tensor-parallel sizes 2..16 (PR #53053 summary, model.py gating chain). */
+#define GSR_MAX_SHARDS 16
+
+/* Plan options (gemm_shard_plan_set_option). 0 restores the default. */
+typedef enum {
+    GSR_OPT_SPLIT_K = 1,    /* pieces per output tile: 0 = heuristic, 1..16 forced */
+    GSR_OPT_BLOCK_N = 2,    /* output tile width: 0 = heuristic, 128 or 256         */
+    GSR_OPT_TIMEOUT_NS = 3, /* limit of every in-kernel wait, ns (default 2e9)      */
+    GSR_OPT_MAX_CTAS = 4    /* cap on persistent CTAs: 0 = one per SM               */
+} gsr_option;
+
+/*
+ * Create a plan for device `device` (a CUDA ordinal). The plan records the
+ * device's SM count and shared-memory limit and the largest shapes it will
+ * accept: max_M rows (AR/RS: M; AG: sum of M_r), max_N output columns, max_K
+ * reduction length (AR/RS: sum of K_r; AG: K) and max_R shards. It mirrors the
+ * pages' init_gemm_rs_ar(max_M, N, all_reduce) singleton (PR #53053 summary,
+ * model.py), minus the mode, which here is chosen per call.
+ * Returns GSR_ERR_UNSUPPORTED (and no plan) on anything but a compute
+ * capability 10.3 device or when no CUDA driver is present;
+ * GSR_ERR_INVALID_VALUE when out is NULL, a maximum is < 1, max_N or max_K is
+ * not a multiple of 8, or max_R is outside 1..GSR_MAX_SHARDS.
+ */
+gsr_status gemm_shard_plan_create(gemm_shard_plan **out, int device, int64_t max_M,
+                                  int64_t max_N, int64_t max_K, int max_R);
+
+/*
+ * Create a plan bound to no device, for a machine without a GPU: it describes
+ * a device with `sm_count` SMs. Calls made with it check their arguments and
+ * workspace exactly as on a device, then return GSR_ERR_UNSUPPORTED instead of
+ * launching (no device pointer is touched). gemm_shard_describe and
+ * gemm_shard_workspace_size work as for a device plan. Errors as
+ * gemm_shard_plan_create, plus GSR_ERR_INVALID_VALUE for sm_count < 1.
+ */
+gsr_status gemm_shard_plan_create_host(gemm_shard_plan **out, int sm_count, int64_t max_M,
+                                       int64_t max_N, int64_t max_K, int max_R);
+
+/* Destroy a plan (NULL is accepted). Outstanding calls are unaffected. */
+gsr_status gemm_shard_plan_destroy(gemm_shard_plan *plan);
+
+/* Set an option (see gsr_option). Options change the kernel configuration of
+ * later calls only; they never change which elements are computed. */
+gsr_status gemm_shard_plan_set_option(gemm_shard_plan *plan, gsr_option option,
+                                      int64_t value);
+
+/*
+ * Bytes of workspace that every call under this plan (at any shape within its
+ * maxima, with its current options) needs. Always > 0: the workspace holds a
+ * status word, per-tile split-K arrival counters and fp32 split-K partials.
+ * Returns 0 for a NULL plan.
+ */
+size_t gemm_shard_workspace_size(const gemm_shard_plan *plan);
+
+/*
+ * Zero the workspace's status word and counters (stream-ordered memset). Do
+ * this once after allocating it, and again after a GSR_ERR_TIMEOUT. Kernels
+ * leave the counters at zero when they finish, so no reset is needed between
+ * calls. ws must be 256-byte aligned and at least gemm_shard_workspace_size
+ * bytes.
+ */
+gsr_status gemm_shard_workspace_init(const gemm_shard_plan *plan, void *ws,
+                                     size_t ws_bytes, gsr_stream_t stream);
+
+/*
+ * AR: Y = sum_{r<R} X_r . W_r^T.
+ *   M      rows of every X_r and of Y; 0 returns GSR_OK with no launch
+ *   N      rows of every W_r and columns of Y (multiple of 8)
+ *   R      number of shards, 1..plan max_R
+ *   K_r    host array of R shard widths, each >= 8 and a multiple of 8
+ *   X_r    host array of R device pointers, X_r[r] is M x K_r[r] bf16
+ *   W_r    host array of R device pointers, W_r[r] is N x K_r[r] bf16
+ *   Y      device pointer, M x N bf16; rows [0, M) are written, nothing else
+ *   ws     workspace of ws_bytes bytes (gemm_shard_workspace_size)
+ * Shards are read in place from their own allocations; no input is copied or
+ * padded. The sum over shards is accumulated in fp32 in a fixed order (shards
+ * ascending, k ascending within a shard, split-K pieces ascending), so results
+ * are deterministic and identical to the rows gemm_rs writes.
+ */
+gsr_status gemm_ar(const gemm_shard_plan *plan, int64_t M, int64_t N, int R,
+                   const int64_t *K_r, const void *const *X_r, const void *const *W_r,
+                   void *Y, void *ws, size_t ws_bytes, gsr_stream_t stream);
+
+/*
+ * RS: the AR sum, scattered by rows. With rps = ceil(M / R), shard s receives
+ * global rows [s*rps, min(M, (s+1)*rps)) as rows [0, count_s) of Y_r[s];
+ * Y_r[s] must hold rps rows of N bf16. Rows of Y_r[s] at or past count_s
+ * (the reference's zero-padding rows) are not written. Arguments otherwise as
+ * gemm_ar. Every written element is bit-identical to the same element of
+ * gemm_ar on the same inputs.
+ */
+gsr_status gemm_rs(const gemm_shard_plan *plan, int64_t M, int64_t N, int R,
+                   const int64_t *K_r, const void *const *X_r, const void *const *W_r,
+                   void *const *Y_r, void *ws, size_t ws_bytes, gsr_stream_t stream);
+
+/*
+ * AG: Y = concat_r(A_r) . W^T.
+ *   N      rows of W and columns of Y (multiple of 8)
+ *   K      columns of every A_r and of W (multiple of 8)
+ *   R      number of shards, 1..plan max_R
+ *   M_r    host array of R row counts (>= 0; a shard of 0 rows is skipped)
+ *   A_r    host array of R device pointers, A_r[r] is M_r[r] x K bf16 (ignored
+ *          when M_r[r] == 0)
+ *   W      device pointer, N x K bf16
+ *   Y      device pointer, (sum M_r) x N bf16; shard r's rows start at
+ *          sum_{q<r} M_q. A sum of 0 returns GSR_OK with no launch.
+ */
+gsr_status gemm_ag(const gemm_shard_plan *plan, int64_t N, int64_t K, int R,
+                   const int64_t *M_r, const void *const *A_r, const void *W, void *Y,
+                   void *ws, size_t ws_bytes, gsr_stream_t stream);
+
+/*
+ * Synchronise `stream`, read the workspace status word, clear it and return
+ * GSR_OK or GSR_ERR_TIMEOUT (the code of the first wait that ran out is
+ * available through gsr_last_error_string). After a timeout, re-run
+ * gemm_shard_workspace_init before the next call.
+ */
+gsr_status gemm_shard_check_status(const gemm_shard_plan *plan, void *ws,
+                                   gsr_stream_t stream);
+
+/* Text of the last error on the calling thread ("" if none). Never NULL. */
+const char *gsr_last_error_string(void);
+
+/* Kernel configuration the plan would choose for a call, for logging and
+ * tests: mode 0 = AR, 1 = RS, 2 = AG. AR/RS use M and sizes = K_r (K is
+ * ignored); AG uses K and sizes = M_r (M is ignored). Writes block_n, split
+ * (pieces per output tile), units (work items) and ctas (persistent CTAs).
+ * Any output pointer may be NULL. */
+gsr_status gemm_shard_describe(const gemm_shard_plan *plan, int mode, int64_t M,
+                               int64_t N, int64_t K, int R, const int64_t *sizes,
+                               int *block_n, int *split, int64_t *units, int *ctas);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GSR_H */

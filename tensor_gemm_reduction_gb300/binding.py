@@ -1,0 +1,287 @@
+"""Python binding of the C ABI in ``include/gsr.h``: argument marshalling only.
+
+Every function here has the name of the C entry point it calls. Tensors are
+checked for dtype, device, contiguity and shape, turned into raw pointers and
+passed to the library with the current CUDA stream; all arithmetic runs in the
+library's kernels. There is no fallback: if the library has not been built, the
+first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libgsr.so")
+_lib = None
+
+GSR_OK = 0
+GSR_ERR_INVALID_VALUE = 1
+GSR_ERR_UNSUPPORTED = 2
+GSR_ERR_WORKSPACE = 3
+GSR_ERR_CUDA = 4
+GSR_ERR_TIMEOUT = 5
+GSR_MAX_SHARDS = 16
+
+GSR_OPT_SPLIT_K = 1
+GSR_OPT_BLOCK_N = 2
+GSR_OPT_TIMEOUT_NS = 3
+GSR_OPT_MAX_CTAS = 4
+
+MODE_AR, MODE_RS, MODE_AG = 0, 1, 2
+
+_STATUS_NAMES = {
+    GSR_OK: "GSR_OK",
+    GSR_ERR_INVALID_VALUE: "GSR_ERR_INVALID_VALUE",
+    GSR_ERR_UNSUPPORTED: "GSR_ERR_UNSUPPORTED",
+    GSR_ERR_WORKSPACE: "GSR_ERR_WORKSPACE",
+    GSR_ERR_CUDA: "GSR_ERR_CUDA",
+    GSR_ERR_TIMEOUT: "GSR_ERR_TIMEOUT",
+}
+
+EXPORTED = (
+    "gemm_shard_plan_create", "gemm_shard_plan_create_host", "gemm_shard_plan_destroy", "gemm_shard_plan_set_option",
+    "gemm_shard_workspace_size", "gemm_shard_workspace_init", "gemm_ar", "gemm_rs",
+    "gemm_ag", "gemm_shard_check_status", "gsr_last_error_string", "gemm_shard_describe",
+)
+
+
+class GsrError(RuntimeError):
+    """A non-zero gsr_status, with the library's message."""
+
+    def __init__(self, status: int, message: str):
+        self.status = status
+        super().__init__(f"{_STATUS_NAMES.get(status, status)}: {message}")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library() -> ctypes.CDLL:
+    """Load the built library (raises if it is missing)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError(
+            f"the CUDA library {_LIB_PATH} is not built; run "
+            "`python -m tensor_gemm_reduction_gb300.build` (or __graft_entry__.build())")
+    lib = ctypes.CDLL(_LIB_PATH)
+    vp, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+    ptr_arr = ctypes.POINTER(ctypes.c_void_p)
+    i64_arr = ctypes.POINTER(ctypes.c_int64)
+    lib.gemm_shard_plan_create.argtypes = [ctypes.POINTER(vp), i32, i64, i64, i64, i32]
+    lib.gemm_shard_plan_create_host.argtypes = [ctypes.POINTER(vp), i32, i64, i64, i64, i32]
+    lib.gemm_shard_plan_destroy.argtypes = [vp]
+    lib.gemm_shard_plan_set_option.argtypes = [vp, i32, i64]
+    lib.gemm_shard_workspace_size.argtypes = [vp]
+    lib.gemm_shard_workspace_size.restype = sz
+    lib.gemm_shard_workspace_init.argtypes = [vp, vp, sz, vp]
+    lib.gemm_ar.argtypes = [vp, i64, i64, i32, i64_arr, ptr_arr, ptr_arr, vp, vp, sz, vp]
+    lib.gemm_rs.argtypes = [vp, i64, i64, i32, i64_arr, ptr_arr, ptr_arr, ptr_arr, vp, sz, vp]
+    lib.gemm_ag.argtypes = [vp, i64, i64, i32, i64_arr, ptr_arr, vp, vp, vp, sz, vp]
+    lib.gemm_shard_check_status.argtypes = [vp, vp, vp]
+    lib.gsr_last_error_string.restype = ctypes.c_char_p
+    lib.gemm_shard_describe.argtypes = [vp, i32, i64, i64, i64, i32, i64_arr,
+                                        ctypes.POINTER(i32), ctypes.POINTER(i32),
+                                        ctypes.POINTER(i64), ctypes.POINTER(i32)]
+    for name in EXPORTED:
+        if name not in ("gemm_shard_workspace_size", "gsr_last_error_string"):
+            getattr(lib, name).restype = i32
+    _lib = lib
+    return lib
+
+
+def gsr_last_error_string() -> str:
+    return load_library().gsr_last_error_string().decode()
+
+
+def _check(status: int) -> None:
+    if status != GSR_OK:
+        raise GsrError(status, gsr_last_error_string())
+
+
+class Plan:
+    """Owns a gemm_shard_plan handle; destroyed with the object."""
+
+    def __init__(self, handle: int, device: int, max_M: int, max_N: int, max_K: int, max_R: int):
+        self.handle = ctypes.c_void_p(handle)
+        self.device, self.max_M, self.max_N, self.max_K, self.max_R = device, max_M, max_N, max_K, max_R
+
+    def __del__(self):
+        if getattr(self, "handle", None) and self.handle.value and _lib is not None:
+            _lib.gemm_shard_plan_destroy(self.handle)
+            self.handle = ctypes.c_void_p(0)
+
+
+def gemm_shard_plan_create(device: int, max_M: int, max_N: int, max_K: int, max_R: int) -> Plan:
+    lib = load_library()
+    h = ctypes.c_void_p()
+    _check(lib.gemm_shard_plan_create(ctypes.byref(h), int(device), int(max_M), int(max_N),
+                                      int(max_K), int(max_R)))
+    return Plan(h.value, device, max_M, max_N, max_K, max_R)
+
+
+def gemm_shard_plan_create_host(sm_count: int, max_M: int, max_N: int, max_K: int,
+                                max_R: int) -> Plan:
+    """A plan bound to no device (argument checks, configuration, workspace size)."""
+    lib = load_library()
+    h = ctypes.c_void_p()
+    _check(lib.gemm_shard_plan_create_host(ctypes.byref(h), int(sm_count), int(max_M),
+                                           int(max_N), int(max_K), int(max_R)))
+    return Plan(h.value, -1, max_M, max_N, max_K, max_R)
+
+
+def gemm_shard_plan_destroy(plan: Plan) -> None:
+    if plan.handle.value:
+        _check(load_library().gemm_shard_plan_destroy(plan.handle))
+        plan.handle = ctypes.c_void_p(0)
+
+
+def gemm_shard_plan_set_option(plan: Plan, option: int, value: int) -> None:
+    _check(load_library().gemm_shard_plan_set_option(plan.handle, int(option), int(value)))
+
+
+def gemm_shard_workspace_size(plan: Plan) -> int:
+    return int(load_library().gemm_shard_workspace_size(plan.handle))
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        stream = stream.cuda_stream
+    return ctypes.c_void_p(int(stream))
+
+
+def _ws(ws: torch.Tensor):
+    if not (ws.is_cuda and ws.is_contiguous()):
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    return ctypes.c_void_p(ws.data_ptr()), ws.numel() * ws.element_size()
+
+
+def gemm_shard_workspace_alloc(plan: Plan) -> torch.Tensor:
+    """A workspace tensor of gemm_shard_workspace_size bytes (torch allocates it)."""
+    n = gemm_shard_workspace_size(plan)
+    return torch.empty(n, dtype=torch.uint8, device=f"cuda:{plan.device}")
+
+
+def gemm_shard_workspace_init(plan: Plan, ws: torch.Tensor, stream=None) -> None:
+    p, n = _ws(ws)
+    _check(load_library().gemm_shard_workspace_init(plan.handle, p, n, _stream(stream)))
+
+
+def _bf16_2d(t: torch.Tensor, name: str) -> None:
+    if t.dtype != torch.bfloat16 or not t.is_cuda or t.dim() != 2 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous 2-D bf16 CUDA tensor")
+
+
+def _ptrs(ts: Sequence[Optional[torch.Tensor]]):
+    arr = (ctypes.c_void_p * len(ts))(*[t.data_ptr() if t is not None else 0 for t in ts])
+    return ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p)), arr
+
+
+def _i64s(vals: Sequence[int]):
+    arr = (ctypes.c_int64 * len(vals))(*[int(v) for v in vals])
+    return ctypes.cast(arr, ctypes.POINTER(ctypes.c_int64)), arr
+
+
+def gemm_ar(plan: Plan, X_r: Sequence[torch.Tensor], W_r: Sequence[torch.Tensor],
+            Y: torch.Tensor, ws: torch.Tensor, stream=None) -> torch.Tensor:
+    """Y = sum_r X_r @ W_r.T (X_r: M x K_r, W_r: N x K_r, Y: M x N, all bf16)."""
+    R = len(X_r)
+    if R != len(W_r) or R == 0:
+        raise ValueError("X_r and W_r need the same, non-zero number of shards")
+    for r in range(R):
+        _bf16_2d(X_r[r], f"X_r[{r}]")
+        _bf16_2d(W_r[r], f"W_r[{r}]")
+    _bf16_2d(Y, "Y")
+    M, N = Y.shape
+    K_r = [x.shape[1] for x in X_r]
+    for r in range(R):
+        if X_r[r].shape[0] != M or W_r[r].shape != (N, K_r[r]):
+            raise ValueError(f"shard {r}: X_r must be {M} x K_r and W_r {N} x K_r")
+    k, ka = _i64s(K_r)
+    xp, xa = _ptrs(X_r)
+    wp, wa = _ptrs(W_r)
+    wsp, wsn = _ws(ws)
+    _check(load_library().gemm_ar(plan.handle, M, N, R, k, xp, wp, ctypes.c_void_p(Y.data_ptr()),
+                                  wsp, wsn, _stream(stream)))
+    return Y
+
+
+def gemm_rs(plan: Plan, X_r: Sequence[torch.Tensor], W_r: Sequence[torch.Tensor],
+            Y_r: Sequence[torch.Tensor], ws: torch.Tensor, M: Optional[int] = None,
+            stream=None) -> Sequence[torch.Tensor]:
+    """Y_r[s] = rows [s*rps, min(M,(s+1)*rps)) of sum_r X_r @ W_r.T, rps = ceil(M/R)."""
+    R = len(X_r)
+    if R != len(W_r) or R != len(Y_r) or R == 0:
+        raise ValueError("X_r, W_r and Y_r need the same, non-zero number of shards")
+    for r in range(R):
+        _bf16_2d(X_r[r], f"X_r[{r}]")
+        _bf16_2d(W_r[r], f"W_r[{r}]")
+        _bf16_2d(Y_r[r], f"Y_r[{r}]")
+    M = X_r[0].shape[0] if M is None else int(M)
+    N = W_r[0].shape[0]
+    rps = -(-M // R)
+    K_r = [x.shape[1] for x in X_r]
+    for r in range(R):
+        if X_r[r].shape[0] != M or W_r[r].shape != (N, K_r[r]):
+            raise ValueError(f"shard {r}: X_r must be {M} x K_r and W_r {N} x K_r")
+        if Y_r[r].shape[0] < rps or Y_r[r].shape[1] != N:
+            raise ValueError(f"Y_r[{r}] must hold at least {rps} rows of {N}")
+    k, ka = _i64s(K_r)
+    xp, xa = _ptrs(X_r)
+    wp, wa = _ptrs(W_r)
+    yp, ya = _ptrs(Y_r)
+    wsp, wsn = _ws(ws)
+    _check(load_library().gemm_rs(plan.handle, M, N, R, k, xp, wp, yp, wsp, wsn, _stream(stream)))
+    return Y_r
+
+
+def gemm_ag(plan: Plan, A_r: Sequence[torch.Tensor], W: torch.Tensor, Y: torch.Tensor,
+            ws: torch.Tensor, stream=None) -> torch.Tensor:
+    """Y = cat(A_r) @ W.T (A_r: M_r x K, W: N x K, Y: sum(M_r) x N, all bf16)."""
+    R = len(A_r)
+    if R == 0:
+        raise ValueError("need at least one shard")
+    _bf16_2d(W, "W")
+    _bf16_2d(Y, "Y")
+    N, K = W.shape
+    M_r = []
+    for r, a in enumerate(A_r):
+        if a.numel() == 0:
+            M_r.append(0)
+            continue
+        _bf16_2d(a, f"A_r[{r}]")
+        if a.shape[1] != K:
+            raise ValueError(f"A_r[{r}] must have K={K} columns")
+        M_r.append(a.shape[0])
+    if Y.shape != (sum(M_r), N):
+        raise ValueError(f"Y must be {sum(M_r)} x {N}")
+    m, ma = _i64s(M_r)
+    ap, aa = _ptrs([a if a.numel() else None for a in A_r])
+    wsp, wsn = _ws(ws)
+    _check(load_library().gemm_ag(plan.handle, N, K, R, m, ap, ctypes.c_void_p(W.data_ptr()),
+                                  ctypes.c_void_p(Y.data_ptr()), wsp, wsn, _stream(stream)))
+    return Y
+
+
+def gemm_shard_check_status(plan: Plan, ws: torch.Tensor, stream=None) -> None:
+    p, _ = _ws(ws)
+    _check(load_library().gemm_shard_check_status(plan.handle, p, _stream(stream)))
+
+
+def gemm_shard_describe(plan: Plan, mode: int, M: int, N: int, K: int,
+                        sizes: Sequence[int]) -> dict:
+    lib = load_library()
+    s, sa = _i64s(sizes)
+    bn, sp, ct = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    un = ctypes.c_int64()
+    _check(lib.gemm_shard_describe(plan.handle, int(mode), int(M), int(N), int(K), len(sizes), s,
+                                   ctypes.byref(bn), ctypes.byref(sp), ctypes.byref(un),
+                                   ctypes.byref(ct)))
+    return {"block_n": bn.value, "split": sp.value, "units": un.value, "ctas": ct.value}

@@ -1,0 +1,544 @@
+// gsr_api.cu -- host side of the C ABI declared in include/gsr.h: plans,
+// argument validation, kernel configuration, per-shard TMA descriptors and the
+// launch. Nothing here allocates device memory.
+//
+// The plan mirrors the pages' init_gemm_rs_ar(max_M, N, all_reduce) singleton
+// and its can_run/should_run checks (vLLM PR #53053 summary, model.py and
+// call sites): shape checks happen once per call on the host, before any
+// launch, and failures come back as status codes instead of exceptions that a
+// caller must catch to fall back.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "gsr.h"
+#include "gsr_params.h"
+
+using gsr::BK;
+using gsr::BM;
+using gsr::kMaxShards;
+
+struct gemm_shard_plan {
+  int device;
+  int sm_count;
+  int64_t max_M, max_N, max_K;
+  int max_R;
+  int opt_split;       // 0 = heuristic
+  int opt_block_n;     // 0 = heuristic
+  int opt_max_ctas;    // 0 = one per SM
+  uint64_t timeout_ns;
+};
+
+namespace {
+
+thread_local std::string g_last_error;
+
+gsr_status fail(gsr_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+gsr_status ok() { return GSR_OK; }
+
+gsr_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(GSR_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point, so that the
+// library itself has no link-time dependency on the driver library.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn g_encode = nullptr;
+std::once_flag g_encode_once;
+
+EncodeTiledFn encode_fn() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  });
+  return g_encode;
+}
+
+// Restores the caller's current device on scope exit.
+struct DeviceScope {
+  int prev = -1;
+  bool switched = false;
+  cudaError_t err = cudaSuccess;
+  explicit DeviceScope(int dev) {
+    err = cudaGetDevice(&prev);
+    if (err == cudaSuccess && prev != dev) {
+      err = cudaSetDevice(dev);
+      switched = (err == cudaSuccess);
+    }
+  }
+  ~DeviceScope() {
+    if (switched) cudaSetDevice(prev);
+  }
+};
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Most output tiles any call under the plan can have: block_n = 128, and in AG
+// mode up to one extra partial m-tile per shard.
+int64_t plan_max_tiles(const gemm_shard_plan* P) {
+  return (cdiv(P->max_M, BM) + P->max_R) * cdiv(P->max_N, 128);
+}
+
+// The counter region has a fixed size per plan, so the partials of one call
+// never overlap the counters of another.
+size_t counters_bytes(const gemm_shard_plan* P) {
+  return round256(4 * static_cast<size_t>(plan_max_tiles(P)));
+}
+
+struct Config {
+  int block_n = 256;
+  int splits = 1;
+  int64_t m_tiles = 0, n_tiles = 0, tiles = 0, kb_total = 0, units = 0;
+  int ctas = 0;
+  int group_m = 8;
+  size_t ws_bytes = 0;
+};
+
+// Kernel configuration: a function of the shape (rows, N, per-shard sizes, R)
+// and the device, never of the mode, so AR and RS on the same inputs run the
+// same tiles, the same split and the same summation order (bit-identical rows).
+Config choose_config(const gemm_shard_plan* P, int mode, int64_t M, int64_t N, int64_t K_ag, int R,
+                     const int64_t* sizes) {
+  Config c;
+  c.block_n = P->opt_block_n ? P->opt_block_n : (N <= 128 ? 128 : 256);
+  if (mode == gsr::kModeAG) {
+    for (int r = 0; r < R; ++r) c.m_tiles += cdiv(sizes[r], BM);
+    c.kb_total = cdiv(K_ag, BK);
+  } else {
+    c.m_tiles = cdiv(M, BM);
+    for (int r = 0; r < R; ++r) c.kb_total += cdiv(sizes[r], BK);
+  }
+  c.n_tiles = cdiv(N, c.block_n);
+  c.tiles = c.m_tiles * c.n_tiles;
+  if (P->opt_split) {
+    c.splits = static_cast<int>(std::min<int64_t>(P->opt_split, c.kb_total));
+  } else if (c.tiles >= P->sm_count) {
+    c.splits = 1;
+  } else {
+    // Fewer tiles than SMs (small M): cut each tile's k range into pieces so
+    // that about one piece runs per SM, each at least 4 k-blocks long.
+    int64_t s = P->sm_count / std::max<int64_t>(c.tiles, 1);
+    s = std::min<int64_t>(s, std::max<int64_t>(c.kb_total / 4, 1));
+    s = std::min<int64_t>(s, 16);
+    c.splits = static_cast<int>(std::max<int64_t>(s, 1));
+  }
+  c.units = c.tiles * c.splits;
+  const int cap = P->opt_max_ctas ? std::min(P->opt_max_ctas, P->sm_count) : P->sm_count;
+  c.ctas = static_cast<int>(std::min<int64_t>(c.units, cap));
+  c.group_m = 8;
+  size_t bytes = gsr::kWsHeader + counters_bytes(P);
+  if (c.splits > 1) bytes += static_cast<size_t>(c.units) * BM * c.block_n * sizeof(float);
+  c.ws_bytes = bytes;
+  return c;
+}
+
+CUresult encode_kmajor(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int box_rows) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+gsr_status check_plan(const gemm_shard_plan* P) {
+  if (!P) return fail(GSR_ERR_INVALID_VALUE, "plan is NULL");
+  return ok();
+}
+
+gsr_status check_ws(const Config& c, const void* ws, size_t ws_bytes) {
+  if (!ws) return fail(GSR_ERR_WORKSPACE, "workspace is NULL");
+  if (reinterpret_cast<uintptr_t>(ws) & 255u)
+    return fail(GSR_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  if (ws_bytes < c.ws_bytes)
+    return fail(GSR_ERR_WORKSPACE, "workspace too small: %zu bytes given, %zu needed", ws_bytes,
+                c.ws_bytes);
+  return ok();
+}
+
+void fill_common(gsr::Params& p, const gemm_shard_plan* P, const Config& c, int mode, int R,
+                 int64_t M, int64_t N, void* ws) {
+  p.mode = mode;
+  p.R = R;
+  p.M = static_cast<int>(M);
+  p.N = static_cast<int>(N);
+  p.m_tiles = static_cast<int>(c.m_tiles);
+  p.n_tiles = static_cast<int>(c.n_tiles);
+  p.tiles = static_cast<int>(c.tiles);
+  p.kb_total = static_cast<int>(c.kb_total);
+  p.splits = c.splits;
+  p.units = static_cast<int>(c.units);
+  p.group_m = c.group_m;
+  p.timeout_ns = P->timeout_ns;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  p.status = reinterpret_cast<uint32_t*>(w);
+  p.counters = reinterpret_cast<uint32_t*>(w + gsr::kWsHeader);
+  p.partials = reinterpret_cast<float*>(w + gsr::kWsHeader + counters_bytes(P));
+}
+
+gsr_status launch(const gemm_shard_plan* P, const gsr::Params& p, const Config& c,
+                  gsr_stream_t stream) {
+  if (P->device < 0) return fail(GSR_ERR_UNSUPPORTED, "host plan: arguments are valid, nothing launched");
+  DeviceScope scope(P->device);
+  if (scope.err != cudaSuccess) return cuda_fail(scope.err, "selecting the plan's device");
+  cudaError_t e = gsr::launch_gemm(p, c.block_n, c.ctas, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  return ok();
+}
+
+// Shared validation of the K-sharded (AR/RS) argument lists.
+gsr_status check_ksharded(const gemm_shard_plan* P, int64_t M, int64_t N, int R, const int64_t* K_r,
+                          const void* const* X_r, const void* const* W_r) {
+  if (M < 0) return fail(GSR_ERR_INVALID_VALUE, "M must be >= 0 (got %lld)", (long long)M);
+  if (M > P->max_M)
+    return fail(GSR_ERR_INVALID_VALUE, "M=%lld exceeds the plan's max_M=%lld", (long long)M,
+                (long long)P->max_M);
+  if (N < 8 || N % 8)
+    return fail(GSR_ERR_INVALID_VALUE, "N must be a positive multiple of 8 (got %lld)", (long long)N);
+  if (N > P->max_N)
+    return fail(GSR_ERR_INVALID_VALUE, "N=%lld exceeds the plan's max_N=%lld", (long long)N,
+                (long long)P->max_N);
+  if (R < 1 || R > P->max_R)
+    return fail(GSR_ERR_INVALID_VALUE, "R=%d outside 1..%d", R, P->max_R);
+  if (!K_r || !X_r || !W_r)
+    return fail(GSR_ERR_INVALID_VALUE, "K_r, X_r and W_r must not be NULL");
+  int64_t K = 0;
+  for (int r = 0; r < R; ++r) {
+    if (K_r[r] < 8 || K_r[r] % 8)
+      return fail(GSR_ERR_INVALID_VALUE, "K_r[%d]=%lld must be a positive multiple of 8", r,
+                  (long long)K_r[r]);
+    if (!X_r[r] || !W_r[r])
+      return fail(GSR_ERR_INVALID_VALUE, "shard %d has a NULL operand pointer", r);
+    if (!aligned16(X_r[r]) || !aligned16(W_r[r]))
+      return fail(GSR_ERR_INVALID_VALUE, "shard %d operand is not 16-byte aligned", r);
+    K += K_r[r];
+  }
+  if (K > P->max_K)
+    return fail(GSR_ERR_INVALID_VALUE, "sum of K_r = %lld exceeds the plan's max_K=%lld",
+                (long long)K, (long long)P->max_K);
+  return ok();
+}
+
+gsr_status run_ksharded(const gemm_shard_plan* P, int mode, int64_t M, int64_t N, int R,
+                        const int64_t* K_r, const void* const* X_r, const void* const* W_r,
+                        void* Y, void* const* Y_r, void* ws, size_t ws_bytes,
+                        gsr_stream_t stream) {
+  gsr_status s = check_plan(P);
+  if (s) return s;
+  s = check_ksharded(P, M, N, R, K_r, X_r, W_r);
+  if (s) return s;
+  if (mode == gsr::kModeAR) {
+    if (!Y || !aligned16(Y)) return fail(GSR_ERR_INVALID_VALUE, "Y must be non-NULL and 16-byte aligned");
+  } else {
+    if (!Y_r) return fail(GSR_ERR_INVALID_VALUE, "Y_r must not be NULL");
+    for (int r = 0; r < R; ++r)
+      if (!Y_r[r] || !aligned16(Y_r[r]))
+        return fail(GSR_ERR_INVALID_VALUE, "Y_r[%d] must be non-NULL and 16-byte aligned", r);
+  }
+  const Config c = choose_config(P, mode, M, N, 0, R, K_r);
+  s = check_ws(c, ws, ws_bytes);
+  if (s) return s;
+  if (M == 0) return ok();
+  if (P->device < 0) return fail(GSR_ERR_UNSUPPORTED, "host plan: arguments are valid, nothing launched");
+  if (!encode_fn()) return fail(GSR_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled is unavailable");
+
+  gsr::Params p;
+  std::memset(&p, 0, sizeof p);
+  fill_common(p, P, c, mode, R, M, N, ws);
+  int kb = 0;
+  for (int r = 0; r < R; ++r) {
+    p.shard_kb_begin[r] = kb;
+    kb += static_cast<int>(cdiv(K_r[r], BK));
+    CUresult cr = encode_kmajor(&p.tmap_a[r], X_r[r], M, K_r[r], BM);
+    if (cr != CUDA_SUCCESS) return fail(GSR_ERR_CUDA, "encoding X_r[%d] descriptor failed (%d)", r, (int)cr);
+    cr = encode_kmajor(&p.tmap_b[r], W_r[r], N, K_r[r], c.block_n);
+    if (cr != CUDA_SUCCESS) return fail(GSR_ERR_CUDA, "encoding W_r[%d] descriptor failed (%d)", r, (int)cr);
+  }
+  for (int r = R; r <= kMaxShards; ++r) p.shard_kb_begin[r] = kb;
+  if (mode == gsr::kModeAR) {
+    p.y = static_cast<uint16_t*>(Y);
+  } else {
+    p.rps = static_cast<int>(cdiv(M, R));
+    for (int r = 0; r < R; ++r) p.y_r[r] = static_cast<uint16_t*>(Y_r[r]);
+  }
+  return launch(P, p, c, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* gsr_last_error_string(void) { return g_last_error.c_str(); }
+
+static gsr_status check_maxima(gemm_shard_plan** out, int64_t max_M, int64_t max_N, int64_t max_K,
+                               int max_R) {
+  if (!out) return fail(GSR_ERR_INVALID_VALUE, "out is NULL");
+  *out = nullptr;
+  if (max_M < 1 || max_N < 8 || max_K < 8 || max_N % 8 || max_K % 8)
+    return fail(GSR_ERR_INVALID_VALUE,
+                "maxima must be >= 1 (max_M) or positive multiples of 8 (max_N, max_K)");
+  if (max_M > INT32_MAX - BM || max_N > INT32_MAX - 256 || max_K > INT32_MAX - BK)
+    return fail(GSR_ERR_INVALID_VALUE, "maxima must stay below 2^31");
+  if (max_R < 1 || max_R > kMaxShards)
+    return fail(GSR_ERR_INVALID_VALUE, "max_R=%d outside 1..%d", max_R, kMaxShards);
+  return ok();
+}
+
+static gemm_shard_plan* new_plan(int device, int sm_count, int64_t max_M, int64_t max_N,
+                                 int64_t max_K, int max_R) {
+  gemm_shard_plan* P = new gemm_shard_plan();
+  P->device = device;
+  P->sm_count = sm_count;
+  P->max_M = max_M;
+  P->max_N = max_N;
+  P->max_K = max_K;
+  P->max_R = max_R;
+  P->opt_split = 0;
+  P->opt_block_n = 0;
+  P->opt_max_ctas = 0;
+  P->timeout_ns = 2000000000ull;
+  return P;
+}
+
+gsr_status gemm_shard_plan_create_host(gemm_shard_plan** out, int sm_count, int64_t max_M,
+                                       int64_t max_N, int64_t max_K, int max_R) {
+  gsr_status s = check_maxima(out, max_M, max_N, max_K, max_R);
+  if (s) return s;
+  if (sm_count < 1) return fail(GSR_ERR_INVALID_VALUE, "sm_count must be >= 1");
+  *out = new_plan(-1, sm_count, max_M, max_N, max_K, max_R);
+  return ok();
+}
+
+gsr_status gemm_shard_plan_create(gemm_shard_plan** out, int device, int64_t max_M, int64_t max_N,
+                                  int64_t max_K, int max_R) {
+  gsr_status s = check_maxima(out, max_M, max_N, max_K, max_R);
+  if (s) return s;
+  int count = 0;
+  cudaError_t e = cudaGetDeviceCount(&count);
+  if (e != cudaSuccess) return fail(GSR_ERR_UNSUPPORTED, "no usable CUDA device: %s", cudaGetErrorString(e));
+  if (device < 0 || device >= count)
+    return fail(GSR_ERR_INVALID_VALUE, "device %d outside 0..%d", device, count - 1);
+  cudaDeviceProp prop;
+  e = cudaGetDeviceProperties(&prop, device);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceProperties");
+  if (prop.major != 10 || prop.minor != 3)
+    return fail(GSR_ERR_UNSUPPORTED, "device %d is compute capability %d.%d; this library is built for sm_103a",
+                device, prop.major, prop.minor);
+  if (!encode_fn()) return fail(GSR_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled is unavailable");
+  {
+    DeviceScope scope(device);
+    if (scope.err != cudaSuccess) return cuda_fail(scope.err, "cudaSetDevice");
+    if (static_cast<size_t>(prop.sharedMemPerBlockOptin) < gsr::kernel_smem_bytes(256))
+      return fail(GSR_ERR_UNSUPPORTED, "device allows %zu bytes of shared memory per block; %zu needed",
+                  static_cast<size_t>(prop.sharedMemPerBlockOptin), gsr::kernel_smem_bytes(256));
+    e = gsr::prepare_kernels(device);
+    if (e != cudaSuccess) return cuda_fail(e, "configuring the kernels");
+  }
+  *out = new_plan(device, prop.multiProcessorCount, max_M, max_N, max_K, max_R);
+  return ok();
+}
+
+gsr_status gemm_shard_plan_destroy(gemm_shard_plan* plan) {
+  delete plan;
+  return ok();
+}
+
+gsr_status gemm_shard_plan_set_option(gemm_shard_plan* plan, gsr_option option, int64_t value) {
+  gsr_status s = check_plan(plan);
+  if (s) return s;
+  switch (option) {
+    case GSR_OPT_SPLIT_K:
+      if (value < 0 || value > 16) return fail(GSR_ERR_INVALID_VALUE, "split must be 0..16");
+      plan->opt_split = static_cast<int>(value);
+      return ok();
+    case GSR_OPT_BLOCK_N:
+      if (value != 0 && value != 128 && value != 256)
+        return fail(GSR_ERR_INVALID_VALUE, "block_n must be 0, 128 or 256");
+      plan->opt_block_n = static_cast<int>(value);
+      return ok();
+    case GSR_OPT_TIMEOUT_NS:
+      if (value < 0) return fail(GSR_ERR_INVALID_VALUE, "timeout must be >= 0");
+      plan->timeout_ns = value ? static_cast<uint64_t>(value) : 2000000000ull;
+      return ok();
+    case GSR_OPT_MAX_CTAS:
+      if (value < 0 || value > INT32_MAX) return fail(GSR_ERR_INVALID_VALUE, "max_ctas must be >= 0");
+      plan->opt_max_ctas = static_cast<int>(value);
+      return ok();
+  }
+  return fail(GSR_ERR_INVALID_VALUE, "unknown option %d", static_cast<int>(option));
+}
+
+size_t gemm_shard_workspace_size(const gemm_shard_plan* P) {
+  if (!P) return 0;
+  // Worst case over every shape within the plan: most tiles at block_n = 128
+  // (AG adds up to one partial m-tile per shard), and split-K partials for the
+  // heuristic (pieces only while tiles < SMs, so at most one slot per SM) or
+  // for a forced split on every tile.
+  const int64_t max_tiles = plan_max_tiles(P);
+  size_t bytes = gsr::kWsHeader + counters_bytes(P);
+  const size_t slot = static_cast<size_t>(BM) * 256 * sizeof(float);
+  if (P->opt_split > 1)
+    bytes += static_cast<size_t>(max_tiles) * P->opt_split * slot;
+  else
+    bytes += static_cast<size_t>(P->sm_count) * slot;
+  return bytes;
+}
+
+gsr_status gemm_shard_workspace_init(const gemm_shard_plan* P, void* ws, size_t ws_bytes,
+                                     gsr_stream_t stream) {
+  gsr_status s = check_plan(P);
+  if (s) return s;
+  if (!ws) return fail(GSR_ERR_WORKSPACE, "workspace is NULL");
+  if (reinterpret_cast<uintptr_t>(ws) & 255u)
+    return fail(GSR_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  const size_t zero_bytes = gsr::kWsHeader + counters_bytes(P);
+  if (ws_bytes < zero_bytes)
+    return fail(GSR_ERR_WORKSPACE, "workspace too small: %zu bytes given, at least %zu needed",
+                ws_bytes, zero_bytes);
+  if (P->device < 0) return fail(GSR_ERR_UNSUPPORTED, "host plan: nothing to initialise");
+  DeviceScope scope(P->device);
+  if (scope.err != cudaSuccess) return cuda_fail(scope.err, "selecting the plan's device");
+  cudaError_t e = cudaMemsetAsync(ws, 0, zero_bytes, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+  return ok();
+}
+
+gsr_status gemm_ar(const gemm_shard_plan* plan, int64_t M, int64_t N, int R, const int64_t* K_r,
+                   const void* const* X_r, const void* const* W_r, void* Y, void* ws,
+                   size_t ws_bytes, gsr_stream_t stream) {
+  return run_ksharded(plan, gsr::kModeAR, M, N, R, K_r, X_r, W_r, Y, nullptr, ws, ws_bytes, stream);
+}
+
+gsr_status gemm_rs(const gemm_shard_plan* plan, int64_t M, int64_t N, int R, const int64_t* K_r,
+                   const void* const* X_r, const void* const* W_r, void* const* Y_r, void* ws,
+                   size_t ws_bytes, gsr_stream_t stream) {
+  return run_ksharded(plan, gsr::kModeRS, M, N, R, K_r, X_r, W_r, nullptr, Y_r, ws, ws_bytes,
+                      stream);
+}
+
+gsr_status gemm_ag(const gemm_shard_plan* P, int64_t N, int64_t K, int R, const int64_t* M_r,
+                   const void* const* A_r, const void* W, void* Y, void* ws, size_t ws_bytes,
+                   gsr_stream_t stream) {
+  gsr_status s = check_plan(P);
+  if (s) return s;
+  if (N < 8 || N % 8)
+    return fail(GSR_ERR_INVALID_VALUE, "N must be a positive multiple of 8 (got %lld)", (long long)N);
+  if (N > P->max_N)
+    return fail(GSR_ERR_INVALID_VALUE, "N=%lld exceeds the plan's max_N=%lld", (long long)N,
+                (long long)P->max_N);
+  if (K < 8 || K % 8)
+    return fail(GSR_ERR_INVALID_VALUE, "K must be a positive multiple of 8 (got %lld)", (long long)K);
+  if (K > P->max_K)
+    return fail(GSR_ERR_INVALID_VALUE, "K=%lld exceeds the plan's max_K=%lld", (long long)K,
+                (long long)P->max_K);
+  if (R < 1 || R > P->max_R) return fail(GSR_ERR_INVALID_VALUE, "R=%d outside 1..%d", R, P->max_R);
+  if (!M_r || !A_r) return fail(GSR_ERR_INVALID_VALUE, "M_r and A_r must not be NULL");
+  if (!W || !aligned16(W)) return fail(GSR_ERR_INVALID_VALUE, "W must be non-NULL and 16-byte aligned");
+  if (!Y || !aligned16(Y)) return fail(GSR_ERR_INVALID_VALUE, "Y must be non-NULL and 16-byte aligned");
+  int64_t M = 0;
+  for (int r = 0; r < R; ++r) {
+    if (M_r[r] < 0) return fail(GSR_ERR_INVALID_VALUE, "M_r[%d] must be >= 0", r);
+    if (M_r[r] > 0 && (!A_r[r] || !aligned16(A_r[r])))
+      return fail(GSR_ERR_INVALID_VALUE, "A_r[%d] must be non-NULL and 16-byte aligned", r);
+    M += M_r[r];
+  }
+  if (M > P->max_M)
+    return fail(GSR_ERR_INVALID_VALUE, "sum of M_r = %lld exceeds the plan's max_M=%lld",
+                (long long)M, (long long)P->max_M);
+  const Config c = choose_config(P, gsr::kModeAG, M, N, K, R, M_r);
+  s = check_ws(c, ws, ws_bytes);
+  if (s) return s;
+  if (M == 0) return ok();
+  if (P->device < 0) return fail(GSR_ERR_UNSUPPORTED, "host plan: arguments are valid, nothing launched");
+  if (!encode_fn()) return fail(GSR_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled is unavailable");
+
+  gsr::Params p;
+  std::memset(&p, 0, sizeof p);
+  fill_common(p, P, c, gsr::kModeAG, R, M, N, ws);
+  int mt = 0, row = 0;
+  for (int r = 0; r < R; ++r) {
+    p.shard_mt_begin[r] = mt;
+    p.shard_row_begin[r] = row;
+    p.shard_rows[r] = static_cast<int>(M_r[r]);
+    mt += static_cast<int>(cdiv(M_r[r], BM));
+    row += static_cast<int>(M_r[r]);
+    if (M_r[r] > 0) {
+      CUresult cr = encode_kmajor(&p.tmap_a[r], A_r[r], M_r[r], K, BM);
+      if (cr != CUDA_SUCCESS) return fail(GSR_ERR_CUDA, "encoding A_r[%d] descriptor failed (%d)", r, (int)cr);
+    }
+  }
+  for (int r = R; r <= kMaxShards; ++r) {
+    p.shard_mt_begin[r] = mt;
+    p.shard_row_begin[r] = row;
+  }
+  CUresult cr = encode_kmajor(&p.tmap_b[0], W, N, K, c.block_n);
+  if (cr != CUDA_SUCCESS) return fail(GSR_ERR_CUDA, "encoding the W descriptor failed (%d)", (int)cr);
+  p.y = static_cast<uint16_t*>(Y);
+  return launch(P, p, c, stream);
+}
+
+gsr_status gemm_shard_check_status(const gemm_shard_plan* P, void* ws, gsr_stream_t stream) {
+  gsr_status s = check_plan(P);
+  if (s) return s;
+  if (!ws) return fail(GSR_ERR_WORKSPACE, "workspace is NULL");
+  if (P->device < 0) return fail(GSR_ERR_UNSUPPORTED, "host plan: no device status to read");
+  DeviceScope scope(P->device);
+  if (scope.err != cudaSuccess) return cuda_fail(scope.err, "selecting the plan's device");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t word = 0;
+  cudaError_t e = cudaMemcpyAsync(&word, ws, sizeof word, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the workspace status word");
+  if (word == 0) return ok();
+  e = cudaMemsetAsync(ws, 0, sizeof word, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "clearing the workspace status word");
+  return fail(GSR_ERR_TIMEOUT, "in-kernel wait ran out (code 0x%08x: role %u, site %u)", word,
+              (word >> 8) & 0xFFu, word & 0xFFu);
+}
+
+gsr_status gemm_shard_describe(const gemm_shard_plan* P, int mode, int64_t M, int64_t N, int64_t K,
+                               int R, const int64_t* sizes, int* block_n, int* split,
+                               int64_t* units, int* ctas) {
+  gsr_status s = check_plan(P);
+  if (s) return s;
+  if (mode < 0 || mode > 2) return fail(GSR_ERR_INVALID_VALUE, "mode must be 0, 1 or 2");
+  if (R < 1 || R > kMaxShards || !sizes) return fail(GSR_ERR_INVALID_VALUE, "bad R or sizes");
+  if (N < 8 || N % 8) return fail(GSR_ERR_INVALID_VALUE, "N must be a positive multiple of 8");
+  const Config c = choose_config(P, mode, M, N, K, R, sizes);
+  if (block_n) *block_n = c.block_n;
+  if (split) *split = c.splits;
+  if (units) *units = c.units;
+  if (ctas) *ctas = c.ctas;
+  return ok();
+}
+
+}  // extern "C"

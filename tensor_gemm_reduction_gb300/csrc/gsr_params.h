@@ -1,0 +1,63 @@
+// gsr_params.h -- launch parameters of the shard-reduction GEMM kernel
+// (internal to the library; not part of the C ABI).
+#pragma once
+
+#include <cuda.h>
+#include <stdint.h>
+
+namespace gsr {
+
+constexpr int kMaxShards = 16;
+constexpr int BM = 128;          // output tile rows = tcgen05 MMA M (cta_group::1)
+constexpr int BK = 64;           // k-block: 64 bf16 = one 128-byte swizzle row
+constexpr int kThreads = 192;    // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+constexpr int kEpilogueThreads = 128;
+
+enum Mode : int { kModeAR = 0, kModeRS = 1, kModeAG = 2 };
+
+// Status word codes written by the kernel (workspace offset 0). 0 = OK.
+// A timed-out wait stores kStatusTimeout | (role << 8) | site.
+constexpr uint32_t kStatusTimeout = 0x54000000u;
+
+// Workspace layout (bytes): [0, 256) header (status word at 0);
+// [256, 256 + 4*counter_slots) per-tile arrival counters, rounded up to 256;
+// then fp32 split-K partial tiles of BM x BN each.
+constexpr size_t kWsHeader = 256;
+
+struct Params {  // 128-byte aligned through its CUtensorMap members
+  // Per-shard TMA descriptors. AR/RS: tmap_a[r] = X_r (box 64 x 128),
+  // tmap_b[r] = W_r (box 64 x BN). AG: tmap_a[r] = A_r, tmap_b[0] = W.
+  CUtensorMap tmap_a[kMaxShards];
+  CUtensorMap tmap_b[kMaxShards];
+
+  uint16_t* y;                  // AR, AG: output rows x N (bf16 bits)
+  uint16_t* y_r[kMaxShards];    // RS: shard outputs, rps x N each
+  uint32_t* status;             // workspace status word
+  uint32_t* counters;           // workspace per-tile arrival counters
+  float* partials;              // workspace split-K partial tiles
+  uint64_t timeout_ns;          // limit of every bounded wait
+
+  int mode;
+  int R;
+  int M;                        // AR/RS: rows; AG: sum of M_r
+  int N;
+  int m_tiles;                  // AR/RS: ceil(M/BM); AG: sum_r ceil(M_r/BM)
+  int n_tiles;                  // ceil(N/BN)
+  int tiles;                    // m_tiles * n_tiles
+  int kb_total;                 // k-blocks per tile (AR/RS: sum_r ceil(K_r/BK))
+  int splits;                   // pieces per tile (1 = no split-K)
+  int units;                    // tiles * splits
+  int group_m;                  // raster group height, in m-tiles
+  int rps;                      // RS: rows per shard = ceil(M/R)
+  int shard_kb_begin[kMaxShards + 1];  // AR/RS: first k-block of shard r
+  int shard_mt_begin[kMaxShards + 1];  // AG: first m-tile of shard r
+  int shard_row_begin[kMaxShards + 1]; // AG: first output row of shard r
+  int shard_rows[kMaxShards];          // AG: M_r
+};
+
+// Host-side launcher (defined with the kernel).
+cudaError_t launch_gemm(const Params& p, int block_n, int ctas, cudaStream_t stream);
+cudaError_t prepare_kernels(int device);
+size_t kernel_smem_bytes(int block_n);
+
+}  // namespace gsr

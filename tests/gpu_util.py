@@ -1,0 +1,90 @@
+"""Helpers shared by the GPU tests: plans, guarded output buffers and the
+element-wise parity check against the oracle."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from tensor_gemm_reduction_gb300 import binding as B
+from tensor_gemm_reduction_gb300 import build as gbuild
+
+# Per-element bound of the parity check: |y - ref| <= RTOL * |ref| + ATOL.
+RTOL = 1e-2
+ATOL = 1e-2
+SENTINEL = 0x7FC1          # a bf16 NaN pattern no computation produces here
+GUARD_ROWS = 2
+
+
+def device() -> torch.device:
+    return torch.device("cuda:0")
+
+
+_PLANS = {}
+
+
+def plan(max_M=34816, max_N=8192, max_K=8192, max_R=16, **options):
+    """A cached plan + initialised workspace for the given maxima and options."""
+    key = (max_M, max_N, max_K, max_R, tuple(sorted(options.items())))
+    if key not in _PLANS:
+        gbuild.build()
+        p = B.gemm_shard_plan_create(0, max_M, max_N, max_K, max_R)
+        for name, value in options.items():
+            B.gemm_shard_plan_set_option(p, getattr(B, f"GSR_OPT_{name.upper()}"), value)
+        ws = B.gemm_shard_workspace_alloc(p)
+        B.gemm_shard_workspace_init(p, ws)
+        _PLANS[key] = (p, ws)
+    return _PLANS[key]
+
+
+class Guarded:
+    """A rows x N bf16 output with GUARD_ROWS sentinel rows before and after."""
+
+    def __init__(self, rows: int, N: int, dev=None):
+        dev = dev or device()
+        self.rows, self.N = rows, N
+        self.full = torch.full((rows + 2 * GUARD_ROWS, N), 0, dtype=torch.int16, device=dev)
+        self.full.fill_(SENTINEL)
+        self.full = self.full.view(torch.bfloat16)
+        self.out = self.full[GUARD_ROWS:GUARD_ROWS + rows]
+
+    def bits(self) -> np.ndarray:
+        return self.full.view(torch.int16).cpu().numpy().view(np.uint16)
+
+    def guards_intact(self, valid_rows: int | None = None) -> bool:
+        b = self.bits()
+        v = self.rows if valid_rows is None else valid_rows
+        pre = b[:GUARD_ROWS]
+        post = b[GUARD_ROWS + v:]
+        return bool((pre == SENTINEL).all() and (post == SENTINEL).all())
+
+
+def to_f64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().to(torch.float64).cpu().numpy()
+
+
+def assert_close(y: np.ndarray, ref: np.ndarray, what: str = "") -> None:
+    assert y.shape == ref.shape, (y.shape, ref.shape)
+    assert np.isfinite(y).all(), f"{what}: non-finite output"
+    err = np.abs(y - ref)
+    bound = RTOL * np.abs(ref) + ATOL
+    bad = err > bound
+    assert not bad.any(), (
+        f"{what}: {int(bad.sum())} of {bad.size} elements out of bound; "
+        f"max abs err {err.max():.4g}, max rel err {(err / (np.abs(ref) + 1e-30)).max():.4g}")
+
+
+def shards_to(dev, tensors, reverse_order=False):
+    """Copy shards to the device, each in its own allocation (optionally in reverse
+    allocation order, with spacer allocations in between)."""
+    out = [None] * len(tensors)
+    spacers = []
+    order = range(len(tensors) - 1, -1, -1) if reverse_order else range(len(tensors))
+    for i in order:
+        out[i] = tensors[i].to(dev).contiguous()
+        if reverse_order:
+            spacers.append(torch.empty(4096 + 512 * i, dtype=torch.uint8, device=dev))
+    return out, spacers
+
+
+def bits_of(t: torch.Tensor) -> np.ndarray:
+    return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)

@@ -1,0 +1,240 @@
+"""C-ABI checks that need no GPU: the library loads, exports every entry point
+the header declares, and its host logic (argument validation, workspace sizing,
+kernel configuration) behaves as documented. Calls go straight through ctypes
+with made-up device addresses; a host plan never dereferences them."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from tensor_gemm_reduction_gb300 import binding as B
+from tensor_gemm_reduction_gb300 import build as gbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    gbuild.build()
+    return B.load_library()
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "gsr.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*([a-z_][a-z0-9_]*)\s*\(",
+                       text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = header_functions()
+    for n in ("gemm_shard_plan_create", "gemm_shard_plan_destroy", "gemm_ar", "gemm_rs", "gemm_ag",
+              "gemm_shard_workspace_size", "gemm_shard_check_status", "gsr_last_error_string"):
+        assert n in names
+    assert sorted(names) == sorted(B.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in header_functions():
+        assert hasattr(lib, n), f"{n} declared in gsr.h but not exported"
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU path")
+def test_device_plan_without_gpu_is_unsupported(lib):
+    h = ctypes.c_void_p(123)
+    st = lib.gemm_shard_plan_create(ctypes.byref(h), 0, 128, 256, 256, 2)
+    assert st == B.GSR_ERR_UNSUPPORTED
+    assert h.value is None
+    assert B.gsr_last_error_string()
+
+
+def test_null_plan_is_rejected(lib):
+    assert lib.gemm_shard_workspace_size(None) == 0
+    assert lib.gemm_shard_plan_set_option(None, B.GSR_OPT_SPLIT_K, 2) == B.GSR_ERR_INVALID_VALUE
+    assert "NULL" in B.gsr_last_error_string()
+    assert lib.gemm_shard_plan_destroy(None) == B.GSR_OK
+
+
+@pytest.mark.parametrize("args", [
+    (0, 128, 256, 256, 2),      # sm_count
+    (148, 0, 256, 256, 2),      # max_M
+    (148, 128, 250, 256, 2),    # max_N not a multiple of 8
+    (148, 128, 256, 12, 2),     # max_K not a multiple of 8
+    (148, 128, 256, 256, 0),    # max_R
+    (148, 128, 256, 256, 17),   # max_R > 16
+])
+def test_host_plan_rejects_bad_maxima(lib, args):
+    h = ctypes.c_void_p()
+    assert lib.gemm_shard_plan_create_host(ctypes.byref(h), *args) == B.GSR_ERR_INVALID_VALUE
+    assert h.value is None
+
+
+def _arr(ctype, vals):
+    return (ctype * len(vals))(*vals)
+
+
+class Host:
+    """A host plan plus raw-pointer call helpers."""
+
+    def __init__(self, lib, sm=148, max_M=32768, max_N=8192, max_K=8192, max_R=16):
+        self.lib = lib
+        self.plan = B.gemm_shard_plan_create_host(sm, max_M, max_N, max_K, max_R)
+        self.ws_bytes = B.gemm_shard_workspace_size(self.plan)
+
+    def ar(self, M, N, K_r, x=None, w=None, y=0x10000, ws=0x20000000, ws_bytes=None, mode="ar"):
+        R = len(K_r)
+        x = x if x is not None else [0x100000 * (r + 1) for r in range(R)]
+        w = w if w is not None else [0x100000 * (r + 1) + 0x80000 for r in range(R)]
+        ws_bytes = self.ws_bytes if ws_bytes is None else ws_bytes
+        k = _arr(ctypes.c_int64, K_r)
+        xa = _arr(ctypes.c_void_p, x)
+        wa = _arr(ctypes.c_void_p, w)
+        if mode == "ar":
+            return self.lib.gemm_ar(self.plan.handle, M, N, R, k, xa, wa, ctypes.c_void_p(y),
+                                    ctypes.c_void_p(ws), ws_bytes, None)
+        ya = _arr(ctypes.c_void_p, y if isinstance(y, list) else [y + 0x1000 * r for r in range(R)])
+        return self.lib.gemm_rs(self.plan.handle, M, N, R, k, xa, wa, ya, ctypes.c_void_p(ws),
+                                ws_bytes, None)
+
+    def ag(self, N, K, M_r, a=None, w=0x700000, y=0x10000, ws=0x20000000, ws_bytes=None):
+        R = len(M_r)
+        a = a if a is not None else [0x100000 * (r + 1) for r in range(R)]
+        ws_bytes = self.ws_bytes if ws_bytes is None else ws_bytes
+        return self.lib.gemm_ag(self.plan.handle, N, K, R, _arr(ctypes.c_int64, M_r),
+                                _arr(ctypes.c_void_p, a), ctypes.c_void_p(w), ctypes.c_void_p(y),
+                                ctypes.c_void_p(ws), ws_bytes, None)
+
+    def describe(self, mode, M, N, K, sizes):
+        return B.gemm_shard_describe(self.plan, mode, M, N, K, sizes)
+
+
+@pytest.fixture()
+def host(lib):
+    return Host(lib)
+
+
+def test_valid_calls_reach_the_launch_point(host):
+    assert host.ar(128, 7168, [896] * 8) == B.GSR_ERR_UNSUPPORTED
+    assert "arguments are valid" in B.gsr_last_error_string()
+    assert host.ar(129, 7168, [896] * 8, mode="rs") == B.GSR_ERR_UNSUPPORTED
+    assert host.ag(6288, 7168, [4096] * 8) == B.GSR_ERR_UNSUPPORTED
+
+
+def test_empty_problems_return_ok_without_launch(host):
+    assert host.ar(0, 256, [128, 128]) == B.GSR_OK
+    assert host.ar(0, 256, [128, 128], mode="rs") == B.GSR_OK
+    assert host.ag(256, 128, [0, 0, 0]) == B.GSR_OK
+
+
+@pytest.mark.parametrize("kw,frag", [
+    (dict(M=-1, N=256, K_r=[128]), "M must be"),
+    (dict(M=40000, N=256, K_r=[128]), "max_M"),
+    (dict(M=16, N=12, K_r=[128]), "multiple of 8"),
+    (dict(M=16, N=0, K_r=[128]), "multiple of 8"),
+    (dict(M=16, N=8200, K_r=[128]), "max_N"),
+    (dict(M=16, N=256, K_r=[]), "R=0"),
+    (dict(M=16, N=256, K_r=[8] * 17), "R=17"),
+    (dict(M=16, N=256, K_r=[128, 20]), "K_r[1]"),
+    (dict(M=16, N=256, K_r=[128, 0]), "K_r[1]"),
+    (dict(M=16, N=256, K_r=[4096, 4104]), "max_K"),
+    (dict(M=16, N=256, K_r=[128, 128], x=[0x100000, 0x100008]), "16-byte"),
+    (dict(M=16, N=256, K_r=[128, 128], w=[0x100000, 0]), "NULL"),
+    (dict(M=16, N=256, K_r=[128], y=0x10004), "16-byte"),
+    (dict(M=16, N=256, K_r=[128], y=0), "Y must"),
+])
+def test_ar_argument_validation(host, kw, frag):
+    assert host.ar(**kw) == B.GSR_ERR_INVALID_VALUE
+    assert frag in B.gsr_last_error_string()
+
+
+def test_rs_output_validation(host):
+    assert host.ar(16, 256, [128, 128], y=[0x10000, 0x10008], mode="rs") == B.GSR_ERR_INVALID_VALUE
+    assert host.ar(16, 256, [128, 128], y=[0x10000, 0], mode="rs") == B.GSR_ERR_INVALID_VALUE
+
+
+@pytest.mark.parametrize("kw,frag", [
+    (dict(N=256, K=100, M_r=[16]), "K must"),
+    (dict(N=256, K=9000, M_r=[16]), "max_K"),
+    (dict(N=252, K=128, M_r=[16]), "N must"),
+    (dict(N=256, K=128, M_r=[16, -1]), "M_r[1]"),
+    (dict(N=256, K=128, M_r=[16, 16], a=[0x100000, 0]), "A_r[1]"),
+    (dict(N=256, K=128, M_r=[16], w=0x700008), "W must"),
+    (dict(N=256, K=128, M_r=[20000, 20000]), "max_M"),
+])
+def test_ag_argument_validation(host, kw, frag):
+    assert host.ag(**kw) == B.GSR_ERR_INVALID_VALUE
+    assert frag in B.gsr_last_error_string()
+
+
+def test_ag_null_pointer_allowed_for_empty_shard(host):
+    assert host.ag(256, 128, [16, 0, 8], a=[0x100000, 0, 0x300000]) == B.GSR_ERR_UNSUPPORTED
+
+
+def test_workspace_checks(host):
+    assert host.ar(128, 7168, [896] * 8, ws=0) == B.GSR_ERR_WORKSPACE
+    assert host.ar(128, 7168, [896] * 8, ws=0x20000080) == B.GSR_ERR_WORKSPACE
+    assert "256-byte" in B.gsr_last_error_string()
+    assert host.ar(128, 7168, [896] * 8, ws_bytes=1024) == B.GSR_ERR_WORKSPACE
+    assert "too small" in B.gsr_last_error_string()
+
+
+def test_workspace_size_covers_every_heuristic_config(host):
+    # The plan's bound must cover the per-call requirement of every shape.
+    sizes = []
+    for M in (1, 7, 127, 128, 129, 257, 1000, 4096, 32768):
+        for N in (8, 136, 3648, 6288, 7168, 8192):
+            for K_r in ([896] * 8, [8], [4096, 4096], [448] * 16):
+                d = host.describe(B.MODE_AR, M, N, 0, K_r)
+                need = 256 + 4 * 0 + (d["units"] * 128 * d["block_n"] * 4 if d["split"] > 1 else 0)
+                sizes.append(need)
+                assert need <= host.ws_bytes
+                assert host.ar(M, N, K_r) == B.GSR_ERR_UNSUPPORTED, B.gsr_last_error_string()
+
+
+def test_config_is_independent_of_mode(host):
+    for M in (1, 128, 129, 1000, 4096, 32768):
+        for K_r in ([896] * 8, [3584] * 2, [448] * 16, [8, 72, 136]):
+            a = host.describe(B.MODE_AR, M, 7168, 0, K_r)
+            r = host.describe(B.MODE_RS, M, 7168, 0, K_r)
+            assert a == r
+
+
+def test_small_m_uses_split_k(host):
+    d = host.describe(B.MODE_AR, 128, 7168, 0, [896] * 8)
+    # 1 x 28 tiles of 128 x 256 on 148 SMs -> 5 pieces per tile, one wave
+    assert d == {"block_n": 256, "split": 5, "units": 140, "ctas": 140}
+    d = host.describe(B.MODE_AR, 32768, 7168, 0, [896] * 8)
+    assert d["split"] == 1 and d["units"] == 256 * 28 and d["ctas"] == 148
+    d = host.describe(B.MODE_AG, 0, 6288, 7168, [4096] * 8)
+    assert d["split"] == 1 and d["units"] == 8 * 32 * 25
+
+
+def test_forced_options(lib):
+    h = Host(lib, max_M=4096, max_N=1024, max_K=1024, max_R=4)
+    base = h.ws_bytes
+    B.gemm_shard_plan_set_option(h.plan, B.GSR_OPT_SPLIT_K, 3)
+    B.gemm_shard_plan_set_option(h.plan, B.GSR_OPT_BLOCK_N, 128)
+    assert B.gemm_shard_workspace_size(h.plan) > base
+    d = h.describe(B.MODE_AR, 1000, 1024, 0, [256, 256])
+    assert d["split"] == 3 and d["block_n"] == 128 and d["units"] == 8 * 8 * 3
+    # a forced split never exceeds the number of k-blocks
+    d = h.describe(B.MODE_AR, 64, 256, 0, [64])
+    assert d["split"] == 1
+    for opt, bad in ((B.GSR_OPT_SPLIT_K, 17), (B.GSR_OPT_BLOCK_N, 64), (B.GSR_OPT_TIMEOUT_NS, -1),
+                     (B.GSR_OPT_MAX_CTAS, -5), (99, 1)):
+        with pytest.raises(B.GsrError) as e:
+            B.gemm_shard_plan_set_option(h.plan, opt, bad)
+        assert e.value.status == B.GSR_ERR_INVALID_VALUE
+    B.gemm_shard_plan_set_option(h.plan, B.GSR_OPT_MAX_CTAS, 10)
+    assert h.describe(B.MODE_AR, 4096, 1024, 0, [256])["ctas"] == 10
+
+
+def test_host_plan_has_no_device_status(host):
+    with pytest.raises(B.GsrError) as e:
+        B.load_library()
+        st = host.lib.gemm_shard_check_status(host.plan.handle, ctypes.c_void_p(0x20000000), None)
+        B._check(st)
+    assert e.value.status == B.GSR_ERR_UNSUPPORTED

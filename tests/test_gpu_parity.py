@@ -1,0 +1,241 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle, element
+by element on the same seeded inputs, at sizes the oracle finishes in seconds
+that still span several tiles and ragged tails. Bound per element:
+|y - ref| <= 1e-2 |ref| + 1e-2 (fp32 accumulation, one bf16 rounding)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tensor_gemm_reduction_gb300 import binding as B
+from tensor_gemm_reduction_gb300 import inputs as gi
+
+from gpu_util import (Guarded, assert_close, bits_of, device, plan, shards_to, to_f64,
+                      SENTINEL)
+
+pytestmark = pytest.mark.gpu
+
+
+def run_ar(inp, p=None, reverse=False):
+    p, ws = p or plan()
+    dev = device()
+    X, s1 = shards_to(dev, inp.X_r, reverse)
+    W, s2 = shards_to(dev, inp.W_r, reverse)
+    Y = Guarded(inp.M, inp.N)
+    B.gemm_ar(p, X, W, Y.out, ws)
+    B.gemm_shard_check_status(p, ws)
+    return Y, X, W
+
+
+def run_rs(inp, p=None):
+    p, ws = p or plan()
+    dev = device()
+    X, _ = shards_to(dev, inp.X_r)
+    W, _ = shards_to(dev, inp.W_r)
+    R = inp.R
+    rps = -(-inp.M // R)
+    Ys = [Guarded(rps, inp.N) for _ in range(R)]
+    B.gemm_rs(p, X, W, [y.out for y in Ys], ws, M=inp.M)
+    B.gemm_shard_check_status(p, ws)
+    return Ys
+
+
+def run_ag(inp, p=None, reverse=False):
+    p, ws = p or plan()
+    dev = device()
+    A, s1 = shards_to(dev, inp.A_r, reverse)
+    W = inp.W.to(dev)
+    Y = Guarded(inp.M, inp.N)
+    B.gemm_ag(p, A, W, Y.out, ws)
+    B.gemm_shard_check_status(p, ws)
+    return Y
+
+
+# ------------------------------------------------------------------ AR
+
+def test_ar_tiny_config():
+    """AR, R=2 shards of K=128, M=128, N=256, seed 0."""
+    w = gi.AR_TINY
+    inp = gi.make_inputs(w)
+    Y, _, _ = run_ar(inp)
+    assert_close(to_f64(Y.out), oracle.ar(inp.X_r, inp.W_r), "ar tiny")
+    assert Y.guards_intact()
+
+
+AR_SHAPES = [
+    (1, 8, [8]),
+    (7, 136, [72, 8]),
+    (127, 264, [136]),
+    (128, 256, [64, 64]),
+    (129, 520, [64, 200, 72]),
+    (257, 1032, [128, 128, 128]),
+    (300, 256, [8] * 16),
+    (513, 640, [520]),
+    (200, 7168, [896, 896]),
+]
+
+
+@pytest.mark.parametrize("M,N,K_r", AR_SHAPES)
+def test_ar_ragged(M, N, K_r):
+    inp = gi.gaussian_ar(M, N, K_r)
+    Y, _, _ = run_ar(inp)
+    assert_close(to_f64(Y.out), oracle.ar(inp.X_r, inp.W_r), f"ar {M}x{N} K_r={K_r}")
+    assert Y.guards_intact()
+
+
+def test_ar_shards_in_reverse_allocation_order():
+    inp = gi.gaussian_ar(190, 392, [40, 96, 16, 64])
+    Y, _, _ = run_ar(inp, reverse=True)
+    assert_close(to_f64(Y.out), oracle.ar(inp.X_r, inp.W_r), "ar reversed allocations")
+
+
+def test_ar_integer_inputs_exact():
+    """Values in {-1,0,1}, K=256: every partial and the result are exact in fp32
+    and bf16, so the GPU must equal the exact oracle bit for bit."""
+    inp = gi.integer_ar(128, 256, [128, 128], amp=1, seed=3)
+    Y, _, _ = run_ar(inp)
+    ref = oracle.ar(inp.X_r, inp.W_r)
+    assert np.array_equal(to_f64(Y.out), ref)
+
+
+def test_ar_identity_weight_returns_x_bitwise():
+    K_r = [64, 128, 64]
+    K = sum(K_r)
+    inp = gi.gaussian_ar(200, K, K_r, seed=12)
+    eye = torch.eye(K, dtype=torch.bfloat16)
+    W_r, c = [], 0
+    for k in K_r:
+        W_r.append(eye[:, c:c + k].contiguous())
+        c += k
+    inp.W_r = W_r
+    Y, _, _ = run_ar(inp)
+    assert np.array_equal(bits_of(Y.out), bits_of(torch.cat(inp.X_r, dim=1)))
+
+
+def test_ar_negated_input_negates_output_and_keeps_first_result():
+    """After the page's lifetime test (M=257, K=768, seed 2500): a second call with
+    -X gives exactly -Y, and the first result, in its own buffer, is untouched."""
+    inp = gi.gaussian_ar(257, 512, [256, 512], seed=2500)
+    p, ws = plan()
+    dev = device()
+    X = [x.to(dev) for x in inp.X_r]
+    W = [w.to(dev) for w in inp.W_r]
+    Y1 = torch.empty(257, 512, dtype=torch.bfloat16, device=dev)
+    Y2 = torch.empty_like(Y1)
+    B.gemm_ar(p, X, W, Y1, ws)
+    snap = Y1.clone()
+    B.gemm_ar(p, [-x for x in X], W, Y2, ws)
+    B.gemm_shard_check_status(p, ws)
+    assert torch.equal(Y1.view(torch.int16), snap.view(torch.int16))
+    assert torch.equal(Y2.view(torch.int16), (-Y1).view(torch.int16))
+    assert_close(to_f64(Y1), oracle.ar(inp.X_r, inp.W_r), "first call")
+
+
+def test_inputs_unchanged():
+    inp = gi.gaussian_ar(150, 264, [64, 72])
+    before = [bits_of(t) for t in inp.X_r + inp.W_r]
+    _, X, W = run_ar(inp)
+    after = [bits_of(t) for t in X + W]
+    assert all(np.array_equal(a, b) for a, b in zip(before, after))
+
+
+def test_m_zero_writes_nothing():
+    p, ws = plan()
+    dev = device()
+    X = [torch.empty(0, 64, dtype=torch.bfloat16, device=dev)]
+    W = [torch.randn(64, 64, device=dev).to(torch.bfloat16)]
+    Y = torch.empty(0, 64, dtype=torch.bfloat16, device=dev)
+    B.gemm_ar(p, X, W, Y, ws)
+    B.gemm_shard_check_status(p, ws)
+
+
+# ------------------------------------------------------------------ RS
+
+RS_SHAPES = [
+    (129, 520, [64, 64]),          # M % R != 0: shard 1 has one unwritten row
+    (257, 264, [72, 8, 136]),
+    (5, 256, [64, 64, 64]),
+    (64, 136, [8] * 16),           # 16 shards of 4 rows
+    (300, 7168, [448] * 16),
+]
+
+
+@pytest.mark.parametrize("M,N,K_r", RS_SHAPES)
+def test_rs_matches_oracle_and_ar_bitwise(M, N, K_r):
+    inp = gi.gaussian_ar(M, N, K_r)
+    Ys = run_rs(inp)
+    Yar, _, _ = run_ar(inp)
+    ar_bits = bits_of(Yar.out)
+    ref = oracle.rs(inp.X_r, inp.W_r)
+    for s, y in enumerate(Ys):
+        first, count = oracle.rs_rows(M, inp.R, s)
+        assert y.guards_intact(valid_rows=count), f"shard {s}: row past its valid count written"
+        if count == 0:
+            continue
+        assert_close(to_f64(y.out[:count]), ref[s][:count], f"rs shard {s}")
+        assert np.array_equal(bits_of(y.out[:count]), ar_bits[first:first + count]), \
+            f"shard {s} differs from AR rows bitwise"
+
+
+# ------------------------------------------------------------------ AG
+
+AG_SHAPES = [
+    ([1], 8, 8),
+    ([130, 1, 257], 520, 200),
+    ([0, 64, 0, 128], 264, 128),
+    ([256] * 8, 6288, 1024),
+    ([448, 384], 3648, 512),
+]
+
+
+@pytest.mark.parametrize("M_r,N,K", AG_SHAPES)
+def test_ag_ragged(M_r, N, K):
+    inp = gi.gaussian_ag(M_r, N, K)
+    Y = run_ag(inp)
+    assert_close(to_f64(Y.out), oracle.ag(inp.A_r, inp.W), f"ag M_r={M_r} N={N} K={K}")
+    assert Y.guards_intact()
+
+
+def test_ag_reverse_allocation_order_and_integers_exact():
+    inp = gi.integer_ag([100, 37, 128], 256, 256, amp=1, seed=4)
+    Y = run_ag(inp, reverse=True)
+    assert np.array_equal(to_f64(Y.out), oracle.ag(inp.A_r, inp.W))
+
+
+# ------------------------------------------------------------------ split-K
+
+@pytest.mark.parametrize("split", [2, 3, 7])
+def test_forced_split_k(split):
+    ps = plan(max_M=4096, max_N=2048, max_K=4096, max_R=16, split_k=split)
+    inp = gi.gaussian_ar(129, 520, [256, 512, 64])
+    Y, _, _ = run_ar(inp, p=ps)
+    assert_close(to_f64(Y.out), oracle.ar(inp.X_r, inp.W_r), f"split {split}")
+    assert Y.guards_intact()
+    # RS under the same split writes the same bits as AR
+    Ys = run_rs(inp, p=ps)
+    ar_bits = bits_of(Y.out)
+    for s, y in enumerate(Ys):
+        first, count = oracle.rs_rows(129, 3, s)
+        assert np.array_equal(bits_of(y.out[:count]), ar_bits[first:first + count])
+        assert y.guards_intact(valid_rows=count)
+    # repeated calls reuse the self-resetting counters
+    Y2, _, _ = run_ar(inp, p=ps)
+    assert np.array_equal(bits_of(Y2.out), ar_bits)
+
+
+def test_split_k_ag_and_block_n_128():
+    ps = plan(max_M=4096, max_N=2048, max_K=4096, max_R=16, split_k=4, block_n=128)
+    inp = gi.gaussian_ag([300, 5], 392, 1024)
+    Y = run_ag(inp, p=ps)
+    assert_close(to_f64(Y.out), oracle.ag(inp.A_r, inp.W), "ag split 4 bn 128")
+    assert Y.guards_intact()
+
+
+def test_heuristic_split_small_m_matches_oracle():
+    """M=128, N=7168, 8 shards of 896: the plan splits each tile's k range."""
+    p, ws = plan()
+    d = B.gemm_shard_describe(p, B.MODE_AR, 128, 7168, 0, [896] * 8)
+    assert d["split"] > 1
+    inp = gi.gaussian_ar(128, 7168, [896] * 8, seed=99)
+    Y, _, _ = run_ar(inp)
+    assert_close(to_f64(Y.out), oracle.ar(inp.X_r, inp.W_r), "ar m128 split")
