@@ -1,0 +1,470 @@
+#!/usr/bin/env python3
+"""Benchmark of the shard-reduction GEMM on GB300; prints ONE JSON line.
+
+A step is one call of the fused projection on one batch of synthetic input.
+The headline workload is the AG mode of the KDA-like projection at its largest
+global M: R = 8 activation shards of 4096 rows, K = 7168, N = 6288 (AG-GEMM
+page, microbenchmark table, last KDA row). Inputs (561 MB per step) are larger
+than the 126 MB L2 and resident in HBM before the timed region.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-sweep] [--no-e2e] [--no-cpu-baseline]
+
+--impl reference times the CPU oracle (the only baseline this path has) on the
+box's host cores, each step a bounded sample of the same workload. Under
+torchrun (N > 1) every rank runs an independent replica of the workload on its
+own GPU (no collective on the data path); the JSON value is the work of all
+ranks over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "BF16 TFLOP/s per mode vs M on 1 GB300; % of dense BF16 peak; oracle time"
+L2_BYTES = 126 * 1024 * 1024
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"bf16_burst": float(d["bf16_tflops"]),
+                "bf16_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"bf16_burst": 1900.0, "bf16_sustained": 1700.0, "hbm_gbs": 6800.0,
+            "source": "fallback"}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("gsr_kernel.cu", "gsr_params.h"):
+        with open(os.path.join(ROOT, "tensor_gemm_reduction_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    e = d.get(workload)
+    if not e or e.get("kernel_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"gsr_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        maxp = max(r[2] for r in rows)
+        loaded = [r for r in rows if r[2] >= 0.5 * maxp] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in loaded for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "power_w_max": maxp, "samples": len(loaded), "reasons": reasons}
+
+
+def workload_by_name(name: str):
+    from tensor_gemm_reduction_gb300 import inputs as gi
+    for w in gi.ALL_WORKLOADS:
+        if w.name == name:
+            return w
+    raise SystemExit(f"unknown workload {name}; choose from {[w.name for w in gi.ALL_WORKLOADS]}")
+
+
+def describe_workload(w) -> dict:
+    sizes = w.shard_sizes()
+    d = {"workload": w.name, "mode": w.mode, "R": w.R, "M": w.M, "N": w.N, "K": w.K}
+    d["M_r" if w.mode == "ag" else "K_r"] = sizes[0] if len(set(sizes)) == 1 else sizes
+    return d
+
+
+class Runner:
+    """Device-resident inputs and outputs of one workload plus its call."""
+
+    def __init__(self, w, plan, ws, dev):
+        import torch
+        from tensor_gemm_reduction_gb300 import binding as B
+        from tensor_gemm_reduction_gb300 import inputs as gi
+        self.w, self.plan, self.ws, self.B = w, plan, ws, B
+        inp = gi.make_inputs(w, device=dev)     # seeded on the device: fast at full size
+        self.inp = inp
+        if w.mode == "ag":
+            self.Y = torch.empty(w.M, w.N, dtype=torch.bfloat16, device=dev)
+        elif w.mode == "ar":
+            self.Y = torch.empty(w.M, w.N, dtype=torch.bfloat16, device=dev)
+        else:
+            rps = -(-w.M // w.R)
+            self.Y_r = [torch.empty(rps, w.N, dtype=torch.bfloat16, device=dev) for _ in range(w.R)]
+
+    def inputs(self):
+        return (self.inp.A_r + [self.inp.W]) if self.w.mode == "ag" else (self.inp.X_r + self.inp.W_r)
+
+    def outputs(self):
+        return [self.Y] if self.w.mode != "rs" else self.Y_r
+
+    def __call__(self):
+        B, inp = self.B, self.inp
+        if self.w.mode == "ag":
+            B.gemm_ag(self.plan, inp.A_r, inp.W, self.Y, self.ws)
+        elif self.w.mode == "ar":
+            B.gemm_ar(self.plan, inp.X_r, inp.W_r, self.Y, self.ws)
+        else:
+            B.gemm_rs(self.plan, inp.X_r, inp.W_r, self.Y_r, self.ws, M=self.w.M)
+
+
+def time_launches(fn, steps: int, warmup: int, flush=None):
+    """Per-launch CUDA-event durations (ms) on the current stream, plus the
+    elapsed time of the whole region (ms)."""
+    import torch
+    for _ in range(warmup):
+        if flush is not None:
+            flush()
+        fn()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for s, e in ev:
+        if flush is not None:
+            flush()
+        s.record()
+        fn()
+        e.record()
+    t1.record()
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in ev], t0.elapsed_time(t1)
+
+
+def cpu_oracle_rate(w, host_inp, target_s: float, max_rows: int | None = None):
+    """Time the oracle on whole output rows of `w` (TFLOP/s), bounded to about
+    target_s seconds of CPU work. Returns (rate, rows, seconds, threads)."""
+    import numpy as np
+    import oracle
+    oracle.build()
+    M, N = w.M, w.N
+    rng = np.random.default_rng(0)
+
+    def run(rows):
+        r = np.repeat(rows, N)
+        c = np.tile(np.arange(N), len(rows))
+        t = time.perf_counter()
+        if w.mode == "ag":
+            oracle.ag_at(host_inp.A_r, host_inp.W, r, c)
+        else:
+            oracle.ar_at(host_inp.X_r, host_inp.W_r, r, c)
+        return time.perf_counter() - t
+
+    probe = rng.integers(0, M, 8)
+    dt = run(probe)
+    n = max(8, int(len(probe) * target_s / max(dt, 1e-3)))
+    if max_rows:
+        n = min(n, max_rows)
+    rows = rng.integers(0, M, n)
+    dt = run(rows)
+    flops = 2.0 * len(rows) * N * w.K
+    return flops / dt / 1e12, len(rows), dt, oracle.threads()
+
+
+def host_copy(inp, w):
+    """CPU copies (bf16) of device inputs for the oracle."""
+    if w.mode == "ag":
+        from tensor_gemm_reduction_gb300.inputs import AGInputs
+        return AGInputs(inp.N, inp.K, inp.M_r, [a.cpu() for a in inp.A_r], inp.W.cpu())
+    from tensor_gemm_reduction_gb300.inputs import ARInputs
+    return ARInputs(inp.M, inp.N, inp.K_r, [x.cpu() for x in inp.X_r], [x.cpu() for x in inp.W_r])
+
+
+def run_reference(args, w):
+    """The oracle, as it stands, on host cores: each step computes a bounded
+    sample (a few whole output rows) of the same workload."""
+    ws_, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    from tensor_gemm_reduction_gb300 import inputs as gi
+    oracle.build()
+    # Inputs from the CPU generator (same recipe; no GPU needed on this arm).
+    inp = gi.make_inputs(w, device="cpu")
+    rows_per_step = args.ref_rows
+    rng = np.random.default_rng(1)
+    N = w.N
+
+    def step():
+        rows = rng.integers(0, w.M, rows_per_step)
+        r = np.repeat(rows, N)
+        c = np.tile(np.arange(N), rows_per_step)
+        if w.mode == "ag":
+            oracle.ag_at(inp.A_r, inp.W, r, c)
+        else:
+            oracle.ar_at(inp.X_r, inp.W_r, r, c)
+
+    for _ in range(args.warmup):
+        step()
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t
+    flops = 2.0 * rows_per_step * N * w.K * args.steps
+    value = flops / dt / 1e12
+    sample = f"{rows_per_step} whole output rows ({rows_per_step * N} outputs) of {w.name} per step"
+    out = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws_, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": describe_workload(w), "impl": "reference",
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def sweep(plan, ws, dev, pk, names):
+    """Per-workload kernel time with an L2 flush before every launch."""
+    import torch
+    from tensor_gemm_reduction_gb300 import inputs as gi
+    flush_buf = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    rows = []
+    for w in gi.ALL_WORKLOADS:
+        if names and w.name not in names:
+            continue
+        try:
+            r = Runner(w, plan, ws, dev)
+        except torch.OutOfMemoryError:
+            continue
+        times, _ = time_launches(r, steps=10, warmup=3, flush=lambda: flush_buf.fill_(1))
+        t = statistics.median(times) * 1e-3
+        t_roof = max(w.flops / (pk["bf16_burst"] * 1e12), w.bytes / (pk["hbm_gbs"] * 1e9))
+        d = B_describe(plan, w)
+        rows.append({"workload": w.name, "mode": w.mode, "M": w.M, "N": w.N, "K": w.K, "R": w.R,
+                     "us": round(t * 1e6, 2), "tflops": round(w.flops / t / 1e12, 1),
+                     "hbm_gbs": round(w.bytes / t / 1e9, 1),
+                     "roofline_frac": round(t_roof / t, 3),
+                     "bound": "tensor" if w.flops / (pk["bf16_burst"] * 1e12) >= w.bytes / (pk["hbm_gbs"] * 1e9) else "hbm",
+                     "split": d["split"], "block_n": d["block_n"]})
+        del r
+        torch.cuda.empty_cache()
+    return rows
+
+
+def B_describe(plan, w):
+    from tensor_gemm_reduction_gb300 import binding as B
+    mode = {"ar": B.MODE_AR, "rs": B.MODE_RS, "ag": B.MODE_AG}[w.mode]
+    return B.gemm_shard_describe(plan, mode, w.M, w.N, w.K, w.shard_sizes())
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=600)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="ag_kda_m32768")
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--sweep-only", default="", help="comma-separated workload names")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--ref-rows", type=int, default=4, help="output rows per reference step")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    w = workload_by_name(args.workload)
+
+    if args.impl == "reference":
+        run_reference(args, w)
+        return
+
+    import torch
+    import torch.distributed as dist
+    from tensor_gemm_reduction_gb300 import binding as B
+    from tensor_gemm_reduction_gb300 import build as gbuild
+
+    world, rank, local = dist_env()
+    if world > 1:
+        dist.init_process_group(backend="gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device(f"cuda:{local}")
+    gbuild.build()
+    pk = peaks()
+
+    plan = B.gemm_shard_plan_create(local, 34816, 8192, 8192, 16)
+    ws = B.gemm_shard_workspace_alloc(plan)
+    B.gemm_shard_workspace_init(plan, ws)
+    run = Runner(w, plan, ws, dev)
+
+    # ---- timed region: K back-to-back steps, inputs resident in HBM
+    for _ in range(args.warmup):
+        run()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    with ClockSampler(local) as clk:
+        t_wall = time.perf_counter()
+        times, region_ms = time_launches(run, steps=args.steps, warmup=0)
+        t_wall = time.perf_counter() - t_wall
+    if world > 1:
+        dist.barrier()
+    B.gemm_shard_check_status(plan, ws)
+    region_s = region_ms * 1e-3
+    if world > 1:
+        t = torch.tensor([region_s], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        region_s = float(t.item())
+    total_flops = w.flops * args.steps * world
+    value = total_flops / region_s / 1e12
+    avg_launch_s = statistics.mean(times) * 1e-3
+    achieved = w.flops / avg_launch_s / 1e12
+    long_loop = region_s > 2.0
+    peak = pk["bf16_sustained"] if long_loop else pk["bf16_burst"]
+    clocks = clk.summary()
+
+    result = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": region_s / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": dict(describe_workload(w), l2="inputs larger than L2: %.0f MB read per step" %
+                       ((w.bytes - 2 * w.M * w.N) / 1e6), parallelism="replicas" if world > 1 else "single",
+                       seed="2000+M+K, torch CUDA generator"),
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": ncu_traffic(w.name),
+                     "peak_kind": ("sustained" if long_loop else "burst") + " bf16, " + pk["source"],
+                     "algorithmic_flops_per_launch": w.flops, "avg_launch_us": avg_launch_s * 1e6},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "pages_context": {"gemm_only_us_gb300": 1576.83, "ag_gemm_tp8_us_gb300": 1747.81,
+                          "note": "AG-GEMM page, KDA M=32768 row; other hardware setup, not a target"},
+    }
+
+    if rank == 0 and not args.no_e2e:
+        result["e2e"] = e2e(run, w, args.e2e_steps, world)
+    if rank == 0 and not args.no_cpu_baseline:
+        host_inp = host_copy(run.inp, w)
+        rate, nrows, secs, thr = cpu_oracle_rate(w, host_inp, args.cpu_seconds)
+        result["cpu_baseline"] = {"value": rate, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
+                                  "sample": f"{nrows} whole output rows ({nrows * w.N} outputs) of "
+                                            f"{w.name}, {secs:.1f} s"}
+    if rank == 0 and not args.no_sweep:
+        del run
+        torch.cuda.empty_cache()
+        names = [s for s in args.sweep_only.split(",") if s]
+        result["per_config"] = sweep(plan, ws, dev, pk, names)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def e2e(run, w, steps, world):
+    """Same metric through the public call with host buffers: each step copies the
+    inputs from pinned host memory, runs the call and copies the output back."""
+    import torch
+    dev_in = run.inputs()
+    dev_out = run.outputs()
+    host_in = [t.cpu().pin_memory() for t in dev_in]
+    host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in dev_out]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+
+    def step():
+        for d, h in zip(dev_in, host_in):
+            d.copy_(h, non_blocking=True)
+        run()
+        for h, d in zip(host_out, dev_out):
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(steps):
+        step()
+    t1.record()
+    torch.cuda.synchronize()
+    s = t0.elapsed_time(t1) * 1e-3
+    return {"value": w.flops * steps / s / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": s / steps * 1e3}
+
+
+if __name__ == "__main__":
+    main()

@@ -135,7 +135,8 @@ gsr_status gemm_shard_workspace_init(const gemm_shard_plan *plan, void *ws,
  *   N      rows of every W_r and columns of Y (multiple of 8)
  *   R      number of shards, 1..plan max_R
  *   K_r    host array of R shard widths, each >= 8 and a multiple of 8
- *   X_r    host array of R device pointers, X_r[r] is M x K_r[r] bf16
+ *   X_r    host array of R device pointers, X_r[r] is M x K_r[r] bf16 (may be
+ *          NULL when M == 0; so may Y)
  *   W_r    host array of R device pointers, W_r[r] is N x K_r[r] bf16
  *   Y      device pointer, M x N bf16; rows [0, M) are written, nothing else
  *   ws     workspace of ws_bytes bytes (gemm_shard_workspace_size)
@@ -170,7 +171,8 @@ gsr_status gemm_rs(const gemm_shard_plan *plan, int64_t M, int64_t N, int R,
  *          when M_r[r] == 0)
  *   W      device pointer, N x K bf16
  *   Y      device pointer, (sum M_r) x N bf16; shard r's rows start at
- *          sum_{q<r} M_q. A sum of 0 returns GSR_OK with no launch.
+ *          sum_{q<r} M_q. A sum of 0 returns GSR_OK with no launch (Y may then
+ *          be NULL).
  */
 gsr_status gemm_ag(const gemm_shard_plan *plan, int64_t N, int64_t K, int R,
                    const int64_t *M_r, const void *const *A_r, const void *W, void *Y,

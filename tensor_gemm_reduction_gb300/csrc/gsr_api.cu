@@ -235,7 +235,8 @@ gsr_status check_ksharded(const gemm_shard_plan* P, int64_t M, int64_t N, int R,
     if (K_r[r] < 8 || K_r[r] % 8)
       return fail(GSR_ERR_INVALID_VALUE, "K_r[%d]=%lld must be a positive multiple of 8", r,
                   (long long)K_r[r]);
-    if (!X_r[r] || !W_r[r])
+    // With M == 0 the activation shards have no rows and may be NULL.
+    if ((M > 0 && !X_r[r]) || !W_r[r])
       return fail(GSR_ERR_INVALID_VALUE, "shard %d has a NULL operand pointer", r);
     if (!aligned16(X_r[r]) || !aligned16(W_r[r]))
       return fail(GSR_ERR_INVALID_VALUE, "shard %d operand is not 16-byte aligned", r);
@@ -255,12 +256,14 @@ gsr_status run_ksharded(const gemm_shard_plan* P, int mode, int64_t M, int64_t N
   if (s) return s;
   s = check_ksharded(P, M, N, R, K_r, X_r, W_r);
   if (s) return s;
+  // Outputs may be NULL only when there is no row to write (M == 0).
   if (mode == gsr::kModeAR) {
-    if (!Y || !aligned16(Y)) return fail(GSR_ERR_INVALID_VALUE, "Y must be non-NULL and 16-byte aligned");
+    if ((M > 0 && !Y) || !aligned16(Y))
+      return fail(GSR_ERR_INVALID_VALUE, "Y must be non-NULL and 16-byte aligned");
   } else {
     if (!Y_r) return fail(GSR_ERR_INVALID_VALUE, "Y_r must not be NULL");
     for (int r = 0; r < R; ++r)
-      if (!Y_r[r] || !aligned16(Y_r[r]))
+      if ((M > 0 && !Y_r[r]) || !aligned16(Y_r[r]))
         return fail(GSR_ERR_INVALID_VALUE, "Y_r[%d] must be non-NULL and 16-byte aligned", r);
   }
   const Config c = choose_config(P, mode, M, N, 0, R, K_r);
@@ -462,7 +465,6 @@ gsr_status gemm_ag(const gemm_shard_plan* P, int64_t N, int64_t K, int R, const 
   if (R < 1 || R > P->max_R) return fail(GSR_ERR_INVALID_VALUE, "R=%d outside 1..%d", R, P->max_R);
   if (!M_r || !A_r) return fail(GSR_ERR_INVALID_VALUE, "M_r and A_r must not be NULL");
   if (!W || !aligned16(W)) return fail(GSR_ERR_INVALID_VALUE, "W must be non-NULL and 16-byte aligned");
-  if (!Y || !aligned16(Y)) return fail(GSR_ERR_INVALID_VALUE, "Y must be non-NULL and 16-byte aligned");
   int64_t M = 0;
   for (int r = 0; r < R; ++r) {
     if (M_r[r] < 0) return fail(GSR_ERR_INVALID_VALUE, "M_r[%d] must be >= 0", r);
@@ -470,6 +472,8 @@ gsr_status gemm_ag(const gemm_shard_plan* P, int64_t N, int64_t K, int R, const 
       return fail(GSR_ERR_INVALID_VALUE, "A_r[%d] must be non-NULL and 16-byte aligned", r);
     M += M_r[r];
   }
+  if ((M > 0 && !Y) || !aligned16(Y))
+    return fail(GSR_ERR_INVALID_VALUE, "Y must be non-NULL and 16-byte aligned");
   if (M > P->max_M)
     return fail(GSR_ERR_INVALID_VALUE, "sum of M_r = %lld exceeds the plan's max_M=%lld",
                 (long long)M, (long long)P->max_M);
