@@ -136,6 +136,18 @@ class ClockSampler:
                 "power_w_max": maxp, "samples": len(loaded), "reasons": reasons}
 
 
+def replica_value(local_seconds: float, flops_per_rank: float, world: int):
+    """Whole-job TFLOP/s of `world` independent replicas: all ranks' flops over
+    the slowest rank's timed region (max over ranks through the process group)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([local_seconds], dtype=torch.float64)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    slowest = float(t.item())
+    return flops_per_rank * world / slowest / 1e12, slowest
+
+
 def workload_by_name(name: str):
     from tensor_gemm_reduction_gb300 import inputs as gi
     for w in gi.ALL_WORKLOADS:
@@ -383,13 +395,7 @@ def main():
     if world > 1:
         dist.barrier()
     B.gemm_shard_check_status(plan, ws)
-    region_s = region_ms * 1e-3
-    if world > 1:
-        t = torch.tensor([region_s], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        region_s = float(t.item())
-    total_flops = w.flops * args.steps * world
-    value = total_flops / region_s / 1e12
+    value, region_s = replica_value(region_ms * 1e-3, w.flops * args.steps, world)
     avg_launch_s = statistics.mean(times) * 1e-3
     achieved = w.flops / avg_launch_s / 1e12
     long_loop = region_s > 2.0
