@@ -179,6 +179,40 @@ gsr_status gemm_ag(const gemm_shard_plan *plan, int64_t N, int64_t K, int R,
                    void *ws, size_t ws_bytes, gsr_stream_t stream);
 
 /*
+ * AR exactly as gemm_ar, for callers that cannot allocate device memory: there
+ * is no workspace argument. (The pages have no counterpart; this entry point
+ * exists for callers such as an inference engine that claims all free HBM for
+ * its KV cache at start-up, or code on a latency-critical path where
+ * cudaMalloc's implicit synchronisation is not acceptable.)
+ *
+ * Its scratch (status word, split-K counters and partials) is one fixed array
+ * of 24 MiB in device global memory, part of the library image: every GPU that
+ * loads the library holds it until the process exits. Nothing is allocated or
+ * freed by the call.
+ *   - A shape whose kernel configuration needs more than 24 MiB of scratch
+ *     (for example a forced split-K on many tiles) is rejected with
+ *     GSR_ERR_WORKSPACE before anything is launched; use gemm_ar with a
+ *     workspace for it. The heuristic configuration always fits when
+ *     4 bytes x (ceil(max_M/128) + max_R) x ceil(max_N/128) counters plus
+ *     128 KiB per SM stay under 24 MiB (on a 152-SM GB300: plans of up to about
+ *     a million output tiles).
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress), once per device; make that first call before
+ *     any stream capture begins.
+ *   - Every call on a device shares the one array and starts by clearing its
+ *     status word and counters (a stream-ordered memset). Calls that may
+ *     overlap on the GPU (different streams, or different host threads without
+ *     ordering) race on it and must not be issued.
+ *   - A bounded in-kernel wait that runs out is not reported back (there is
+ *     no workspace to pass to gemm_shard_check_status); use gemm_ar where that
+ *     report is needed.
+ * Arguments, validation and results are those of gemm_ar.
+ */
+gsr_status gemm_ar_noalloc(const gemm_shard_plan *plan, int64_t M, int64_t N, int R,
+                           const int64_t *K_r, const void *const *X_r,
+                           const void *const *W_r, void *Y, gsr_stream_t stream);
+
+/*
  * Synchronise `stream`, read the workspace status word, clear it and return
  * GSR_OK or GSR_ERR_TIMEOUT (the code of the first wait that ran out is
  * available through gsr_last_error_string). After a timeout, re-run

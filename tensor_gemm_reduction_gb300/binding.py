@@ -45,6 +45,7 @@ EXPORTED = (
     "gemm_shard_plan_create", "gemm_shard_plan_create_host", "gemm_shard_plan_destroy", "gemm_shard_plan_set_option",
     "gemm_shard_workspace_size", "gemm_shard_workspace_init", "gemm_ar", "gemm_rs",
     "gemm_ag", "gemm_shard_check_status", "gsr_last_error_string", "gemm_shard_describe",
+    "gemm_ar_noalloc",
 )
 
 
@@ -83,6 +84,7 @@ def load_library() -> ctypes.CDLL:
     lib.gemm_ar.argtypes = [vp, i64, i64, i32, i64_arr, ptr_arr, ptr_arr, vp, vp, sz, vp]
     lib.gemm_rs.argtypes = [vp, i64, i64, i32, i64_arr, ptr_arr, ptr_arr, ptr_arr, vp, sz, vp]
     lib.gemm_ag.argtypes = [vp, i64, i64, i32, i64_arr, ptr_arr, vp, vp, vp, sz, vp]
+    lib.gemm_ar_noalloc.argtypes = [vp, i64, i64, i32, i64_arr, ptr_arr, ptr_arr, vp, vp]
     lib.gemm_shard_check_status.argtypes = [vp, vp, vp]
     lib.gsr_last_error_string.restype = ctypes.c_char_p
     lib.gemm_shard_describe.argtypes = [vp, i32, i64, i64, i64, i32, i64_arr,
@@ -210,6 +212,31 @@ def gemm_ar(plan: Plan, X_r: Sequence[torch.Tensor], W_r: Sequence[torch.Tensor]
     wsp, wsn = _ws(ws)
     _check(load_library().gemm_ar(plan.handle, M, N, R, k, xp, wp, ctypes.c_void_p(Y.data_ptr()),
                                   wsp, wsn, _stream(stream)))
+    return Y
+
+
+def gemm_ar_noalloc(plan: Plan, X_r: Sequence[torch.Tensor], W_r: Sequence[torch.Tensor],
+                    Y: torch.Tensor, stream=None) -> torch.Tensor:
+    """gemm_ar for callers that cannot allocate device memory: no workspace; the
+    library's built-in 24 MiB device scratch is used (shared by every call on a
+    device, so calls must not overlap on the GPU)."""
+    R = len(X_r)
+    if R != len(W_r) or R == 0:
+        raise ValueError("X_r and W_r need the same, non-zero number of shards")
+    for r in range(R):
+        _bf16_2d(X_r[r], f"X_r[{r}]")
+        _bf16_2d(W_r[r], f"W_r[{r}]")
+    _bf16_2d(Y, "Y")
+    M, N = Y.shape
+    K_r = [x.shape[1] for x in X_r]
+    for r in range(R):
+        if X_r[r].shape[0] != M or W_r[r].shape != (N, K_r[r]):
+            raise ValueError(f"shard {r}: X_r must be {M} x K_r and W_r {N} x K_r")
+    k, ka = _i64s(K_r)
+    xp, xa = _ptrs(X_r)
+    wp, wa = _ptrs(W_r)
+    _check(load_library().gemm_ar_noalloc(plan.handle, M, N, R, k, xp, wp,
+                                          ctypes.c_void_p(Y.data_ptr()), _stream(stream)))
     return Y
 
 

@@ -546,3 +546,73 @@ gsr_status gemm_shard_describe(const gemm_shard_plan* P, int mode, int64_t M, in
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// AR without any device allocation.
+//
+// Some callers cannot allocate device memory at all, not even once: an
+// inference engine that claims all free HBM for its KV cache at start-up and
+// afterwards hands a kernel nothing but its inputs and outputs, or a caller on
+// a latency-critical path where cudaMalloc's implicit device synchronisation
+// is not acceptable. gemm_ar_noalloc serves them from a scratch array that is
+// part of the library's device image: it exists on every GPU that loads the
+// library, from load until process exit, and is never allocated by a call.
+
+namespace {
+constexpr size_t kBuiltinScratchBytes = size_t(24) << 20;  // 24 MiB
+constexpr int kScratchDevices = 64;
+}  // namespace
+
+static __device__ __align__(256) unsigned char gsr_builtin_scratch[kBuiltinScratchBytes];
+
+namespace {
+std::mutex g_scratch_mutex;
+void* g_scratch_addr[kScratchDevices] = {};
+
+// Device address of the scratch array on `device`, looked up once per device
+// (the device must be current). Host code cannot use the array's name as an
+// address: on the host it names a shadow object, not device memory.
+gsr_status builtin_scratch_address(int device, void** out) {
+  if (device < 0 || device >= kScratchDevices)
+    return fail(GSR_ERR_UNSUPPORTED, "device ordinal %d has no built-in scratch slot", device);
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (!g_scratch_addr[device]) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, gsr_builtin_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "looking up the built-in scratch address");
+    g_scratch_addr[device] = p;
+  }
+  *out = g_scratch_addr[device];
+  return ok();
+}
+}  // namespace
+
+extern "C" gsr_status gemm_ar_noalloc(const gemm_shard_plan* P, int64_t M, int64_t N, int R,
+                                      const int64_t* K_r, const void* const* X_r,
+                                      const void* const* W_r, void* Y, gsr_stream_t stream) {
+  gsr_status s = check_plan(P);
+  if (s) return s;
+  s = check_ksharded(P, M, N, R, K_r, X_r, W_r);
+  if (s) return s;
+  const Config c = choose_config(P, gsr::kModeAR, M, N, 0, R, K_r);
+  if (c.ws_bytes > kBuiltinScratchBytes)
+    return fail(GSR_ERR_WORKSPACE,
+                "this call needs %zu bytes of scratch but the built-in scratch of gemm_ar_noalloc "
+                "holds %zu; use gemm_ar with a workspace of gemm_shard_workspace_size bytes",
+                c.ws_bytes, kBuiltinScratchBytes);
+  if (M == 0) return ok();
+  if (P->device < 0) return fail(GSR_ERR_UNSUPPORTED, "host plan: arguments are valid, nothing launched");
+  DeviceScope scope(P->device);
+  if (scope.err != cudaSuccess) return cuda_fail(scope.err, "selecting the plan's device");
+  void* scratch = nullptr;
+  s = builtin_scratch_address(P->device, &scratch);
+  if (s) return s;
+  // The array keeps whatever the previous call left; the status word and the
+  // split-K arrival counters must start at zero.
+  cudaError_t e = cudaMemsetAsync(scratch, 0, gsr::kWsHeader + counters_bytes(P),
+                                  reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "clearing the built-in scratch");
+  return run_ksharded(P, gsr::kModeAR, M, N, R, K_r, X_r, W_r, Y, nullptr, scratch,
+                      kBuiltinScratchBytes, stream);
+}
+
