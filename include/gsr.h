@@ -74,7 +74,14 @@ typedef enum {
     GSR_OPT_SPLIT_K = 1,    /* pieces per output tile: 0 = heuristic, 1..16 forced */
     GSR_OPT_BLOCK_N = 2,    /* output tile width: 0 = heuristic, 128 or 256         */
     GSR_OPT_TIMEOUT_NS = 3, /* limit of every in-kernel wait, ns (default 2e9)      */
-    GSR_OPT_MAX_CTAS = 4    /* cap on persistent CTAs: 0 = one per SM               */
+    GSR_OPT_MAX_CTAS = 4,   /* cap on persistent CTAs: 0 = one per SM               */
+    GSR_OPT_RASTER_M = 5,   /* m-tiles per raster group (m runs fastest inside a
+                               group): 0 = heuristic, 1..64                         */
+    GSR_OPT_L2_HINTS = 6,   /* TMA L2 eviction hints: 0 = heuristic, 1 = none,
+                               2 = A evict-last / B evict-first,
+                               3 = A evict-first / B evict-last                     */
+    GSR_OPT_CTA_GROUP = 7   /* CTAs per MMA tile: 0 = heuristic, 1 = one CTA per
+                               128-row tile, 2 = a CTA pair per 256-row tile        */
 } gsr_option;
 
 /*
@@ -227,11 +234,12 @@ const char *gsr_last_error_string(void);
 /* Kernel configuration the plan would choose for a call, for logging and
  * tests: mode 0 = AR, 1 = RS, 2 = AG. AR/RS use M and sizes = K_r (K is
  * ignored); AG uses K and sizes = M_r (M is ignored). Writes block_n, split
- * (pieces per output tile), units (work items) and ctas (persistent CTAs).
- * Any output pointer may be NULL. */
+ * (pieces per output tile), units (work items), ctas (persistent CTAs) and
+ * cta_group (1 or 2 CTAs per MMA tile). Any output pointer may be NULL. */
 gsr_status gemm_shard_describe(const gemm_shard_plan *plan, int mode, int64_t M,
                                int64_t N, int64_t K, int R, const int64_t *sizes,
-                               int *block_n, int *split, int64_t *units, int *ctas);
+                               int *block_n, int *split, int64_t *units, int *ctas,
+                               int *cta_group);
 
 #ifdef __cplusplus
 }

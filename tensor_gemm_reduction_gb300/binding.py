@@ -29,6 +29,9 @@ GSR_OPT_SPLIT_K = 1
 GSR_OPT_BLOCK_N = 2
 GSR_OPT_TIMEOUT_NS = 3
 GSR_OPT_MAX_CTAS = 4
+GSR_OPT_RASTER_M = 5
+GSR_OPT_L2_HINTS = 6
+GSR_OPT_CTA_GROUP = 7
 
 MODE_AR, MODE_RS, MODE_AG = 0, 1, 2
 
@@ -89,7 +92,8 @@ def load_library() -> ctypes.CDLL:
     lib.gsr_last_error_string.restype = ctypes.c_char_p
     lib.gemm_shard_describe.argtypes = [vp, i32, i64, i64, i64, i32, i64_arr,
                                         ctypes.POINTER(i32), ctypes.POINTER(i32),
-                                        ctypes.POINTER(i64), ctypes.POINTER(i32)]
+                                        ctypes.POINTER(i64), ctypes.POINTER(i32),
+                                        ctypes.POINTER(i32)]
     for name in EXPORTED:
         if name not in ("gemm_shard_workspace_size", "gsr_last_error_string"):
             getattr(lib, name).restype = i32
@@ -306,9 +310,10 @@ def gemm_shard_describe(plan: Plan, mode: int, M: int, N: int, K: int,
                         sizes: Sequence[int]) -> dict:
     lib = load_library()
     s, sa = _i64s(sizes)
-    bn, sp, ct = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    bn, sp, ct, cg = ctypes.c_int(), ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
     un = ctypes.c_int64()
     _check(lib.gemm_shard_describe(plan.handle, int(mode), int(M), int(N), int(K), len(sizes), s,
                                    ctypes.byref(bn), ctypes.byref(sp), ctypes.byref(un),
-                                   ctypes.byref(ct)))
-    return {"block_n": bn.value, "split": sp.value, "units": un.value, "ctas": ct.value}
+                                   ctypes.byref(ct), ctypes.byref(cg)))
+    return {"block_n": bn.value, "split": sp.value, "units": un.value, "ctas": ct.value,
+            "cta_group": cg.value}

@@ -32,6 +32,10 @@ struct gemm_shard_plan {
   int opt_split;       // 0 = heuristic
   int opt_block_n;     // 0 = heuristic
   int opt_max_ctas;    // 0 = one per SM
+  int opt_raster_m;    // 0 = heuristic
+  int opt_l2_hints;    // 0 = heuristic
+  int opt_cta_group;   // 0 = heuristic
+  int pair_clusters;   // CTA pairs that can be resident at once
   uint64_t timeout_ns;
 };
 
@@ -103,7 +107,9 @@ size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 // Most output tiles any call under the plan can have: block_n = 128, and in AG
 // mode up to one extra partial m-tile per shard.
 int64_t plan_max_tiles(const gemm_shard_plan* P) {
-  return (cdiv(P->max_M, BM) + P->max_R) * cdiv(P->max_N, 128);
+  // Per-shard rounding adds at most one m-tile per shard, and CTA-pair tiles
+  // (two counters each) at most one more.
+  return (cdiv(P->max_M, BM) + 2 * P->max_R) * cdiv(P->max_N, 128);
 }
 
 // The counter region has a fixed size per plan, so the partials of one call
@@ -114,12 +120,16 @@ size_t counters_bytes(const gemm_shard_plan* P) {
 
 struct Config {
   int block_n = 256;
+  int cta_group = 1;
   int splits = 1;
   int64_t m_tiles = 0, n_tiles = 0, tiles = 0, kb_total = 0, units = 0;
   int ctas = 0;
-  int group_m = 8;
+  int group_m = 1;
+  int policy_a = gsr::kPolicyNormal;
+  int policy_b = gsr::kPolicyNormal;
   size_t ws_bytes = 0;
 };
+
 
 // Kernel configuration: a function of the shape (rows, N, per-shard sizes, R)
 // and the device, never of the mode, so AR and RS on the same inputs run the
@@ -128,13 +138,22 @@ Config choose_config(const gemm_shard_plan* P, int mode, int64_t M, int64_t N, i
                      const int64_t* sizes) {
   Config c;
   c.block_n = P->opt_block_n ? P->opt_block_n : (N <= 128 ? 128 : 256);
+  // Tile rows: 128 per CTA; a CTA pair (cta_group 2) covers 256.
+  auto count_m_tiles = [&](int64_t rows_per_tile) {
+    int64_t mt = 0;
+    if (mode == gsr::kModeAG) {
+      for (int r = 0; r < R; ++r) mt += cdiv(sizes[r], rows_per_tile);
+    } else {
+      mt = cdiv(M, rows_per_tile);
+    }
+    return mt;
+  };
   if (mode == gsr::kModeAG) {
-    for (int r = 0; r < R; ++r) c.m_tiles += cdiv(sizes[r], BM);
     c.kb_total = cdiv(K_ag, BK);
   } else {
-    c.m_tiles = cdiv(M, BM);
     for (int r = 0; r < R; ++r) c.kb_total += cdiv(sizes[r], BK);
   }
+  c.m_tiles = count_m_tiles(BM);
   c.n_tiles = cdiv(N, c.block_n);
   c.tiles = c.m_tiles * c.n_tiles;
   if (P->opt_split) {
@@ -149,12 +168,47 @@ Config choose_config(const gemm_shard_plan* P, int mode, int64_t M, int64_t N, i
     s = std::min<int64_t>(s, 16);
     c.splits = static_cast<int>(std::max<int64_t>(s, 1));
   }
+  // Whole tiles (no split) at block_n 256 run as CTA pairs: a 256 x 256 tile
+  // per pair halves each SM's bytes of B per flop and deepens the smem ring.
+  if (P->opt_cta_group)
+    c.cta_group = (P->opt_cta_group == 2 && P->pair_clusters > 0) ? 2 : 1;
+  else
+    c.cta_group = (c.splits == 1 && c.block_n == 256 && P->pair_clusters > 0) ? 2 : 1;
+  if (c.cta_group == 2) {
+    c.m_tiles = count_m_tiles(2 * BM);
+    c.tiles = c.m_tiles * c.n_tiles;
+  }
   c.units = c.tiles * c.splits;
   const int cap = P->opt_max_ctas ? std::min(P->opt_max_ctas, P->sm_count) : P->sm_count;
-  c.ctas = static_cast<int>(std::min<int64_t>(c.units, cap));
-  c.group_m = 8;
+  if (c.cta_group == 2) {
+    const int64_t pairs = std::min<int64_t>({c.units, static_cast<int64_t>(cap / 2),
+                                              static_cast<int64_t>(P->pair_clusters)});
+    c.ctas = static_cast<int>(2 * std::max<int64_t>(pairs, 1));
+  } else {
+    c.ctas = static_cast<int>(std::min<int64_t>(c.units, cap));
+  }
+  // Raster: groups of group_m m-tiles, m fastest inside a group, so a wave of
+  // concurrent CTAs covers about group_m x (#SMs / group_m) tiles and reads
+  // that many A row-blocks and W column-blocks once each from HBM; the group's
+  // A rows stay in L2 for the group's later waves.
+  c.group_m = P->opt_raster_m ? P->opt_raster_m : 16;
+  switch (P->opt_l2_hints) {
+    case 2:
+      c.policy_a = gsr::kPolicyEvictLast;
+      c.policy_b = gsr::kPolicyEvictFirst;
+      break;
+    case 3:
+      c.policy_a = gsr::kPolicyEvictFirst;
+      c.policy_b = gsr::kPolicyEvictLast;
+      break;
+    default:
+      c.policy_a = gsr::kPolicyNormal;
+      c.policy_b = gsr::kPolicyNormal;
+      break;
+  }
   size_t bytes = gsr::kWsHeader + counters_bytes(P);
-  if (c.splits > 1) bytes += static_cast<size_t>(c.units) * BM * c.block_n * sizeof(float);
+  if (c.splits > 1)
+    bytes += static_cast<size_t>(c.units) * c.cta_group * BM * c.block_n * sizeof(float);
   c.ws_bytes = bytes;
   return c;
 }
@@ -197,6 +251,8 @@ void fill_common(gsr::Params& p, const gemm_shard_plan* P, const Config& c, int 
   p.splits = c.splits;
   p.units = static_cast<int>(c.units);
   p.group_m = c.group_m;
+  p.policy_a = c.policy_a;
+  p.policy_b = c.policy_b;
   p.timeout_ns = P->timeout_ns;
   uint8_t* w = static_cast<uint8_t*>(ws);
   p.status = reinterpret_cast<uint32_t*>(w);
@@ -209,7 +265,8 @@ gsr_status launch(const gemm_shard_plan* P, const gsr::Params& p, const Config& 
   if (P->device < 0) return fail(GSR_ERR_UNSUPPORTED, "host plan: arguments are valid, nothing launched");
   DeviceScope scope(P->device);
   if (scope.err != cudaSuccess) return cuda_fail(scope.err, "selecting the plan's device");
-  cudaError_t e = gsr::launch_gemm(p, c.block_n, c.ctas, reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t e = gsr::launch_gemm(p, c.block_n, c.cta_group, c.ctas,
+                                   reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
   return ok();
 }
@@ -282,7 +339,7 @@ gsr_status run_ksharded(const gemm_shard_plan* P, int mode, int64_t M, int64_t N
     kb += static_cast<int>(cdiv(K_r[r], BK));
     CUresult cr = encode_kmajor(&p.tmap_a[r], X_r[r], M, K_r[r], BM);
     if (cr != CUDA_SUCCESS) return fail(GSR_ERR_CUDA, "encoding X_r[%d] descriptor failed (%d)", r, (int)cr);
-    cr = encode_kmajor(&p.tmap_b[r], W_r[r], N, K_r[r], c.block_n);
+    cr = encode_kmajor(&p.tmap_b[r], W_r[r], N, K_r[r], c.block_n / c.cta_group);
     if (cr != CUDA_SUCCESS) return fail(GSR_ERR_CUDA, "encoding W_r[%d] descriptor failed (%d)", r, (int)cr);
   }
   for (int r = R; r <= kMaxShards; ++r) p.shard_kb_begin[r] = kb;
@@ -327,6 +384,10 @@ static gemm_shard_plan* new_plan(int device, int sm_count, int64_t max_M, int64_
   P->opt_split = 0;
   P->opt_block_n = 0;
   P->opt_max_ctas = 0;
+  P->opt_raster_m = 0;
+  P->opt_l2_hints = 0;
+  P->opt_cta_group = 0;
+  P->pair_clusters = sm_count / 2;   // host plans: every SM pairs up
   P->timeout_ns = 2000000000ull;
   return P;
 }
@@ -356,16 +417,19 @@ gsr_status gemm_shard_plan_create(gemm_shard_plan** out, int device, int64_t max
     return fail(GSR_ERR_UNSUPPORTED, "device %d is compute capability %d.%d; this library is built for sm_103a",
                 device, prop.major, prop.minor);
   if (!encode_fn()) return fail(GSR_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled is unavailable");
+  int pair_clusters = 0;
   {
     DeviceScope scope(device);
     if (scope.err != cudaSuccess) return cuda_fail(scope.err, "cudaSetDevice");
-    if (static_cast<size_t>(prop.sharedMemPerBlockOptin) < gsr::kernel_smem_bytes(256))
+    const size_t need = std::max(gsr::kernel_smem_bytes(256, 1), gsr::kernel_smem_bytes(256, 2));
+    if (static_cast<size_t>(prop.sharedMemPerBlockOptin) < need)
       return fail(GSR_ERR_UNSUPPORTED, "device allows %zu bytes of shared memory per block; %zu needed",
-                  static_cast<size_t>(prop.sharedMemPerBlockOptin), gsr::kernel_smem_bytes(256));
-    e = gsr::prepare_kernels(device);
+                  static_cast<size_t>(prop.sharedMemPerBlockOptin), need);
+    e = gsr::prepare_kernels(device, &pair_clusters);
     if (e != cudaSuccess) return cuda_fail(e, "configuring the kernels");
   }
   *out = new_plan(device, prop.multiProcessorCount, max_M, max_N, max_K, max_R);
+  (*out)->pair_clusters = pair_clusters;
   return ok();
 }
 
@@ -394,6 +458,18 @@ gsr_status gemm_shard_plan_set_option(gemm_shard_plan* plan, gsr_option option, 
     case GSR_OPT_MAX_CTAS:
       if (value < 0 || value > INT32_MAX) return fail(GSR_ERR_INVALID_VALUE, "max_ctas must be >= 0");
       plan->opt_max_ctas = static_cast<int>(value);
+      return ok();
+    case GSR_OPT_RASTER_M:
+      if (value < 0 || value > 64) return fail(GSR_ERR_INVALID_VALUE, "raster_m must be 0..64");
+      plan->opt_raster_m = static_cast<int>(value);
+      return ok();
+    case GSR_OPT_L2_HINTS:
+      if (value < 0 || value > 3) return fail(GSR_ERR_INVALID_VALUE, "l2_hints must be 0..3");
+      plan->opt_l2_hints = static_cast<int>(value);
+      return ok();
+    case GSR_OPT_CTA_GROUP:
+      if (value < 0 || value > 2) return fail(GSR_ERR_INVALID_VALUE, "cta_group must be 0..2");
+      plan->opt_cta_group = static_cast<int>(value);
       return ok();
   }
   return fail(GSR_ERR_INVALID_VALUE, "unknown option %d", static_cast<int>(option));
@@ -492,7 +568,7 @@ gsr_status gemm_ag(const gemm_shard_plan* P, int64_t N, int64_t K, int R, const 
     p.shard_mt_begin[r] = mt;
     p.shard_row_begin[r] = row;
     p.shard_rows[r] = static_cast<int>(M_r[r]);
-    mt += static_cast<int>(cdiv(M_r[r], BM));
+    mt += static_cast<int>(cdiv(M_r[r], BM * c.cta_group));   // tiles never cross a shard
     row += static_cast<int>(M_r[r]);
     if (M_r[r] > 0) {
       CUresult cr = encode_kmajor(&p.tmap_a[r], A_r[r], M_r[r], K, BM);
@@ -503,7 +579,7 @@ gsr_status gemm_ag(const gemm_shard_plan* P, int64_t N, int64_t K, int R, const 
     p.shard_mt_begin[r] = mt;
     p.shard_row_begin[r] = row;
   }
-  CUresult cr = encode_kmajor(&p.tmap_b[0], W, N, K, c.block_n);
+  CUresult cr = encode_kmajor(&p.tmap_b[0], W, N, K, c.block_n / c.cta_group);
   if (cr != CUDA_SUCCESS) return fail(GSR_ERR_CUDA, "encoding the W descriptor failed (%d)", (int)cr);
   p.y = static_cast<uint16_t*>(Y);
   return launch(P, p, c, stream);
@@ -531,7 +607,7 @@ gsr_status gemm_shard_check_status(const gemm_shard_plan* P, void* ws, gsr_strea
 
 gsr_status gemm_shard_describe(const gemm_shard_plan* P, int mode, int64_t M, int64_t N, int64_t K,
                                int R, const int64_t* sizes, int* block_n, int* split,
-                               int64_t* units, int* ctas) {
+                               int64_t* units, int* ctas, int* cta_group) {
   gsr_status s = check_plan(P);
   if (s) return s;
   if (mode < 0 || mode > 2) return fail(GSR_ERR_INVALID_VALUE, "mode must be 0, 1 or 2");
@@ -542,6 +618,7 @@ gsr_status gemm_shard_describe(const gemm_shard_plan* P, int mode, int64_t M, in
   if (split) *split = c.splits;
   if (units) *units = c.units;
   if (ctas) *ctas = c.ctas;
+  if (cta_group) *cta_group = c.cta_group;
   return ok();
 }
 

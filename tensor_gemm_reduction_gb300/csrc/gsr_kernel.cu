@@ -89,6 +89,27 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// Same load with an L2 cache policy (from createpolicy) attached.
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                                 int x, int y, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t make_l2_policy(int kind) {
+  uint64_t pol;
+  if (kind == kPolicyEvictLast)
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  else if (kind == kPolicyEvictFirst)
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  else
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -181,6 +202,85 @@ __device__ __forceinline__ bool epilogue_bar_and(bool v) {
   return out != 0;
 }
 
+// ------------------------------------------------------------ CTA-pair glue
+// A CTA pair is a cluster of two CTAs (ranks 0 and 1); rank 0 issues the
+// pair's MMAs (cta_group::2), each CTA holds half of A (rows) and half of B
+// (columns of the output) in its own shared memory and TMEM.
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Shared-memory address `addr` of this CTA, as seen in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_shared_to_rank(uint32_t addr, uint32_t rank) {
+  uint32_t out;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(addr), "r"(rank));
+  return out;
+}
+
+__device__ __forceinline__ void cluster_barrier() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::
+          : "memory");
+}
+
+// Arrive on an mbarrier given by its shared::cluster address (possibly the peer's).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+
+// TMA load into this CTA's shared memory whose completion is counted on an
+// mbarrier of either CTA of the pair (the leader's).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map,
+                                                 uint32_t bar_cluster, int x, int y,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t slot_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem),
+               "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+// D (256 rows split over the pair's TMEM) (+)= A (pair halves) * B (pair halves)^T.
+__device__ __forceinline__ void mma_bf16_ss_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                 uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive once on the mbarrier at offset `bar` in every CTA of `mask` when all
+// tcgen05 ops this thread issued so far are done.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(mask)
+      : "memory");
+}
+
 // ------------------------------------------------------------ descriptors
 
 // Shared-memory matrix descriptor of a K-major bf16 tile written by TMA with
@@ -254,14 +354,15 @@ __device__ __noinline__ bool wait_drain(uint32_t bar, uint32_t parity, uint64_t 
 struct Unit {
   int tile;       // output tile index (also the split-K counter index)
   int split;      // piece of the tile's k range
-  int n0;         // first output column
-  int m0;         // first row in the A operand: AR/RS global, AG local to shard
+  int n0;         // first output column of the tile
+  int m0;         // first row of the tile in the A operand: AR/RS global, AG
+                  // local to the shard (a CTA pair's tile spans 2 x BM rows)
   int shard;      // AG: M-shard of the tile
   int kb_begin;   // k-blocks [kb_begin, kb_end) of this piece
   int kb_end;
 };
 
-template <int BN>
+template <int BN, int CG>
 __device__ __forceinline__ Unit decode_unit(const Params& p, int u) {
   Unit t;
   t.tile = u / p.splits;
@@ -280,22 +381,28 @@ __device__ __forceinline__ Unit decode_unit(const Params& p, int u) {
     int r = 0;
     while (r + 1 < p.R && p.shard_mt_begin[r + 1] <= mt) ++r;
     t.shard = r;
-    t.m0 = (mt - p.shard_mt_begin[r]) * BM;
+    t.m0 = (mt - p.shard_mt_begin[r]) * (BM * CG);
   } else {
     t.shard = 0;
-    t.m0 = mt * BM;
+    t.m0 = mt * (BM * CG);
   }
   t.kb_begin = static_cast<int>((static_cast<long long>(t.split) * p.kb_total) / p.splits);
   t.kb_end = static_cast<int>((static_cast<long long>(t.split + 1) * p.kb_total) / p.splits);
   return t;
 }
 
+// MMA N of a tile: the full BN, or the ragged tail rounded up to 16 columns.
+template <int BN>
+__device__ __forceinline__ uint32_t tile_mma_n(const Params& p, const Unit& t) {
+  return static_cast<uint32_t>(min(BN, (p.N - t.n0 + 15) & ~15));
+}
+
 // ------------------------------------------------------------ shared layout
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int CG>
 struct Layout {
-  static constexpr uint32_t kABytes = BM * BK * 2;
-  static constexpr uint32_t kBBytes = BN * BK * 2;
+  static constexpr uint32_t kABytes = BM * BK * 2;            // this CTA's rows of A
+  static constexpr uint32_t kBBytes = (BN / CG) * BK * 2;     // this CTA's columns of B
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
   static constexpr uint32_t kTiles = STAGES * kStageBytes;
   // barriers: full[S], empty[S], tmem_full[2], tmem_empty[2], drain
@@ -308,9 +415,10 @@ struct Layout {
 
 // ------------------------------------------------------------ roles
 
-template <int BN, int STAGES>
-__device__ void run_producer(const Params& p, uint32_t tiles_base, uint32_t bars, const Ctl& ctl) {
-  using L = Layout<BN, STAGES>;
+template <int BN, int STAGES, int CG>
+__device__ void run_producer(const Params& p, uint32_t tiles_base, uint32_t bars, uint32_t rank,
+                             const Ctl& ctl) {
+  using L = Layout<BN, STAGES, CG>;
   const uint32_t full0 = bars, empty0 = bars + 8 * STAGES;
   if (p.mode == kModeAG) {
     for (int r = 0; r < p.R; ++r)
@@ -322,10 +430,17 @@ __device__ void run_producer(const Params& p, uint32_t tiles_base, uint32_t bars
       prefetch_tensormap(&p.tmap_b[r]);
     }
   }
+  const uint64_t pol_a = make_l2_policy(p.policy_a);
+  const uint64_t pol_b = make_l2_policy(p.policy_b);
+  const int stride = static_cast<int>(gridDim.x) / CG;
   uint32_t issued = 0;
   bool ok = true;
-  for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
-    const Unit t = decode_unit<BN>(p, u);
+  for (int u = static_cast<int>(blockIdx.x) / CG; u < p.units && ok; u += stride) {
+    const Unit t = decode_unit<BN, CG>(p, u);
+    // This CTA's rows of A, and its columns of B: with a CTA pair the MMA's N
+    // columns are split in halves between the two CTAs.
+    const int a_row = t.m0 + BM * static_cast<int>(rank);
+    const int b_row = t.n0 + static_cast<int>(rank * (tile_mma_n<BN>(p, t) / CG));
     int r = 0;
     if (p.mode != kModeAG)
       while (p.shard_kb_begin[r + 1] <= t.kb_begin) ++r;
@@ -339,37 +454,54 @@ __device__ void run_producer(const Params& p, uint32_t tiles_base, uint32_t bars
       const uint32_t full = full0 + 8 * stage;
       const uint32_t sa = tiles_base + stage * L::kABytes;
       const uint32_t sb = tiles_base + STAGES * L::kABytes + stage * L::kBBytes;
-      mbar_arrive_expect_tx(full, L::kStageBytes);
+      const CUtensorMap* ma;
+      const CUtensorMap* mb;
+      int kx;
       if (p.mode == kModeAG) {
-        tma_load_2d(sa, &p.tmap_a[t.shard], full, kb * BK, t.m0);
-        tma_load_2d(sb, &p.tmap_b[0], full, kb * BK, t.n0);
+        ma = &p.tmap_a[t.shard];
+        mb = &p.tmap_b[0];
+        kx = kb * BK;
       } else {
         while (p.shard_kb_begin[r + 1] <= kb) ++r;
-        const int kx = (kb - p.shard_kb_begin[r]) * BK;
-        tma_load_2d(sa, &p.tmap_a[r], full, kx, t.m0);
-        tma_load_2d(sb, &p.tmap_b[r], full, kx, t.n0);
+        ma = &p.tmap_a[r];
+        mb = &p.tmap_b[r];
+        kx = (kb - p.shard_kb_begin[r]) * BK;
+      }
+      if constexpr (CG == 1) {
+        mbar_arrive_expect_tx(full, L::kStageBytes);
+        tma_load_2d_hint(sa, ma, full, kx, a_row, pol_a);
+        tma_load_2d_hint(sb, mb, full, kx, b_row, pol_b);
+      } else {
+        // Both CTAs' bytes are counted on the leader's full barrier, which the
+        // leader alone arms (for the pair's bytes).
+        if (rank == 0) mbar_arrive_expect_tx(full, CG * L::kStageBytes);
+        const uint32_t lead_full = map_shared_to_rank(full, 0);
+        tma_load_2d_pair(sa, ma, lead_full, kx, a_row, pol_a);
+        tma_load_2d_pair(sb, mb, lead_full, kx, b_row, pol_b);
       }
       ++issued;
     }
   }
-  if (!ok) {
-    // Let every copy already issued land before the CTA's shared memory goes away.
+  if (!ok && (CG == 1 || rank == 0)) {
+    // Let every copy already issued land before the CTA's shared memory goes
+    // away (with a pair, the leader's barriers count the peer's copies too).
     const uint32_t first = issued > STAGES ? issued - STAGES : 0;
     for (uint32_t i = first; i < issued; ++i)
       wait_drain(full0 + 8 * (i % STAGES), (i / STAGES) & 1u, 100000000ull);
   }
 }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int CG>
 __device__ void run_mma(const Params& p, uint32_t tiles_base, uint32_t bars, uint32_t tmem_base,
                         const Ctl& ctl) {
-  using L = Layout<BN, STAGES>;
+  using L = Layout<BN, STAGES, CG>;
   const uint32_t full0 = bars, tfull0 = bars + 16 * STAGES, tempty0 = tfull0 + 16;
   const uint32_t empty0 = bars + 8 * STAGES, drain = tempty0 + 16;
+  const int stride = static_cast<int>(gridDim.x) / CG;
   uint32_t consumed = 0, local = 0;
   bool ok = true, issued_any = false;
-  for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x, ++local) {
-    const Unit t = decode_unit<BN>(p, u);
+  for (int u = static_cast<int>(blockIdx.x) / CG; u < p.units && ok; u += stride, ++local) {
+    const Unit t = decode_unit<BN, CG>(p, u);
     const uint32_t acc = local & 1u;
     const uint32_t acc_parity = ((local >> 1) & 1u) ^ 1u;
     if (!wait_bounded(tempty0 + 8 * acc, acc_parity, ctl, (kRoleMma << 8) | 1)) {
@@ -378,9 +510,7 @@ __device__ void run_mma(const Params& p, uint32_t tiles_base, uint32_t bars, uin
     }
     tc_fence_after_sync();
     const uint32_t d_tmem = tmem_base + acc * BN;
-    const int n_left = p.N - t.n0;
-    const uint32_t mma_n = static_cast<uint32_t>(min(BN, (n_left + 15) & ~15));
-    const uint32_t idesc = make_idesc(BM, mma_n);
+    const uint32_t idesc = make_idesc(BM * CG, tile_mma_n<BN>(p, t));
     for (int kb = t.kb_begin; kb < t.kb_end; ++kb) {
       const uint32_t stage = consumed % STAGES;
       const uint32_t parity = (consumed / STAGES) & 1u;
@@ -394,24 +524,35 @@ __device__ void run_mma(const Params& p, uint32_t tiles_base, uint32_t bars, uin
 #pragma unroll
       for (int k = 0; k < BK / 16; ++k) {
         // advance 16 elements (32 bytes) along K inside the swizzled 128-byte rows
-        mma_bf16_ss(d_tmem, a_desc + 2 * k, b_desc + 2 * k, idesc,
-                    (kb > t.kb_begin || k > 0) ? 1u : 0u);
+        const uint32_t accumulate = (kb > t.kb_begin || k > 0) ? 1u : 0u;
+        if constexpr (CG == 1)
+          mma_bf16_ss(d_tmem, a_desc + 2 * k, b_desc + 2 * k, idesc, accumulate);
+        else
+          mma_bf16_ss_pair(d_tmem, a_desc + 2 * k, b_desc + 2 * k, idesc, accumulate);
       }
       issued_any = true;
-      mma_commit(empty0 + 8 * stage);
+      if constexpr (CG == 1)
+        mma_commit(empty0 + 8 * stage);
+      else
+        mma_commit_pair(empty0 + 8 * stage, 0x3);   // frees the stage in both CTAs
       ++consumed;
     }
     if (!ok) break;
-    mma_commit(tfull0 + 8 * acc);
+    if constexpr (CG == 1)
+      mma_commit(tfull0 + 8 * acc);
+    else
+      mma_commit_pair(tfull0 + 8 * acc, 0x3);       // both CTAs' epilogues may read
   }
   if (!ok && issued_any) {
     // Every MMA issued so far must finish before the TMEM is released.
-    mma_commit(drain);
+    if constexpr (CG == 1)
+      mma_commit(drain);
+    else
+      mma_commit_pair(drain, 0x1);
     wait_drain(drain, 0, 100000000ull);
   }
 }
 
-template <int BN>
 __device__ __forceinline__ void store_row_chunk(uint16_t* row_ptr, int col_in_tile, int n_valid,
                                                 const uint32_t (&v)[32], bool row_ok) {
 #pragma unroll
@@ -428,17 +569,19 @@ __device__ __forceinline__ void store_row_chunk(uint16_t* row_ptr, int col_in_ti
   }
 }
 
-template <int BN, int STAGES>
-__device__ void run_epilogue(const Params& p, uint32_t bars, uint32_t tmem_base,
+template <int BN, int STAGES, int CG>
+__device__ void run_epilogue(const Params& p, uint32_t bars, uint32_t tmem_base, uint32_t rank,
                              volatile int* last_flag, const Ctl& ctl) {
   const uint32_t tfull0 = bars + 16 * STAGES, tempty0 = tfull0 + 16;
   const int et = static_cast<int>(threadIdx.x) - 64;          // 0..127
+  const int lane = static_cast<int>(threadIdx.x) & 31;
   const int quad = (static_cast<int>(threadIdx.x) >> 5) & 3;  // TMEM lanes this warp may read
-  const int row_in_tile = quad * 32 + (static_cast<int>(threadIdx.x) & 31);
+  const int row_in_tile = quad * 32 + lane;
   const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
+  const int stride = static_cast<int>(gridDim.x) / CG;
   uint32_t local = 0;
-  for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++local) {
-    const Unit t = decode_unit<BN>(p, u);
+  for (int u = static_cast<int>(blockIdx.x) / CG; u < p.units; u += stride, ++local) {
+    const Unit t = decode_unit<BN, CG>(p, u);
     const uint32_t acc = local & 1u;
     const uint32_t acc_parity = (local >> 1) & 1u;
     bool ok = wait_bounded(tfull0 + 8 * acc, acc_parity, ctl, (kRoleEpilogue << 8) | 1);
@@ -448,16 +591,17 @@ __device__ void run_epilogue(const Params& p, uint32_t bars, uint32_t tmem_base,
     const uint32_t taddr = tmem_base + lane_addr + acc * BN;
     const int n_valid = min(BN, p.N - t.n0);
     const int chunks = (n_valid + 31) >> 5;
+    const int m0 = t.m0 + BM * static_cast<int>(rank);   // this CTA's first row
 
     // Where this thread's output row goes.
     bool row_ok;
     uint16_t* row_ptr;
     if (p.mode == kModeAG) {
-      const int lr = t.m0 + row_in_tile;
+      const int lr = m0 + row_in_tile;
       row_ok = lr < p.shard_rows[t.shard];
       row_ptr = p.y + (static_cast<size_t>(p.shard_row_begin[t.shard]) + lr) * p.N + t.n0;
     } else {
-      const int gr = t.m0 + row_in_tile;
+      const int gr = m0 + row_in_tile;
       row_ok = gr < p.M;
       if (p.mode == kModeRS) {
         const int s = row_ok ? gr / p.rps : 0;
@@ -467,21 +611,35 @@ __device__ void run_epilogue(const Params& p, uint32_t bars, uint32_t tmem_base,
       }
     }
 
+    // Hands the accumulator back to the MMA issuer (the leader's barrier with a
+    // pair): one arrival per warp once its TMEM reads are complete.
+    auto release_accumulator = [&]() {
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) {
+        if constexpr (CG == 1)
+          mbar_arrive(tempty0 + 8 * acc);
+        else
+          mbar_arrive_cluster(map_shared_to_rank(tempty0 + 8 * acc, 0));
+      }
+    };
+
     if (p.splits == 1) {
       for (int c = 0; c < chunks; ++c) {
         uint32_t v[32];
         tmem_ld_32cols(taddr + 32 * c, v);
         tmem_ld_wait(v);
-        store_row_chunk<BN>(row_ptr, 32 * c, n_valid, v, row_ok);
+        store_row_chunk(row_ptr, 32 * c, n_valid, v, row_ok);
       }
-      tc_fence_before_sync();
-      mbar_arrive(tempty0 + 8 * acc);
+      release_accumulator();
       continue;
     }
 
-    // Split-K: publish this piece's fp32 partial tile. Layout inside a slot:
-    // [column group of 4][row][4], so a warp's float4 stores are contiguous.
-    float* slot = p.partials + static_cast<size_t>(u) * (BM * BN);
+    // Split-K: publish this CTA's fp32 partial of the tile. Layout inside a
+    // slot: [column group of 4][row][4], so a warp's float4 stores are contiguous.
+    // A CTA pair keeps one slot and one counter per CTA half.
+    const int half = t.tile * CG + static_cast<int>(rank);
+    float* slot = p.partials + (static_cast<size_t>(u) * CG + rank) * (BM * BN);
     for (int c = 0; c < chunks; ++c) {
       uint32_t v[32];
       tmem_ld_32cols(taddr + 32 * c, v);
@@ -493,49 +651,49 @@ __device__ void run_epilogue(const Params& p, uint32_t bars, uint32_t tmem_base,
         __stcg(reinterpret_cast<float4*>(slot) + (8 * c + j) * BM + row_in_tile, f);
       }
     }
-    tc_fence_before_sync();
-    mbar_arrive(tempty0 + 8 * acc);  // the accumulator is free for the next tile
+    release_accumulator();  // the accumulator is free for the next tile
     __threadfence();
     epilogue_bar_sync();
     if (et == 0) {
-      const uint32_t before = atomicAdd(&p.counters[t.tile], 1u);
+      const uint32_t before = atomicAdd(&p.counters[half], 1u);
       *last_flag = (before == static_cast<uint32_t>(p.splits - 1)) ? 1 : 0;
     }
     epilogue_bar_sync();
     if (*last_flag) {
       __threadfence();
-      const float4* piece0 =
-          reinterpret_cast<const float4*>(p.partials + static_cast<size_t>(t.tile) * p.splits * (BM * BN));
+      // Pieces of this half-tile are units tile*splits + s, slots (unit*CG + rank).
+      const size_t slot_floats = static_cast<size_t>(BM) * BN;
+      const float4* base = reinterpret_cast<const float4*>(p.partials);
       for (int c = 0; c < chunks; ++c) {
         float a[32];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float4 f = __ldcg(piece0 + (8 * c + j) * BM + row_in_tile);
-          a[4 * j] = f.x; a[4 * j + 1] = f.y; a[4 * j + 2] = f.z; a[4 * j + 3] = f.w;
-        }
-        for (int s = 1; s < p.splits; ++s) {
-          const float4* piece = piece0 + static_cast<size_t>(s) * (BM * BN / 4);
+        for (int s = 0; s < p.splits; ++s) {
+          const size_t sl = (static_cast<size_t>(t.tile) * p.splits + s) * CG + rank;
+          const float4* piece = base + sl * (slot_floats / 4);
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const float4 f = __ldcg(piece + (8 * c + j) * BM + row_in_tile);
-            a[4 * j] += f.x; a[4 * j + 1] += f.y; a[4 * j + 2] += f.z; a[4 * j + 3] += f.w;
+            if (s == 0) {
+              a[4 * j] = f.x; a[4 * j + 1] = f.y; a[4 * j + 2] = f.z; a[4 * j + 3] = f.w;
+            } else {
+              a[4 * j] += f.x; a[4 * j + 1] += f.y; a[4 * j + 2] += f.z; a[4 * j + 3] += f.w;
+            }
           }
         }
         uint32_t v[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(a[j]);
-        store_row_chunk<BN>(row_ptr, 32 * c, n_valid, v, row_ok);
+        store_row_chunk(row_ptr, 32 * c, n_valid, v, row_ok);
       }
-      if (et == 0) atomicExch(&p.counters[t.tile], 0u);  // ready for the next call
+      if (et == 0) atomicExch(&p.counters[half], 0u);  // ready for the next call
     }
   }
 }
 
 // ------------------------------------------------------------ kernel
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int CG>
 __global__ void __launch_bounds__(kThreads, 1) gsr_gemm_kernel(const __grid_constant__ Params p) {
-  using L = Layout<BN, STAGES>;
+  using L = Layout<BN, STAGES, CG>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t tiles_base = (raw + 1023u) & ~1023u;
@@ -548,15 +706,16 @@ __global__ void __launch_bounds__(kThreads, 1) gsr_gemm_kernel(const __grid_cons
 
   const int warp = static_cast<int>(threadIdx.x) >> 5;
   const int lane = static_cast<int>(threadIdx.x) & 31;
+  const uint32_t rank = (CG == 1) ? 0u : cluster_rank();
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
-      mbar_init(bars + 8 * i, 1);                 // full: producer's expect_tx + TMA bytes
+      mbar_init(bars + 8 * i, 1);                 // full: the (leader's) expect_tx + TMA bytes
       mbar_init(bars + 8 * (STAGES + i), 1);      // empty: one MMA commit
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bars + 16 * STAGES + 8 * i, 1);                      // tmem_full: MMA commit
-      mbar_init(bars + 16 * STAGES + 16 + 8 * i, kEpilogueThreads);  // tmem_empty
+      mbar_init(bars + 16 * STAGES + 8 * i, 1);               // tmem_full: MMA commit
+      mbar_init(bars + 16 * STAGES + 16 + 8 * i, 4 * CG);     // tmem_empty: one per epilogue warp
     }
     mbar_init(bars + 16 * STAGES + 32, 1);  // drain
     *abort_flag = 0;
@@ -565,62 +724,118 @@ __global__ void __launch_bounds__(kThreads, 1) gsr_gemm_kernel(const __grid_cons
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), 2 * BN);
-    tmem_relinquish();
+    if constexpr (CG == 1) {
+      tmem_alloc(smem_u32(tmem_slot), 2 * BN);
+      tmem_relinquish();
+    } else {
+      tmem_alloc_pair(smem_u32(tmem_slot), 2 * BN);
+      tmem_relinquish_pair();
+    }
   }
   tc_fence_before_sync();
-  __syncthreads();
+  if constexpr (CG == 1)
+    __syncthreads();
+  else
+    cluster_barrier();   // the peer's barriers exist before anyone signals them
   tc_fence_after_sync();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
 
   Ctl ctl{abort_flag, p.status, p.timeout_ns};
   if (warp == 0) {
-    if (lane == 0) run_producer<BN, STAGES>(p, tiles_base, bars, ctl);
+    if (lane == 0) run_producer<BN, STAGES, CG>(p, tiles_base, bars, rank, ctl);
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0) run_mma<BN, STAGES>(p, tiles_base, bars, tmem_base, ctl);
+    if (lane == 0 && rank == 0) run_mma<BN, STAGES, CG>(p, tiles_base, bars, tmem_base, ctl);
     __syncwarp();
   } else {
-    run_epilogue<BN, STAGES>(p, bars, tmem_base, last_flag, ctl);
+    run_epilogue<BN, STAGES, CG>(p, bars, tmem_base, rank, last_flag, ctl);
   }
 
   tc_fence_before_sync();
-  __syncthreads();
+  if constexpr (CG == 1)
+    __syncthreads();
+  else
+    cluster_barrier();   // no CTA leaves while its peer may still signal it
   if (warp == 1) {
     tc_fence_after_sync();
-    tmem_dealloc(tmem_base, 2 * BN);
+    if constexpr (CG == 1)
+      tmem_dealloc(tmem_base, 2 * BN);
+    else
+      tmem_dealloc_pair(tmem_base, 2 * BN);
   }
 }
 
-constexpr int kStages256 = 4;
-constexpr int kStages128 = 6;
+// Ring depths: each instance fills about 192 KB of shared memory.
+template <int BN, int CG> struct Stages;
+template <> struct Stages<256, 1> { static constexpr int value = 4; };   // 48 KB stages
+template <> struct Stages<128, 1> { static constexpr int value = 6; };   // 32 KB
+template <> struct Stages<256, 2> { static constexpr int value = 6; };   // 32 KB per CTA
+template <> struct Stages<128, 2> { static constexpr int value = 8; };   // 24 KB per CTA
+
+template <int BN, int CG>
+using KernelLayout = Layout<BN, Stages<BN, CG>::value, CG>;
+
+template <int BN, int CG>
+cudaError_t set_smem_limit() {
+  return cudaFuncSetAttribute(gsr_gemm_kernel<BN, Stages<BN, CG>::value, CG>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(KernelLayout<BN, CG>::kSmem));
+}
+
+template <int BN, int CG>
+cudaError_t launch_instance(const Params& p, int ctas, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CG;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(ctas, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = KernelLayout<BN, CG>::kSmem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = CG == 2 ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, gsr_gemm_kernel<BN, Stages<BN, CG>::value, CG>, p);
+}
 
 }  // namespace
 
-size_t kernel_smem_bytes(int block_n) {
-  return block_n == 256 ? Layout<256, kStages256>::kSmem : Layout<128, kStages128>::kSmem;
+size_t kernel_smem_bytes(int block_n, int cta_group) {
+  if (cta_group == 2)
+    return block_n == 256 ? KernelLayout<256, 2>::kSmem : KernelLayout<128, 2>::kSmem;
+  return block_n == 256 ? KernelLayout<256, 1>::kSmem : KernelLayout<128, 1>::kSmem;
 }
 
-cudaError_t prepare_kernels(int device) {
+cudaError_t prepare_kernels(int device, int* pair_clusters) {
   (void)device;  // the caller has made `device` current
-  cudaError_t e = cudaFuncSetAttribute(gsr_gemm_kernel<256, kStages256>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(Layout<256, kStages256>::kSmem));
+  cudaError_t e = set_smem_limit<256, 1>();
+  if (e == cudaSuccess) e = set_smem_limit<128, 1>();
+  if (e == cudaSuccess) e = set_smem_limit<256, 2>();
+  if (e == cudaSuccess) e = set_smem_limit<128, 2>();
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(gsr_gemm_kernel<128, kStages128>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(Layout<128, kStages128>::kSmem));
+  // How many CTA pairs can be resident at once (SMs pair up inside a GPC).
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = KernelLayout<256, 2>::kSmem;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaOccupancyMaxActiveClusters(pair_clusters,
+                                        gsr_gemm_kernel<256, Stages<256, 2>::value, 2>, &cfg);
 }
 
-cudaError_t launch_gemm(const Params& p, int block_n, int ctas, cudaStream_t stream) {
-  if (block_n == 256) {
-    gsr_gemm_kernel<256, kStages256>
-        <<<ctas, kThreads, Layout<256, kStages256>::kSmem, stream>>>(p);
-  } else {
-    gsr_gemm_kernel<128, kStages128>
-        <<<ctas, kThreads, Layout<128, kStages128>::kSmem, stream>>>(p);
-  }
-  return cudaGetLastError();
+cudaError_t launch_gemm(const Params& p, int block_n, int cta_group, int ctas, cudaStream_t stream) {
+  if (cta_group == 2)
+    return block_n == 256 ? launch_instance<256, 2>(p, ctas, stream)
+                          : launch_instance<128, 2>(p, ctas, stream);
+  return block_n == 256 ? launch_instance<256, 1>(p, ctas, stream)
+                        : launch_instance<128, 1>(p, ctas, stream);
 }
 
 }  // namespace gsr

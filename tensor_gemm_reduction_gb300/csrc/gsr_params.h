@@ -15,6 +15,9 @@ constexpr int kEpilogueThreads = 128;
 
 enum Mode : int { kModeAR = 0, kModeRS = 1, kModeAG = 2 };
 
+// L2 eviction priority requested for an operand's TMA loads.
+enum Policy : int { kPolicyNormal = 0, kPolicyEvictFirst = 1, kPolicyEvictLast = 2 };
+
 // Status word codes written by the kernel (workspace offset 0). 0 = OK.
 // A timed-out wait stores kStatusTimeout | (role << 8) | site.
 constexpr uint32_t kStatusTimeout = 0x54000000u;
@@ -47,7 +50,9 @@ struct Params {  // 128-byte aligned through its CUtensorMap members
   int kb_total;                 // k-blocks per tile (AR/RS: sum_r ceil(K_r/BK))
   int splits;                   // pieces per tile (1 = no split-K)
   int units;                    // tiles * splits
-  int group_m;                  // raster group height, in m-tiles
+  int group_m;                  // raster group height, in m-tiles (1 = n fastest)
+  int policy_a;                 // L2 policy of A-operand loads (kPolicy*)
+  int policy_b;                 // L2 policy of B-operand loads (kPolicy*)
   int rps;                      // RS: rows per shard = ceil(M/R)
   int shard_kb_begin[kMaxShards + 1];  // AR/RS: first k-block of shard r
   int shard_mt_begin[kMaxShards + 1];  // AG: first m-tile of shard r
@@ -56,8 +61,11 @@ struct Params {  // 128-byte aligned through its CUtensorMap members
 };
 
 // Host-side launcher (defined with the kernel).
-cudaError_t launch_gemm(const Params& p, int block_n, int ctas, cudaStream_t stream);
-cudaError_t prepare_kernels(int device);
-size_t kernel_smem_bytes(int block_n);
+// cta_group 1: one CTA per 128-row tile; 2: a CTA pair (cluster of two) per
+// 256-row tile. block_n is 128 or 256. `ctas` counts CTAs (even for pairs).
+cudaError_t launch_gemm(const Params& p, int block_n, int cta_group, int ctas, cudaStream_t stream);
+// Sets shared-memory limits and reports how many CTA pairs can be resident.
+cudaError_t prepare_kernels(int device, int* pair_clusters);
+size_t kernel_smem_bytes(int block_n, int cta_group);
 
 }  // namespace gsr

@@ -23,6 +23,7 @@ _PLANS = {}
 
 
 def plan(max_M=34816, max_N=8192, max_K=8192, max_R=16, **options):
+    """Options are GSR_OPT_* names in lower case (split_k, block_n, cta_group, ...)."""
     """A cached plan + initialised workspace for the given maxima and options."""
     key = (max_M, max_N, max_K, max_R, tuple(sorted(options.items())))
     if key not in _PLANS:

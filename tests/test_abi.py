@@ -205,11 +205,21 @@ def test_config_is_independent_of_mode(host):
 def test_small_m_uses_split_k(host):
     d = host.describe(B.MODE_AR, 128, 7168, 0, [896] * 8)
     # 1 x 28 tiles of 128 x 256 on 148 SMs -> 5 pieces per tile, one wave
-    assert d == {"block_n": 256, "split": 5, "units": 140, "ctas": 140}
+    assert d == {"block_n": 256, "split": 5, "units": 140, "ctas": 140, "cta_group": 1}
+
+
+def test_large_m_uses_cta_pairs(host):
+    # whole 256 x 256 tiles per CTA pair; the grid is an even number of CTAs
     d = host.describe(B.MODE_AR, 32768, 7168, 0, [896] * 8)
-    assert d["split"] == 1 and d["units"] == 256 * 28 and d["ctas"] == 148
+    assert d == {"block_n": 256, "split": 1, "units": 128 * 28, "ctas": 148, "cta_group": 2}
     d = host.describe(B.MODE_AG, 0, 6288, 7168, [4096] * 8)
-    assert d["split"] == 1 and d["units"] == 8 * 32 * 25
+    assert d["split"] == 1 and d["cta_group"] == 2 and d["units"] == 8 * 16 * 25
+    # AG pair tiles never cross a shard: 448-row shards take two pair tiles each
+    d = host.describe(B.MODE_AG, 0, 3648, 7168, [448] * 8)
+    assert d["cta_group"] == 2 and d["units"] == 8 * 2 * 15
+    # too few 1-CTA tiles for the SMs: split-K on single CTAs instead
+    d = host.describe(B.MODE_AR, 500, 4096, 0, [896] * 8)
+    assert d["cta_group"] == 1 and d["split"] == 2
 
 
 def test_forced_options(lib):
@@ -230,6 +240,12 @@ def test_forced_options(lib):
         assert e.value.status == B.GSR_ERR_INVALID_VALUE
     B.gemm_shard_plan_set_option(h.plan, B.GSR_OPT_MAX_CTAS, 10)
     assert h.describe(B.MODE_AR, 4096, 1024, 0, [256])["ctas"] == 10
+    B.gemm_shard_plan_set_option(h.plan, B.GSR_OPT_CTA_GROUP, 2)
+    d = h.describe(B.MODE_AR, 1000, 1024, 0, [256, 256])
+    assert d["cta_group"] == 2 and d["ctas"] == 10 and d["units"] == 4 * 8 * 3
+    # forced split on pairs still fits the plan's workspace bound
+    need = 256 + d["units"] * 2 * 128 * d["block_n"] * 4
+    assert need <= B.gemm_shard_workspace_size(h.plan)
 
 
 def test_host_plan_has_no_device_status(host):

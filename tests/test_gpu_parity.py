@@ -15,6 +15,20 @@ from gpu_util import (Guarded, assert_close, bits_of, device, plan, shards_to, t
 
 pytestmark = pytest.mark.gpu
 
+# Kernel configurations every ragged shape runs under (they must all agree with
+# the oracle): the heuristic, CTA pairs with 128- and 256-column tiles, and CTA
+# pairs with split-K.
+VARIANTS = {
+    "auto": {},
+    "pair128": dict(cta_group=2, block_n=128, split_k=1),
+    "pair256": dict(cta_group=2, block_n=256, split_k=1),
+    "pairsplit": dict(max_M=4096, max_N=8192, max_K=8192, max_R=16, cta_group=2, split_k=3),
+}
+
+
+def vplan(variant):
+    return plan(**VARIANTS[variant])
+
 
 def run_ar(inp, p=None, reverse=False):
     p, ws = p or plan()
@@ -75,10 +89,11 @@ AR_SHAPES = [
 ]
 
 
+@pytest.mark.parametrize("variant", list(VARIANTS))
 @pytest.mark.parametrize("M,N,K_r", AR_SHAPES)
-def test_ar_ragged(M, N, K_r):
+def test_ar_ragged(M, N, K_r, variant):
     inp = gi.gaussian_ar(M, N, K_r)
-    Y, _, _ = run_ar(inp)
+    Y, _, _ = run_ar(inp, p=vplan(variant))
     assert_close(to_f64(Y.out), oracle.ar(inp.X_r, inp.W_r), f"ar {M}x{N} K_r={K_r}")
     assert Y.guards_intact()
 
@@ -160,11 +175,12 @@ RS_SHAPES = [
 ]
 
 
+@pytest.mark.parametrize("variant", list(VARIANTS))
 @pytest.mark.parametrize("M,N,K_r", RS_SHAPES)
-def test_rs_matches_oracle_and_ar_bitwise(M, N, K_r):
+def test_rs_matches_oracle_and_ar_bitwise(M, N, K_r, variant):
     inp = gi.gaussian_ar(M, N, K_r)
-    Ys = run_rs(inp)
-    Yar, _, _ = run_ar(inp)
+    Ys = run_rs(inp, p=vplan(variant))
+    Yar, _, _ = run_ar(inp, p=vplan(variant))
     ar_bits = bits_of(Yar.out)
     ref = oracle.rs(inp.X_r, inp.W_r)
     for s, y in enumerate(Ys):
@@ -185,13 +201,15 @@ AG_SHAPES = [
     ([0, 64, 0, 128], 264, 128),
     ([256] * 8, 6288, 1024),
     ([448, 384], 3648, 512),
+    ([300, 5, 700], 520, 256),
 ]
 
 
+@pytest.mark.parametrize("variant", list(VARIANTS))
 @pytest.mark.parametrize("M_r,N,K", AG_SHAPES)
-def test_ag_ragged(M_r, N, K):
+def test_ag_ragged(M_r, N, K, variant):
     inp = gi.gaussian_ag(M_r, N, K)
-    Y = run_ag(inp)
+    Y = run_ag(inp, p=vplan(variant))
     assert_close(to_f64(Y.out), oracle.ag(inp.A_r, inp.W), f"ag M_r={M_r} N={N} K={K}")
     assert Y.guards_intact()
 
