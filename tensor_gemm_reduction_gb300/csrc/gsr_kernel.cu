@@ -765,11 +765,11 @@ __global__ void __launch_bounds__(kThreads, 1) gsr_gemm_kernel(const __grid_cons
   }
 }
 
-// Ring depths: each instance fills about 192 KB of shared memory.
+// Ring depths: each instance fills 192-224 KB of shared memory.
 template <int BN, int CG> struct Stages;
 template <> struct Stages<256, 1> { static constexpr int value = 4; };   // 48 KB stages
 template <> struct Stages<128, 1> { static constexpr int value = 6; };   // 32 KB
-template <> struct Stages<256, 2> { static constexpr int value = 6; };   // 32 KB per CTA
+template <> struct Stages<256, 2> { static constexpr int value = 7; };   // 32 KB per CTA
 template <> struct Stages<128, 2> { static constexpr int value = 8; };   // 24 KB per CTA
 
 template <int BN, int CG>
