@@ -80,8 +80,12 @@ typedef enum {
     GSR_OPT_L2_HINTS = 6,   /* TMA L2 eviction hints: 0 = heuristic, 1 = none,
                                2 = A evict-last / B evict-first,
                                3 = A evict-first / B evict-last                     */
-    GSR_OPT_CTA_GROUP = 7   /* CTAs per MMA tile: 0 = heuristic, 1 = one CTA per
+    GSR_OPT_CTA_GROUP = 7,  /* CTAs per MMA tile: 0 = heuristic, 1 = one CTA per
                                128-row tile, 2 = a CTA pair per 256-row tile        */
+    GSR_OPT_SCHEDULE = 8    /* work schedule: 0 = heuristic (stream-K hybrid),
+                               1 = uniform (every tile cut into the same number
+                               of pieces), 2 = stream-K over the last one or two
+                               waves, 3 = stream-K over the partial last wave    */
 } gsr_option;
 
 /*
@@ -196,13 +200,15 @@ gsr_status gemm_ag(const gemm_shard_plan *plan, int64_t N, int64_t K, int R,
  * of 24 MiB in device global memory, part of the library image: every GPU that
  * loads the library holds it until the process exits. Nothing is allocated or
  * freed by the call.
- *   - A shape whose kernel configuration needs more than 24 MiB of scratch
- *     (for example a forced split-K on many tiles) is rejected with
- *     GSR_ERR_WORKSPACE before anything is launched; use gemm_ar with a
- *     workspace for it. The heuristic configuration always fits when
- *     4 bytes x (ceil(max_M/128) + max_R) x ceil(max_N/128) counters plus
- *     128 KiB per SM stay under 24 MiB (on a 152-SM GB300: plans of up to about
- *     a million output tiles).
+ *   - When the plan's configuration for a shape needs more than 24 MiB of
+ *     scratch, the call runs the uniform schedule instead (the same results
+ *     within rounding; split pieces then need at most one 128 KiB slot per
+ *     SM). A shape that needs more even then (for example a forced split-K on
+ *     many tiles) is rejected with GSR_ERR_WORKSPACE before anything is
+ *     launched; use gemm_ar with a workspace for it. The uniform schedule
+ *     always fits when 4 bytes x (ceil(max_M/128) + 2 max_R) x ceil(max_N/128)
+ *     counters plus 128 KiB per SM stay under 24 MiB (on a 152-SM GB300:
+ *     plans of up to about a million output tiles).
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress), once per device; make that first call before
  *     any stream capture begins.
@@ -231,15 +237,27 @@ gsr_status gemm_shard_check_status(const gemm_shard_plan *plan, void *ws,
 /* Text of the last error on the calling thread ("" if none). Never NULL. */
 const char *gsr_last_error_string(void);
 
-/* Kernel configuration the plan would choose for a call, for logging and
- * tests: mode 0 = AR, 1 = RS, 2 = AG. AR/RS use M and sizes = K_r (K is
- * ignored); AG uses K and sizes = M_r (M is ignored). Writes block_n, split
- * (pieces per output tile), units (work items), ctas (persistent CTAs) and
- * cta_group (1 or 2 CTAs per MMA tile). Any output pointer may be NULL. */
+/* Kernel configuration of a call, as gemm_shard_describe reports it. */
+typedef struct {
+    int block_n;            /* output tile width: 128 or 256                        */
+    int cta_group;          /* 1: a CTA per 128-row tile; 2: a CTA pair per 256 rows */
+    int schedule;           /* 1 = uniform pieces, 2 = stream-K hybrid              */
+    int split;              /* uniform schedule: pieces per tile                    */
+    int64_t tiles;          /* output tiles                                         */
+    int64_t dp_tiles;       /* stream-K: tiles run whole                            */
+    int64_t sk_iters;       /* stream-K: k-blocks shared out over the workers       */
+    int ctas;               /* persistent CTAs launched                             */
+    size_t workspace_bytes; /* workspace this call needs                           */
+} gsr_config;
+
+/* The kernel configuration the plan chooses for a call, for logging and tests:
+ * mode 0 = AR, 1 = RS, 2 = AG. AR/RS use M and sizes = K_r (K is ignored); AG
+ * uses K and sizes = M_r (M is ignored). The configuration depends on the
+ * shape, the device and the plan's options, never on the mode, except that AG
+ * counts tiles per shard. */
 gsr_status gemm_shard_describe(const gemm_shard_plan *plan, int mode, int64_t M,
                                int64_t N, int64_t K, int R, const int64_t *sizes,
-                               int *block_n, int *split, int64_t *units, int *ctas,
-                               int *cta_group);
+                               gsr_config *out);
 
 #ifdef __cplusplus
 }

@@ -32,6 +32,7 @@ GSR_OPT_MAX_CTAS = 4
 GSR_OPT_RASTER_M = 5
 GSR_OPT_L2_HINTS = 6
 GSR_OPT_CTA_GROUP = 7
+GSR_OPT_SCHEDULE = 8
 
 MODE_AR, MODE_RS, MODE_AG = 0, 1, 2
 
@@ -50,6 +51,15 @@ EXPORTED = (
     "gemm_ag", "gemm_shard_check_status", "gsr_last_error_string", "gemm_shard_describe",
     "gemm_ar_noalloc",
 )
+
+
+class GsrConfig(ctypes.Structure):
+    """Mirror of gsr_config (include/gsr.h)."""
+    _fields_ = [("block_n", ctypes.c_int), ("cta_group", ctypes.c_int),
+                ("schedule", ctypes.c_int), ("split", ctypes.c_int),
+                ("tiles", ctypes.c_int64), ("dp_tiles", ctypes.c_int64),
+                ("sk_iters", ctypes.c_int64), ("ctas", ctypes.c_int),
+                ("workspace_bytes", ctypes.c_size_t)]
 
 
 class GsrError(RuntimeError):
@@ -91,9 +101,7 @@ def load_library() -> ctypes.CDLL:
     lib.gemm_shard_check_status.argtypes = [vp, vp, vp]
     lib.gsr_last_error_string.restype = ctypes.c_char_p
     lib.gemm_shard_describe.argtypes = [vp, i32, i64, i64, i64, i32, i64_arr,
-                                        ctypes.POINTER(i32), ctypes.POINTER(i32),
-                                        ctypes.POINTER(i64), ctypes.POINTER(i32),
-                                        ctypes.POINTER(i32)]
+                                        ctypes.POINTER(GsrConfig)]
     for name in EXPORTED:
         if name not in ("gemm_shard_workspace_size", "gsr_last_error_string"):
             getattr(lib, name).restype = i32
@@ -310,10 +318,7 @@ def gemm_shard_describe(plan: Plan, mode: int, M: int, N: int, K: int,
                         sizes: Sequence[int]) -> dict:
     lib = load_library()
     s, sa = _i64s(sizes)
-    bn, sp, ct, cg = ctypes.c_int(), ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
-    un = ctypes.c_int64()
+    cfg = GsrConfig()
     _check(lib.gemm_shard_describe(plan.handle, int(mode), int(M), int(N), int(K), len(sizes), s,
-                                   ctypes.byref(bn), ctypes.byref(sp), ctypes.byref(un),
-                                   ctypes.byref(ct), ctypes.byref(cg)))
-    return {"block_n": bn.value, "split": sp.value, "units": un.value, "ctas": ct.value,
-            "cta_group": cg.value}
+                                   ctypes.byref(cfg)))
+    return {name: getattr(cfg, name) for name, _ in GsrConfig._fields_}

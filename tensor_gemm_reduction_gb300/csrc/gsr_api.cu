@@ -35,6 +35,8 @@ struct gemm_shard_plan {
   int opt_raster_m;    // 0 = heuristic
   int opt_l2_hints;    // 0 = heuristic
   int opt_cta_group;   // 0 = heuristic
+  int opt_schedule;    // 0 = heuristic (stream-K hybrid), 1 = uniform, 2 = stream-K hybrid,
+                       // 3 = stream-K only for a partial last wave
   int pair_clusters;   // CTA pairs that can be resident at once
   uint64_t timeout_ns;
 };
@@ -121,8 +123,10 @@ size_t counters_bytes(const gemm_shard_plan* P) {
 struct Config {
   int block_n = 256;
   int cta_group = 1;
+  int sched = gsr::kSchedUniform;
   int splits = 1;
   int64_t m_tiles = 0, n_tiles = 0, tiles = 0, kb_total = 0, units = 0;
+  int64_t dp_tiles = 0, sk_iters = 0, slots = 0;   // slots: fp32 partial tiles per CTA half
   int ctas = 0;
   int group_m = 1;
   int policy_a = gsr::kPolicyNormal;
@@ -133,12 +137,13 @@ struct Config {
 
 // Kernel configuration: a function of the shape (rows, N, per-shard sizes, R)
 // and the device, never of the mode, so AR and RS on the same inputs run the
-// same tiles, the same split and the same summation order (bit-identical rows).
+// same tiles, the same pieces and the same summation order (bit-identical rows).
 Config choose_config(const gemm_shard_plan* P, int mode, int64_t M, int64_t N, int64_t K_ag, int R,
                      const int64_t* sizes) {
   Config c;
   c.block_n = P->opt_block_n ? P->opt_block_n : (N <= 128 ? 128 : 256);
-  // Tile rows: 128 per CTA; a CTA pair (cta_group 2) covers 256.
+  // Tile rows: 128 per CTA; a CTA pair (cta_group 2) covers 256. AG tiles never
+  // cross a shard.
   auto count_m_tiles = [&](int64_t rows_per_tile) {
     int64_t mt = 0;
     if (mode == gsr::kModeAG) {
@@ -148,49 +153,82 @@ Config choose_config(const gemm_shard_plan* P, int mode, int64_t M, int64_t N, i
     }
     return mt;
   };
+  int64_t rows = 0;
   if (mode == gsr::kModeAG) {
     c.kb_total = cdiv(K_ag, BK);
+    for (int r = 0; r < R; ++r) rows += sizes[r];
   } else {
     for (int r = 0; r < R; ++r) c.kb_total += cdiv(sizes[r], BK);
+    rows = M;
   }
-  c.m_tiles = count_m_tiles(BM);
   c.n_tiles = cdiv(N, c.block_n);
-  c.tiles = c.m_tiles * c.n_tiles;
-  if (P->opt_split) {
-    c.splits = static_cast<int>(std::min<int64_t>(P->opt_split, c.kb_total));
-  } else if (c.tiles >= P->sm_count) {
-    c.splits = 1;
-  } else {
-    // Fewer tiles than SMs (small M): cut each tile's k range into pieces so
-    // that about one piece runs per SM, each at least 4 k-blocks long.
-    int64_t s = P->sm_count / std::max<int64_t>(c.tiles, 1);
-    s = std::min<int64_t>(s, std::max<int64_t>(c.kb_total / 4, 1));
-    s = std::min<int64_t>(s, 16);
-    c.splits = static_cast<int>(std::max<int64_t>(s, 1));
-  }
-  // Whole tiles (no split) at block_n 256 run as CTA pairs: a 256 x 256 tile
-  // per pair halves each SM's bytes of B per flop and deepens the smem ring.
-  if (P->opt_cta_group)
-    c.cta_group = (P->opt_cta_group == 2 && P->pair_clusters > 0) ? 2 : 1;
-  else
-    c.cta_group = (c.splits == 1 && c.block_n == 256 && P->pair_clusters > 0) ? 2 : 1;
-  if (c.cta_group == 2) {
-    c.m_tiles = count_m_tiles(2 * BM);
-    c.tiles = c.m_tiles * c.n_tiles;
-  }
-  c.units = c.tiles * c.splits;
+  const int64_t mt1 = count_m_tiles(BM), mt2 = count_m_tiles(2 * BM);
   const int cap = P->opt_max_ctas ? std::min(P->opt_max_ctas, P->sm_count) : P->sm_count;
-  if (c.cta_group == 2) {
-    const int64_t pairs = std::min<int64_t>({c.units, static_cast<int64_t>(cap / 2),
-                                              static_cast<int64_t>(P->pair_clusters)});
-    c.ctas = static_cast<int>(2 * std::max<int64_t>(pairs, 1));
+
+  // CTA pairs halve each SM's bytes of B per flop and deepen the smem ring; they
+  // run when there are at least as many single-CTA tiles as SMs and 256-row
+  // tiles waste no more rows than 128-row tiles do (AG shards of 384 rows
+  // would leave a quarter of every pair's rows empty).
+  const bool pairs_fit = P->pair_clusters > 0 && cap >= 2;
+  if (P->opt_cta_group) {
+    c.cta_group = (P->opt_cta_group == 2 && pairs_fit) ? 2 : 1;
   } else {
-    c.ctas = static_cast<int>(std::min<int64_t>(c.units, cap));
+    const double eff1 = static_cast<double>(rows) / (mt1 * BM);
+    const double eff2 = static_cast<double>(rows) / (mt2 * 2 * BM);
+    c.cta_group = (pairs_fit && mt1 * c.n_tiles >= P->sm_count && eff2 >= 0.97 * eff1) ? 2 : 1;
   }
+  c.m_tiles = c.cta_group == 2 ? mt2 : mt1;
+  c.tiles = c.m_tiles * c.n_tiles;
+  const int64_t workers =
+      c.cta_group == 2 ? std::min<int64_t>(cap / 2, P->pair_clusters) : static_cast<int64_t>(cap);
+
+  if (P->opt_split || P->opt_schedule == 1) {
+    // Uniform schedule: every tile cut into the same number of pieces.
+    c.sched = gsr::kSchedUniform;
+    if (P->opt_split) {
+      c.splits = static_cast<int>(std::min<int64_t>(P->opt_split, c.kb_total));
+    } else if (c.tiles >= workers) {
+      c.splits = 1;
+    } else {
+      int64_t sp = workers / std::max<int64_t>(c.tiles, 1);
+      sp = std::min<int64_t>(sp, std::max<int64_t>(c.kb_total / 4, 1));
+      c.splits = static_cast<int>(std::max<int64_t>(std::min<int64_t>(sp, 16), 1));
+    }
+    c.units = c.tiles * c.splits;
+    c.dp_tiles = 0;
+    c.sk_iters = 0;
+    c.slots = c.splits > 1 ? c.units : 0;
+    c.ctas = static_cast<int>(c.cta_group * std::min<int64_t>(c.units, workers));
+  } else {
+    // Stream-K hybrid: whole tiles for all but the last one or two waves, then
+    // the remaining tiles' k-blocks cut evenly over every worker.
+    c.sched = gsr::kSchedStreamK;
+    c.splits = 1;
+    const int64_t full = c.tiles / workers, rem = c.tiles % workers;
+    int64_t dp = c.tiles;
+    if (rem != 0) {
+      if (P->opt_schedule == 3)
+        dp = full * workers;                          // only the partial last wave
+      else
+        dp = full >= 2 ? (full - 1) * workers : 0;    // the last one or two waves
+    }
+    int64_t sk_iters = (c.tiles - dp) * c.kb_total;
+    if (sk_iters > 0 && sk_iters < 4 * workers) {   // too little to share out
+      dp = c.tiles;
+      sk_iters = 0;
+    }
+    c.dp_tiles = dp;
+    c.sk_iters = sk_iters;
+    c.units = c.tiles;
+    c.slots = sk_iters > 0 ? (c.tiles - dp) + workers - 1 : 0;
+    c.ctas = static_cast<int>(c.cta_group *
+                              (sk_iters > 0 ? workers : std::min<int64_t>(c.tiles, workers)));
+  }
+  c.ctas = std::max(c.ctas, c.cta_group);
+
   // Raster: groups of group_m m-tiles, m fastest inside a group, so a wave of
-  // concurrent CTAs covers about group_m x (#SMs / group_m) tiles and reads
-  // that many A row-blocks and W column-blocks once each from HBM; the group's
-  // A rows stay in L2 for the group's later waves.
+  // concurrent CTAs covers about group_m x (#workers / group_m) tiles and reads
+  // that many A row-blocks and W column-blocks once each from HBM.
   c.group_m = P->opt_raster_m ? P->opt_raster_m : 16;
   switch (P->opt_l2_hints) {
     case 2:
@@ -207,8 +245,7 @@ Config choose_config(const gemm_shard_plan* P, int mode, int64_t M, int64_t N, i
       break;
   }
   size_t bytes = gsr::kWsHeader + counters_bytes(P);
-  if (c.splits > 1)
-    bytes += static_cast<size_t>(c.units) * c.cta_group * BM * c.block_n * sizeof(float);
+  bytes += static_cast<size_t>(c.slots) * c.cta_group * BM * c.block_n * sizeof(float);
   c.ws_bytes = bytes;
   return c;
 }
@@ -250,6 +287,9 @@ void fill_common(gsr::Params& p, const gemm_shard_plan* P, const Config& c, int 
   p.kb_total = static_cast<int>(c.kb_total);
   p.splits = c.splits;
   p.units = static_cast<int>(c.units);
+  p.sched = c.sched;
+  p.dp_tiles = static_cast<int>(c.dp_tiles);
+  p.sk_iters = c.sk_iters;
   p.group_m = c.group_m;
   p.policy_a = c.policy_a;
   p.policy_b = c.policy_b;
@@ -387,6 +427,7 @@ static gemm_shard_plan* new_plan(int device, int sm_count, int64_t max_M, int64_
   P->opt_raster_m = 0;
   P->opt_l2_hints = 0;
   P->opt_cta_group = 0;
+  P->opt_schedule = 0;
   P->pair_clusters = sm_count / 2;   // host plans: every SM pairs up
   P->timeout_ns = 2000000000ull;
   return P;
@@ -471,6 +512,10 @@ gsr_status gemm_shard_plan_set_option(gemm_shard_plan* plan, gsr_option option, 
       if (value < 0 || value > 2) return fail(GSR_ERR_INVALID_VALUE, "cta_group must be 0..2");
       plan->opt_cta_group = static_cast<int>(value);
       return ok();
+    case GSR_OPT_SCHEDULE:
+      if (value < 0 || value > 3) return fail(GSR_ERR_INVALID_VALUE, "schedule must be 0..3");
+      plan->opt_schedule = static_cast<int>(value);
+      return ok();
   }
   return fail(GSR_ERR_INVALID_VALUE, "unknown option %d", static_cast<int>(option));
 }
@@ -484,10 +529,16 @@ size_t gemm_shard_workspace_size(const gemm_shard_plan* P) {
   const int64_t max_tiles = plan_max_tiles(P);
   size_t bytes = gsr::kWsHeader + counters_bytes(P);
   const size_t slot = static_cast<size_t>(BM) * 256 * sizeof(float);
-  if (P->opt_split > 1)
+  if (P->opt_split > 1) {
     bytes += static_cast<size_t>(max_tiles) * P->opt_split * slot;
-  else
+  } else if (P->opt_schedule == 1) {
+    // uniform heuristic: pieces only while tiles < workers, one slot per CTA
     bytes += static_cast<size_t>(P->sm_count) * slot;
+  } else {
+    // stream-K: fewer than two waves of tiles are cut, plus one piece per
+    // worker boundary: under three slots per CTA
+    bytes += static_cast<size_t>(3) * P->sm_count * slot;
+  }
   return bytes;
 }
 
@@ -606,19 +657,23 @@ gsr_status gemm_shard_check_status(const gemm_shard_plan* P, void* ws, gsr_strea
 }
 
 gsr_status gemm_shard_describe(const gemm_shard_plan* P, int mode, int64_t M, int64_t N, int64_t K,
-                               int R, const int64_t* sizes, int* block_n, int* split,
-                               int64_t* units, int* ctas, int* cta_group) {
+                               int R, const int64_t* sizes, gsr_config* out) {
   gsr_status s = check_plan(P);
   if (s) return s;
+  if (!out) return fail(GSR_ERR_INVALID_VALUE, "out is NULL");
   if (mode < 0 || mode > 2) return fail(GSR_ERR_INVALID_VALUE, "mode must be 0, 1 or 2");
   if (R < 1 || R > kMaxShards || !sizes) return fail(GSR_ERR_INVALID_VALUE, "bad R or sizes");
   if (N < 8 || N % 8) return fail(GSR_ERR_INVALID_VALUE, "N must be a positive multiple of 8");
   const Config c = choose_config(P, mode, M, N, K, R, sizes);
-  if (block_n) *block_n = c.block_n;
-  if (split) *split = c.splits;
-  if (units) *units = c.units;
-  if (ctas) *ctas = c.ctas;
-  if (cta_group) *cta_group = c.cta_group;
+  out->block_n = c.block_n;
+  out->cta_group = c.cta_group;
+  out->schedule = c.sched == gsr::kSchedStreamK ? 2 : 1;
+  out->split = c.splits;
+  out->tiles = c.tiles;
+  out->dp_tiles = c.sched == gsr::kSchedStreamK ? c.dp_tiles : c.tiles;
+  out->sk_iters = c.sk_iters;
+  out->ctas = c.ctas;
+  out->workspace_bytes = c.ws_bytes;
   return ok();
 }
 
@@ -671,12 +726,19 @@ extern "C" gsr_status gemm_ar_noalloc(const gemm_shard_plan* P, int64_t M, int64
   if (s) return s;
   s = check_ksharded(P, M, N, R, K_r, X_r, W_r);
   if (s) return s;
-  const Config c = choose_config(P, gsr::kModeAR, M, N, 0, R, K_r);
+  // The plan's own configuration when its scratch fits; otherwise the uniform
+  // schedule, whose split pieces need at most one 128 KiB slot per SM.
+  gemm_shard_plan fitted = *P;
+  if (choose_config(P, gsr::kModeAR, M, N, 0, R, K_r).ws_bytes > kBuiltinScratchBytes &&
+      P->opt_split == 0)
+    fitted.opt_schedule = 1;
+  const Config c = choose_config(&fitted, gsr::kModeAR, M, N, 0, R, K_r);
   if (c.ws_bytes > kBuiltinScratchBytes)
     return fail(GSR_ERR_WORKSPACE,
                 "this call needs %zu bytes of scratch but the built-in scratch of gemm_ar_noalloc "
                 "holds %zu; use gemm_ar with a workspace of gemm_shard_workspace_size bytes",
                 c.ws_bytes, kBuiltinScratchBytes);
+  P = &fitted;
   if (M == 0) return ok();
   if (P->device < 0) return fail(GSR_ERR_UNSUPPORTED, "host plan: arguments are valid, nothing launched");
   DeviceScope scope(P->device);

@@ -353,7 +353,9 @@ __device__ __noinline__ bool wait_drain(uint32_t bar, uint32_t parity, uint64_t 
 
 struct Unit {
   int tile;       // output tile index (also the split-K counter index)
-  int split;      // piece of the tile's k range
+  int piece;      // which piece of the tile's k range (k order)
+  int npieces;    // pieces the tile is cut into (1 = whole tile)
+  int slot0;      // partial slot of the tile's piece 0 (pieces are consecutive)
   int n0;         // first output column of the tile
   int m0;         // first row of the tile in the A operand: AR/RS global, AG
                   // local to the shard (a CTA pair's tile spans 2 x BM rows)
@@ -362,11 +364,9 @@ struct Unit {
   int kb_end;
 };
 
+// Position of the tile in the output (raster order) and its shard.
 template <int BN, int CG>
-__device__ __forceinline__ Unit decode_unit(const Params& p, int u) {
-  Unit t;
-  t.tile = u / p.splits;
-  t.split = u - t.tile * p.splits;
+__device__ __forceinline__ void place_tile(const Params& p, Unit& t) {
   // Raster: groups of group_m m-tiles; inside a group the m index runs fastest,
   // so CTAs working at the same time share W (B) panels and A rows in L2.
   const int span = p.group_m * p.n_tiles;
@@ -386,9 +386,78 @@ __device__ __forceinline__ Unit decode_unit(const Params& p, int u) {
     t.shard = 0;
     t.m0 = mt * (BM * CG);
   }
-  t.kb_begin = static_cast<int>((static_cast<long long>(t.split) * p.kb_total) / p.splits);
-  t.kb_end = static_cast<int>((static_cast<long long>(t.split + 1) * p.kb_total) / p.splits);
-  return t;
+}
+
+// Per-worker walk over the schedule; every role of a CTA walks it identically.
+struct Sched {
+  int w;              // this worker (CTA, or CTA pair)
+  int G;              // workers
+  int next;           // uniform: next unit; stream-K: next whole tile
+  long long it;       // stream-K: next k-block of this worker's range
+  long long it_end;
+};
+
+template <int CG>
+__device__ __forceinline__ Sched sched_begin(const Params& p) {
+  Sched s;
+  s.w = static_cast<int>(blockIdx.x) / CG;
+  s.G = static_cast<int>(gridDim.x) / CG;
+  s.next = s.w;
+  s.it = (static_cast<long long>(s.w) * p.sk_iters) / s.G;
+  s.it_end = (static_cast<long long>(s.w + 1) * p.sk_iters) / s.G;
+  return s;
+}
+
+// The worker whose stream-K range holds k-block `it` (ranges are
+// [w*I/G, (w+1)*I/G), every one non-empty because I >= G).
+__device__ __forceinline__ int sk_worker_of(long long it, long long I, int G) {
+  return static_cast<int>(((it + 1) * G + I - 1) / I) - 1;
+}
+
+template <int BN, int CG>
+__device__ __forceinline__ bool sched_next(const Params& p, Sched& s, Unit& t) {
+  if (p.sched == kSchedUniform) {
+    if (s.next >= p.units) return false;
+    const int u = s.next;
+    s.next += s.G;
+    t.tile = u / p.splits;
+    t.piece = u - t.tile * p.splits;
+    t.npieces = p.splits;
+    t.slot0 = t.tile * p.splits;
+    t.kb_begin = static_cast<int>((static_cast<long long>(t.piece) * p.kb_total) / p.splits);
+    t.kb_end = static_cast<int>((static_cast<long long>(t.piece + 1) * p.kb_total) / p.splits);
+    place_tile<BN, CG>(p, t);
+    return true;
+  }
+  if (s.next < p.dp_tiles) {           // a whole tile
+    t.tile = s.next;
+    s.next += s.G;
+    t.piece = 0;
+    t.npieces = 1;
+    t.slot0 = 0;
+    t.kb_begin = 0;
+    t.kb_end = p.kb_total;
+    place_tile<BN, CG>(p, t);
+    return true;
+  }
+  if (s.it >= s.it_end) return false;  // the next piece of this worker's range
+  const long long kt = p.kb_total;
+  const int sk_tile = static_cast<int>(s.it / kt);
+  const int k_lo = static_cast<int>(s.it - sk_tile * kt);
+  const int k_hi = static_cast<int>(min(kt, k_lo + (s.it_end - s.it)));
+  s.it += k_hi - k_lo;
+  const int first_w = sk_worker_of(sk_tile * kt, p.sk_iters, s.G);
+  const int last_w = sk_worker_of((sk_tile + 1) * kt - 1, p.sk_iters, s.G);
+  t.tile = p.dp_tiles + sk_tile;
+  t.piece = s.w - first_w;
+  t.npieces = last_w - first_w + 1;
+  // Along the stream-K range each new piece starts a new tile, a new worker's
+  // range, or both, so (tile + worker) numbers the pieces without collisions.
+  t.slot0 = sk_tile + first_w;
+  t.kb_begin = k_lo;
+  t.kb_end = k_hi;
+  place_tile<BN, CG>(p, t);
+  return true;
 }
 
 // MMA N of a tile: the full BN, or the ragged tail rounded up to 16 columns.
@@ -432,11 +501,11 @@ __device__ void run_producer(const Params& p, uint32_t tiles_base, uint32_t bars
   }
   const uint64_t pol_a = make_l2_policy(p.policy_a);
   const uint64_t pol_b = make_l2_policy(p.policy_b);
-  const int stride = static_cast<int>(gridDim.x) / CG;
   uint32_t issued = 0;
   bool ok = true;
-  for (int u = static_cast<int>(blockIdx.x) / CG; u < p.units && ok; u += stride) {
-    const Unit t = decode_unit<BN, CG>(p, u);
+  Sched sch = sched_begin<CG>(p);
+  Unit t;
+  while (ok && sched_next<BN, CG>(p, sch, t)) {
     // This CTA's rows of A, and its columns of B: with a CTA pair the MMA's N
     // columns are split in halves between the two CTAs.
     const int a_row = t.m0 + BM * static_cast<int>(rank);
@@ -497,11 +566,11 @@ __device__ void run_mma(const Params& p, uint32_t tiles_base, uint32_t bars, uin
   using L = Layout<BN, STAGES, CG>;
   const uint32_t full0 = bars, tfull0 = bars + 16 * STAGES, tempty0 = tfull0 + 16;
   const uint32_t empty0 = bars + 8 * STAGES, drain = tempty0 + 16;
-  const int stride = static_cast<int>(gridDim.x) / CG;
   uint32_t consumed = 0, local = 0;
   bool ok = true, issued_any = false;
-  for (int u = static_cast<int>(blockIdx.x) / CG; u < p.units && ok; u += stride, ++local) {
-    const Unit t = decode_unit<BN, CG>(p, u);
+  Sched sch = sched_begin<CG>(p);
+  Unit t;
+  for (; ok && sched_next<BN, CG>(p, sch, t); ++local) {
     const uint32_t acc = local & 1u;
     const uint32_t acc_parity = ((local >> 1) & 1u) ^ 1u;
     if (!wait_bounded(tempty0 + 8 * acc, acc_parity, ctl, (kRoleMma << 8) | 1)) {
@@ -578,10 +647,10 @@ __device__ void run_epilogue(const Params& p, uint32_t bars, uint32_t tmem_base,
   const int quad = (static_cast<int>(threadIdx.x) >> 5) & 3;  // TMEM lanes this warp may read
   const int row_in_tile = quad * 32 + lane;
   const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
-  const int stride = static_cast<int>(gridDim.x) / CG;
   uint32_t local = 0;
-  for (int u = static_cast<int>(blockIdx.x) / CG; u < p.units; u += stride, ++local) {
-    const Unit t = decode_unit<BN, CG>(p, u);
+  Sched sch = sched_begin<CG>(p);
+  Unit t;
+  for (; sched_next<BN, CG>(p, sch, t); ++local) {
     const uint32_t acc = local & 1u;
     const uint32_t acc_parity = (local >> 1) & 1u;
     bool ok = wait_bounded(tfull0 + 8 * acc, acc_parity, ctl, (kRoleEpilogue << 8) | 1);
@@ -624,7 +693,7 @@ __device__ void run_epilogue(const Params& p, uint32_t bars, uint32_t tmem_base,
       }
     };
 
-    if (p.splits == 1) {
+    if (t.npieces == 1) {
       for (int c = 0; c < chunks; ++c) {
         uint32_t v[32];
         tmem_ld_32cols(taddr + 32 * c, v);
@@ -635,11 +704,12 @@ __device__ void run_epilogue(const Params& p, uint32_t bars, uint32_t tmem_base,
       continue;
     }
 
-    // Split-K: publish this CTA's fp32 partial of the tile. Layout inside a
+    // Split tile: publish this CTA's fp32 partial of the tile. Layout inside a
     // slot: [column group of 4][row][4], so a warp's float4 stores are contiguous.
     // A CTA pair keeps one slot and one counter per CTA half.
     const int half = t.tile * CG + static_cast<int>(rank);
-    float* slot = p.partials + (static_cast<size_t>(u) * CG + rank) * (BM * BN);
+    float* slot = p.partials +
+                  (static_cast<size_t>(t.slot0 + t.piece) * CG + rank) * (BM * BN);
     for (int c = 0; c < chunks; ++c) {
       uint32_t v[32];
       tmem_ld_32cols(taddr + 32 * c, v);
@@ -656,18 +726,18 @@ __device__ void run_epilogue(const Params& p, uint32_t bars, uint32_t tmem_base,
     epilogue_bar_sync();
     if (et == 0) {
       const uint32_t before = atomicAdd(&p.counters[half], 1u);
-      *last_flag = (before == static_cast<uint32_t>(p.splits - 1)) ? 1 : 0;
+      *last_flag = (before == static_cast<uint32_t>(t.npieces - 1)) ? 1 : 0;
     }
     epilogue_bar_sync();
     if (*last_flag) {
       __threadfence();
-      // Pieces of this half-tile are units tile*splits + s, slots (unit*CG + rank).
+      // The tile's pieces sit in consecutive slots from slot0, in k order.
       const size_t slot_floats = static_cast<size_t>(BM) * BN;
       const float4* base = reinterpret_cast<const float4*>(p.partials);
       for (int c = 0; c < chunks; ++c) {
         float a[32];
-        for (int s = 0; s < p.splits; ++s) {
-          const size_t sl = (static_cast<size_t>(t.tile) * p.splits + s) * CG + rank;
+        for (int s = 0; s < t.npieces; ++s) {
+          const size_t sl = (static_cast<size_t>(t.slot0) + s) * CG + rank;
           const float4* piece = base + sl * (slot_floats / 4);
 #pragma unroll
           for (int j = 0; j < 8; ++j) {

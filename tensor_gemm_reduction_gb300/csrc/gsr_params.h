@@ -15,6 +15,13 @@ constexpr int kEpilogueThreads = 128;
 
 enum Mode : int { kModeAR = 0, kModeRS = 1, kModeAG = 2 };
 
+// Work schedules. Uniform: unit u = tile * splits + piece, dealt round-robin.
+// Stream-K: tiles [0, dp_tiles) are dealt whole, round-robin; the k-blocks of
+// the remaining tiles, in tile order, are cut into one contiguous range per
+// worker (a CTA, or a CTA pair), and a tile cut by a worker boundary is
+// summed by the last of its pieces to finish, in k order.
+enum Sched : int { kSchedUniform = 0, kSchedStreamK = 1 };
+
 // L2 eviction priority requested for an operand's TMA loads.
 enum Policy : int { kPolicyNormal = 0, kPolicyEvictFirst = 1, kPolicyEvictLast = 2 };
 
@@ -48,8 +55,11 @@ struct Params {  // 128-byte aligned through its CUtensorMap members
   int n_tiles;                  // ceil(N/BN)
   int tiles;                    // m_tiles * n_tiles
   int kb_total;                 // k-blocks per tile (AR/RS: sum_r ceil(K_r/BK))
-  int splits;                   // pieces per tile (1 = no split-K)
-  int units;                    // tiles * splits
+  int splits;                   // uniform schedule: pieces per tile (1 = none)
+  int units;                    // uniform schedule: tiles * splits
+  int sched;                    // kSchedUniform or kSchedStreamK
+  int dp_tiles;                 // stream-K: tiles [0, dp_tiles) run whole, round-robin
+  long long sk_iters;           // stream-K: k-blocks of tiles [dp_tiles, tiles)
   int group_m;                  // raster group height, in m-tiles (1 = n fastest)
   int policy_a;                 // L2 policy of A-operand loads (kPolicy*)
   int policy_b;                 // L2 policy of B-operand loads (kPolicy*)

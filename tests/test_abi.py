@@ -183,15 +183,16 @@ def test_workspace_checks(host):
 
 def test_workspace_size_covers_every_heuristic_config(host):
     # The plan's bound must cover the per-call requirement of every shape.
-    sizes = []
     for M in (1, 7, 127, 128, 129, 257, 1000, 4096, 32768):
         for N in (8, 136, 3648, 6288, 7168, 8192):
             for K_r in ([896] * 8, [8], [4096, 4096], [448] * 16):
                 d = host.describe(B.MODE_AR, M, N, 0, K_r)
-                need = 256 + 4 * 0 + (d["units"] * 128 * d["block_n"] * 4 if d["split"] > 1 else 0)
-                sizes.append(need)
-                assert need <= host.ws_bytes
+                assert d["workspace_bytes"] <= host.ws_bytes
                 assert host.ar(M, N, K_r) == B.GSR_ERR_UNSUPPORTED, B.gsr_last_error_string()
+    for M_r in ([256] * 8, [384] * 8, [4096] * 8, [1, 130, 0, 257]):
+        for N in (3648, 6288):
+            d = host.describe(B.MODE_AG, 0, N, 7168, M_r)
+            assert d["workspace_bytes"] <= host.ws_bytes
 
 
 def test_config_is_independent_of_mode(host):
@@ -202,24 +203,49 @@ def test_config_is_independent_of_mode(host):
             assert a == r
 
 
-def test_small_m_uses_split_k(host):
+def test_small_m_shares_k_over_every_sm(host):
+    # 28 tiles of 128 x 256 on 148 SMs: every tile's 112 k-blocks go to the
+    # stream-K region, about 21 k-blocks per CTA
     d = host.describe(B.MODE_AR, 128, 7168, 0, [896] * 8)
-    # 1 x 28 tiles of 128 x 256 on 148 SMs -> 5 pieces per tile, one wave
-    assert d == {"block_n": 256, "split": 5, "units": 140, "ctas": 140, "cta_group": 1}
+    assert d["cta_group"] == 1 and d["schedule"] == 2 and d["tiles"] == 28
+    assert d["dp_tiles"] == 0 and d["sk_iters"] == 28 * 112 and d["ctas"] == 148
 
 
-def test_large_m_uses_cta_pairs(host):
-    # whole 256 x 256 tiles per CTA pair; the grid is an even number of CTAs
+def test_uniform_schedule_splits_small_m(lib):
+    h = Host(lib)
+    B.gemm_shard_plan_set_option(h.plan, B.GSR_OPT_SCHEDULE, 1)
+    d = h.describe(B.MODE_AR, 128, 7168, 0, [896] * 8)
+    assert (d["schedule"], d["split"], d["ctas"], d["cta_group"]) == (1, 5, 140, 1)
+    assert d["workspace_bytes"] <= B.gemm_shard_workspace_size(h.plan)
+
+
+def test_large_m_uses_cta_pairs_and_a_stream_k_tail(host):
+    # 256 x 256 tiles per CTA pair: 128 x 28 = 3584 tiles on 74 pairs is 48.4
+    # waves; the last 1.4 waves (106 tiles) are shared out k-block by k-block
     d = host.describe(B.MODE_AR, 32768, 7168, 0, [896] * 8)
-    assert d == {"block_n": 256, "split": 1, "units": 128 * 28, "ctas": 148, "cta_group": 2}
+    assert d["cta_group"] == 2 and d["schedule"] == 2 and d["ctas"] == 148
+    assert d["tiles"] == 3584 and d["dp_tiles"] == 47 * 74 and d["sk_iters"] == 106 * 112
     d = host.describe(B.MODE_AG, 0, 6288, 7168, [4096] * 8)
-    assert d["split"] == 1 and d["cta_group"] == 2 and d["units"] == 8 * 16 * 25
-    # AG pair tiles never cross a shard: 448-row shards take two pair tiles each
+    assert d["cta_group"] == 2 and d["tiles"] == 8 * 16 * 25
+    # 448-row shards: two pair tiles each, 87.5 % of rows used, as with 128-row tiles
     d = host.describe(B.MODE_AG, 0, 3648, 7168, [448] * 8)
-    assert d["cta_group"] == 2 and d["units"] == 8 * 2 * 15
-    # too few 1-CTA tiles for the SMs: split-K on single CTAs instead
-    d = host.describe(B.MODE_AR, 500, 4096, 0, [896] * 8)
-    assert d["cta_group"] == 1 and d["split"] == 2
+    assert d["cta_group"] == 2 and d["tiles"] == 8 * 2 * 15
+    # 384-row shards would leave a quarter of every pair's rows empty: single CTAs
+    d = host.describe(B.MODE_AG, 0, 3648, 7168, [384] * 8)
+    assert d["cta_group"] == 1 and d["tiles"] == 8 * 3 * 15
+
+
+def test_whole_waves_have_no_stream_k(lib):
+    h = Host(lib, sm=16)
+    d = h.describe(B.MODE_AR, 2048, 4096, 0, [256])   # 8 x 16 = 128 pair tiles on 8 pairs
+    assert d["cta_group"] == 2 and d["dp_tiles"] == 128 and d["sk_iters"] == 0
+    B.gemm_shard_plan_set_option(h.plan, B.GSR_OPT_SCHEDULE, 3)
+    d = h.describe(B.MODE_AR, 2304, 4096, 0, [256])   # 9 x 16 = 144 pair tiles on 8 pairs
+    assert d["dp_tiles"] == 144 and d["sk_iters"] == 0
+    d = h.describe(B.MODE_AR, 2560, 4096, 0, [256])   # 10 x 16 = 160 = 20 waves
+    assert d["sk_iters"] == 0
+    d = h.describe(B.MODE_AR, 2304, 4000, 0, [256])   # 9 x 16 tiles, 4000 wide: same tiles
+    assert d["sk_iters"] == 0
 
 
 def test_forced_options(lib):
@@ -229,12 +255,14 @@ def test_forced_options(lib):
     B.gemm_shard_plan_set_option(h.plan, B.GSR_OPT_BLOCK_N, 128)
     assert B.gemm_shard_workspace_size(h.plan) > base
     d = h.describe(B.MODE_AR, 1000, 1024, 0, [256, 256])
-    assert d["split"] == 3 and d["block_n"] == 128 and d["units"] == 8 * 8 * 3
+    assert d["split"] == 3 and d["block_n"] == 128 and d["schedule"] == 1
+    assert d["tiles"] == 8 * 8 and d["cta_group"] == 1
     # a forced split never exceeds the number of k-blocks
     d = h.describe(B.MODE_AR, 64, 256, 0, [64])
     assert d["split"] == 1
     for opt, bad in ((B.GSR_OPT_SPLIT_K, 17), (B.GSR_OPT_BLOCK_N, 64), (B.GSR_OPT_TIMEOUT_NS, -1),
-                     (B.GSR_OPT_MAX_CTAS, -5), (99, 1)):
+                     (B.GSR_OPT_MAX_CTAS, -5), (B.GSR_OPT_SCHEDULE, 4), (B.GSR_OPT_CTA_GROUP, 3),
+                     (99, 1)):
         with pytest.raises(B.GsrError) as e:
             B.gemm_shard_plan_set_option(h.plan, opt, bad)
         assert e.value.status == B.GSR_ERR_INVALID_VALUE
@@ -242,10 +270,8 @@ def test_forced_options(lib):
     assert h.describe(B.MODE_AR, 4096, 1024, 0, [256])["ctas"] == 10
     B.gemm_shard_plan_set_option(h.plan, B.GSR_OPT_CTA_GROUP, 2)
     d = h.describe(B.MODE_AR, 1000, 1024, 0, [256, 256])
-    assert d["cta_group"] == 2 and d["ctas"] == 10 and d["units"] == 4 * 8 * 3
-    # forced split on pairs still fits the plan's workspace bound
-    need = 256 + d["units"] * 2 * 128 * d["block_n"] * 4
-    assert need <= B.gemm_shard_workspace_size(h.plan)
+    assert d["cta_group"] == 2 and d["ctas"] == 10 and d["tiles"] == 4 * 8
+    assert d["workspace_bytes"] <= B.gemm_shard_workspace_size(h.plan)
 
 
 def test_host_plan_has_no_device_status(host):

@@ -16,12 +16,17 @@ from gpu_util import (Guarded, assert_close, bits_of, device, plan, shards_to, t
 pytestmark = pytest.mark.gpu
 
 # Kernel configurations every ragged shape runs under (they must all agree with
-# the oracle): the heuristic, CTA pairs with 128- and 256-column tiles, and CTA
-# pairs with split-K.
+# the oracle): the heuristic; the uniform schedule; stream-K on only 8 CTAs (so
+# that even small shapes cut tiles into several pieces); CTA pairs with 128-
+# and 256-column whole tiles; CTA pairs with stream-K; CTA pairs with a
+# uniform 3-way split.
 VARIANTS = {
     "auto": {},
-    "pair128": dict(cta_group=2, block_n=128, split_k=1),
-    "pair256": dict(cta_group=2, block_n=256, split_k=1),
+    "uniform": dict(schedule=1),
+    "sk8": dict(schedule=2, max_ctas=8),
+    "pair128": dict(cta_group=2, block_n=128, schedule=1),
+    "pair256": dict(cta_group=2, block_n=256, schedule=1),
+    "pairsk8": dict(cta_group=2, schedule=2, max_ctas=8),
     "pairsplit": dict(max_M=4096, max_N=8192, max_K=8192, max_R=16, cta_group=2, split_k=3),
 }
 
@@ -250,10 +255,11 @@ def test_split_k_ag_and_block_n_128():
 
 
 def test_heuristic_split_small_m_matches_oracle():
-    """M=128, N=7168, 8 shards of 896: the plan splits each tile's k range."""
+    """M=128, N=7168, 8 shards of 896: the plan shares every tile's k range out
+    over all SMs (stream-K)."""
     p, ws = plan()
     d = B.gemm_shard_describe(p, B.MODE_AR, 128, 7168, 0, [896] * 8)
-    assert d["split"] > 1
+    assert d["sk_iters"] > 0 and d["dp_tiles"] == 0
     inp = gi.gaussian_ar(128, 7168, [896] * 8, seed=99)
     Y, _, _ = run_ar(inp)
     assert_close(to_f64(Y.out), oracle.ar(inp.X_r, inp.W_r), "ar m128 split")
