@@ -82,10 +82,11 @@ typedef enum {
                                3 = A evict-first / B evict-last                     */
     GSR_OPT_CTA_GROUP = 7,  /* CTAs per MMA tile: 0 = heuristic, 1 = one CTA per
                                128-row tile, 2 = a CTA pair per 256-row tile        */
-    GSR_OPT_SCHEDULE = 8    /* work schedule: 0 = heuristic (stream-K hybrid),
-                               1 = uniform (every tile cut into the same number
-                               of pieces), 2 = stream-K over the last one or two
-                               waves, 3 = stream-K over the partial last wave    */
+    GSR_OPT_SCHEDULE = 8    /* work schedule: 0 = heuristic (stream-K over the
+                               partial last wave), 1 = uniform (every tile cut
+                               into the same number of pieces), 2 = stream-K
+                               over the last one or two waves, 3 = stream-K
+                               over the partial last wave                        */
 } gsr_option;
 
 /*

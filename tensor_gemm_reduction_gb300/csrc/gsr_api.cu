@@ -170,19 +170,25 @@ Config choose_config(const gemm_shard_plan* P, int mode, int64_t M, int64_t N, i
   // tiles waste no more rows than 128-row tiles do (AG shards of 384 rows
   // would leave a quarter of every pair's rows empty).
   const bool pairs_fit = P->pair_clusters > 0 && cap >= 2;
+  // With fewer single-CTA tiles than SMs (small M) the kernel streams W at HBM
+  // bandwidth: CTA pairs cut into a few uniform pieces measured fastest there
+  // (fewer partial tiles to sum than stream-K's pieces of every tile).
+  const bool small = mt1 * c.n_tiles < P->sm_count;
   if (P->opt_cta_group) {
     c.cta_group = (P->opt_cta_group == 2 && pairs_fit) ? 2 : 1;
+  } else if (small) {
+    c.cta_group = pairs_fit && c.block_n == 256 ? 2 : 1;
   } else {
     const double eff1 = static_cast<double>(rows) / (mt1 * BM);
     const double eff2 = static_cast<double>(rows) / (mt2 * 2 * BM);
-    c.cta_group = (pairs_fit && mt1 * c.n_tiles >= P->sm_count && eff2 >= 0.97 * eff1) ? 2 : 1;
+    c.cta_group = (pairs_fit && eff2 >= 0.97 * eff1) ? 2 : 1;
   }
   c.m_tiles = c.cta_group == 2 ? mt2 : mt1;
   c.tiles = c.m_tiles * c.n_tiles;
   const int64_t workers =
       c.cta_group == 2 ? std::min<int64_t>(cap / 2, P->pair_clusters) : static_cast<int64_t>(cap);
 
-  if (P->opt_split || P->opt_schedule == 1) {
+  if (P->opt_split || P->opt_schedule == 1 || (P->opt_schedule == 0 && small)) {
     // Uniform schedule: every tile cut into the same number of pieces.
     c.sched = gsr::kSchedUniform;
     if (P->opt_split) {
@@ -200,17 +206,19 @@ Config choose_config(const gemm_shard_plan* P, int mode, int64_t M, int64_t N, i
     c.slots = c.splits > 1 ? c.units : 0;
     c.ctas = static_cast<int>(c.cta_group * std::min<int64_t>(c.units, workers));
   } else {
-    // Stream-K hybrid: whole tiles for all but the last one or two waves, then
-    // the remaining tiles' k-blocks cut evenly over every worker.
+    // Stream-K hybrid: whole tiles for every full wave, then the k-blocks of
+    // the partial last wave cut evenly over every worker (schedule 2 shares
+    // out the last one or two waves instead). Fewer cut tiles mean fewer
+    // partial tiles to publish and sum.
     c.sched = gsr::kSchedStreamK;
     c.splits = 1;
     const int64_t full = c.tiles / workers, rem = c.tiles % workers;
     int64_t dp = c.tiles;
     if (rem != 0) {
-      if (P->opt_schedule == 3)
-        dp = full * workers;                          // only the partial last wave
-      else
+      if (P->opt_schedule == 2)
         dp = full >= 2 ? (full - 1) * workers : 0;    // the last one or two waves
+      else
+        dp = full * workers;                          // only the partial last wave
     }
     int64_t sk_iters = (c.tiles - dp) * c.kb_total;
     if (sk_iters > 0 && sk_iters < 4 * workers) {   // too little to share out

@@ -183,6 +183,12 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&v)[32]) {
                : "memory");
 }
 
+__device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 // Named barrier over the 128 epilogue threads.
 __device__ __forceinline__ void epilogue_bar_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kEpilogueThreads) : "memory");
@@ -704,50 +710,75 @@ __device__ void run_epilogue(const Params& p, uint32_t bars, uint32_t tmem_base,
       continue;
     }
 
-    // Split tile: publish this CTA's fp32 partial of the tile. Layout inside a
-    // slot: [column group of 4][row][4], so a warp's float4 stores are contiguous.
-    // A CTA pair keeps one slot and one counter per CTA half.
+    // Split tile. A piece that finds every other piece already published is
+    // the last: it keeps its own accumulator in TMEM and writes no partial.
+    // Otherwise it publishes its fp32 partial (slot layout [column group of
+    // 4][row][4], so a warp's float4 stores are contiguous), fences, and bumps
+    // the tile's counter; the piece that brings the counter to npieces - 1 is
+    // the last. The last piece sums all pieces in k order (its own from TMEM)
+    // and stores the tile. A CTA pair keeps one slot and one counter per half.
     const int half = t.tile * CG + static_cast<int>(rank);
-    float* slot = p.partials +
-                  (static_cast<size_t>(t.slot0 + t.piece) * CG + rank) * (BM * BN);
-    for (int c = 0; c < chunks; ++c) {
-      uint32_t v[32];
-      tmem_ld_32cols(taddr + 32 * c, v);
-      tmem_ld_wait(v);
+    const uint32_t others = static_cast<uint32_t>(t.npieces - 1);
+    if (et == 0) *last_flag = (ld_relaxed_gpu(&p.counters[half]) == others) ? 1 : 0;
+    epilogue_bar_sync();
+    bool last = *last_flag != 0;
+    if (!last) {
+      float* slot = p.partials +
+                    (static_cast<size_t>(t.slot0 + t.piece) * CG + rank) * (BM * BN);
+      for (int c = 0; c < chunks; ++c) {
+        uint32_t v[32];
+        tmem_ld_32cols(taddr + 32 * c, v);
+        tmem_ld_wait(v);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        float4 f = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                               __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
-        __stcg(reinterpret_cast<float4*>(slot) + (8 * c + j) * BM + row_in_tile, f);
+        for (int j = 0; j < 8; ++j) {
+          float4 f = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                 __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+          __stcg(reinterpret_cast<float4*>(slot) + (8 * c + j) * BM + row_in_tile, f);
+        }
       }
+      __threadfence();
+      epilogue_bar_sync();
+      if (et == 0) *last_flag = (atomicAdd(&p.counters[half], 1u) == others) ? 1 : 0;
+      epilogue_bar_sync();
+      last = *last_flag != 0;
     }
-    release_accumulator();  // the accumulator is free for the next tile
-    __threadfence();
-    epilogue_bar_sync();
-    if (et == 0) {
-      const uint32_t before = atomicAdd(&p.counters[half], 1u);
-      *last_flag = (before == static_cast<uint32_t>(t.npieces - 1)) ? 1 : 0;
-    }
-    epilogue_bar_sync();
-    if (*last_flag) {
+    if (last) {
       __threadfence();
       // The tile's pieces sit in consecutive slots from slot0, in k order.
-      const size_t slot_floats = static_cast<size_t>(BM) * BN;
       const float4* base = reinterpret_cast<const float4*>(p.partials);
-      for (int c = 0; c < chunks; ++c) {
-        float a[32];
-        for (int s = 0; s < t.npieces; ++s) {
-          const size_t sl = (static_cast<size_t>(t.slot0) + s) * CG + rank;
-          const float4* piece = base + sl * (slot_floats / 4);
+      const size_t slot_f4 = static_cast<size_t>(BM) * BN / 4;
+      auto load_piece = [&](int s, int c, float (&d)[32]) {
+        if (s == t.piece) {
+          uint32_t v[32];
+          tmem_ld_32cols(taddr + 32 * c, v);
+          tmem_ld_wait(v);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) d[j] = __uint_as_float(v[j]);
+        } else {
+          const float4* src = base + ((static_cast<size_t>(t.slot0) + s) * CG + rank) * slot_f4;
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            const float4 f = __ldcg(piece + (8 * c + j) * BM + row_in_tile);
-            if (s == 0) {
-              a[4 * j] = f.x; a[4 * j + 1] = f.y; a[4 * j + 2] = f.z; a[4 * j + 3] = f.w;
-            } else {
-              a[4 * j] += f.x; a[4 * j + 1] += f.y; a[4 * j + 2] += f.z; a[4 * j + 3] += f.w;
-            }
+            const float4 f = __ldcg(src + (8 * c + j) * BM + row_in_tile);
+            d[4 * j] = f.x; d[4 * j + 1] = f.y; d[4 * j + 2] = f.z; d[4 * j + 3] = f.w;
           }
+        }
+      };
+      for (int c = 0; c < chunks; ++c) {
+        float a[32], b[32], d[32];
+        load_piece(0, c, a);
+        int s = 1;
+        for (; s + 1 < t.npieces; s += 2) {   // two pieces in flight, summed in order
+          load_piece(s, c, b);
+          load_piece(s + 1, c, d);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) a[j] += b[j];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) a[j] += d[j];
+        }
+        if (s < t.npieces) {
+          load_piece(s, c, b);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) a[j] += b[j];
         }
         uint32_t v[32];
 #pragma unroll
@@ -756,6 +787,7 @@ __device__ void run_epilogue(const Params& p, uint32_t bars, uint32_t tmem_base,
       }
       if (et == 0) atomicExch(&p.counters[half], 0u);  // ready for the next call
     }
+    release_accumulator();  // the TMEM accumulator is free for the next tile
   }
 }
 

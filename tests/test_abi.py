@@ -203,10 +203,16 @@ def test_config_is_independent_of_mode(host):
             assert a == r
 
 
-def test_small_m_shares_k_over_every_sm(host):
-    # 28 tiles of 128 x 256 on 148 SMs: every tile's 112 k-blocks go to the
-    # stream-K region, about 21 k-blocks per CTA
+def test_small_m_splits_pair_tiles(host):
+    # 28 single-CTA tiles < 148 SMs: 28 pair tiles (256 x 256, half the rows
+    # empty), each cut into 74 // 28 = 2 pieces of 56 k-blocks: 112 CTAs
     d = host.describe(B.MODE_AR, 128, 7168, 0, [896] * 8)
+    assert (d["cta_group"], d["schedule"], d["split"], d["tiles"], d["ctas"]) == (2, 1, 2, 28, 112)
+    # stream-K on demand: every tile's 112 k-blocks shared out over all SMs
+    plan2 = B.gemm_shard_plan_create_host(148, 32768, 8192, 8192, 16)
+    B.gemm_shard_plan_set_option(plan2, B.GSR_OPT_SCHEDULE, 3)
+    B.gemm_shard_plan_set_option(plan2, B.GSR_OPT_CTA_GROUP, 1)
+    d = B.gemm_shard_describe(plan2, B.MODE_AR, 128, 7168, 0, [896] * 8)
     assert d["cta_group"] == 1 and d["schedule"] == 2 and d["tiles"] == 28
     assert d["dp_tiles"] == 0 and d["sk_iters"] == 28 * 112 and d["ctas"] == 148
 
@@ -221,10 +227,14 @@ def test_uniform_schedule_splits_small_m(lib):
 
 def test_large_m_uses_cta_pairs_and_a_stream_k_tail(host):
     # 256 x 256 tiles per CTA pair: 128 x 28 = 3584 tiles on 74 pairs is 48.4
-    # waves; the last 1.4 waves (106 tiles) are shared out k-block by k-block
+    # waves; the partial last wave (32 tiles) is shared out k-block by k-block
     d = host.describe(B.MODE_AR, 32768, 7168, 0, [896] * 8)
     assert d["cta_group"] == 2 and d["schedule"] == 2 and d["ctas"] == 148
-    assert d["tiles"] == 3584 and d["dp_tiles"] == 47 * 74 and d["sk_iters"] == 106 * 112
+    assert d["tiles"] == 3584 and d["dp_tiles"] == 48 * 74 and d["sk_iters"] == 32 * 112
+    plan2 = B.gemm_shard_plan_create_host(148, 32768, 8192, 8192, 16)
+    B.gemm_shard_plan_set_option(plan2, B.GSR_OPT_SCHEDULE, 2)   # the last 1.4 waves
+    d = B.gemm_shard_describe(plan2, B.MODE_AR, 32768, 7168, 0, [896] * 8)
+    assert d["dp_tiles"] == 47 * 74 and d["sk_iters"] == 106 * 112
     d = host.describe(B.MODE_AG, 0, 6288, 7168, [4096] * 8)
     assert d["cta_group"] == 2 and d["tiles"] == 8 * 16 * 25
     # 448-row shards: two pair tiles each, 87.5 % of rows used, as with 128-row tiles
@@ -239,7 +249,7 @@ def test_whole_waves_have_no_stream_k(lib):
     h = Host(lib, sm=16)
     d = h.describe(B.MODE_AR, 2048, 4096, 0, [256])   # 8 x 16 = 128 pair tiles on 8 pairs
     assert d["cta_group"] == 2 and d["dp_tiles"] == 128 and d["sk_iters"] == 0
-    B.gemm_shard_plan_set_option(h.plan, B.GSR_OPT_SCHEDULE, 3)
+    B.gemm_shard_plan_set_option(h.plan, B.GSR_OPT_SCHEDULE, 2)
     d = h.describe(B.MODE_AR, 2304, 4096, 0, [256])   # 9 x 16 = 144 pair tiles on 8 pairs
     assert d["dp_tiles"] == 144 and d["sk_iters"] == 0
     d = h.describe(B.MODE_AR, 2560, 4096, 0, [256])   # 10 x 16 = 160 = 20 waves

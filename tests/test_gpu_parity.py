@@ -255,11 +255,11 @@ def test_split_k_ag_and_block_n_128():
 
 
 def test_heuristic_split_small_m_matches_oracle():
-    """M=128, N=7168, 8 shards of 896: the plan shares every tile's k range out
-    over all SMs (stream-K)."""
+    """M=128, N=7168, 8 shards of 896: the plan cuts every tile's k range into
+    pieces summed in k order."""
     p, ws = plan()
     d = B.gemm_shard_describe(p, B.MODE_AR, 128, 7168, 0, [896] * 8)
-    assert d["sk_iters"] > 0 and d["dp_tiles"] == 0
+    assert d["split"] > 1 or d["sk_iters"] > 0
     inp = gi.gaussian_ar(128, 7168, [896] * 8, seed=99)
     Y, _, _ = run_ar(inp)
     assert_close(to_f64(Y.out), oracle.ar(inp.X_r, inp.W_r), "ar m128 split")
