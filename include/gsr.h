@@ -191,6 +191,39 @@ gsr_status gemm_ag(const gemm_shard_plan *plan, int64_t N, int64_t K, int R,
                    void *ws, size_t ws_bytes, gsr_stream_t stream);
 
 /*
+ * AG whose shards may still be arriving when the call starts: the single-kernel
+ * AG-GEMM with in-kernel waiting that the AG-GEMM page names as future work
+ * ("[Kimi-K3] AG-GEMM for Sequence Parallelism", Component breakdown, closing
+ * remark). Before the kernel reads any row of A_r it waits until the device
+ * word ready[r] reaches `epoch` (compared with wrap-around: (int32)(ready[r] -
+ * epoch) >= 0), so the copies that bring the shards in (a copy stream, in shard
+ * order) overlap the GEMM on the shards already present. Pass a new epoch per
+ * call instead of resetting the flags.
+ *   ready  device array of R uint32 words, 4-byte aligned; written by another
+ *          agent, typically gemm_shard_signal on the copy stream
+ * The wait is bounded by the plan's timeout (GSR_OPT_TIMEOUT_NS): if a flag
+ * never arrives the kernel records GSR_ERR_TIMEOUT in the workspace status
+ * word, lets its in-flight copies land, frees its resources and returns;
+ * gemm_shard_check_status reports it and the workspace must be re-initialised.
+ * Y is then incomplete. Arguments otherwise as gemm_ag.
+ */
+gsr_status gemm_ag_flagged(const gemm_shard_plan *plan, int64_t N, int64_t K, int R,
+                           const int64_t *M_r, const void *const *A_r, const void *W, void *Y,
+                           const uint32_t *ready, uint32_t epoch, void *ws, size_t ws_bytes,
+                           gsr_stream_t stream);
+
+/*
+ * Enqueue on `stream` a write of `value` to the device word `flag`, after all
+ * earlier work on the stream and behind a system-wide memory fence. It is a
+ * stream memory operation (cuStreamWriteValue32): it runs no kernel, so it can
+ * signal a kernel that occupies every SM, such as gemm_ag_flagged.
+ * GSR_ERR_INVALID_VALUE for a NULL or misaligned flag; GSR_ERR_UNSUPPORTED on
+ * a host plan or a driver without stream memory operations.
+ */
+gsr_status gemm_shard_signal(const gemm_shard_plan *plan, uint32_t *flag, uint32_t value,
+                             gsr_stream_t stream);
+
+/*
  * AR exactly as gemm_ar, for callers that cannot allocate device memory: there
  * is no workspace argument. (The pages have no counterpart; this entry point
  * exists for callers such as an inference engine that claims all free HBM for

@@ -49,7 +49,7 @@ EXPORTED = (
     "gemm_shard_plan_create", "gemm_shard_plan_create_host", "gemm_shard_plan_destroy", "gemm_shard_plan_set_option",
     "gemm_shard_workspace_size", "gemm_shard_workspace_init", "gemm_ar", "gemm_rs",
     "gemm_ag", "gemm_shard_check_status", "gsr_last_error_string", "gemm_shard_describe",
-    "gemm_ar_noalloc",
+    "gemm_ar_noalloc", "gemm_ag_flagged", "gemm_shard_signal",
 )
 
 
@@ -98,6 +98,9 @@ def load_library() -> ctypes.CDLL:
     lib.gemm_rs.argtypes = [vp, i64, i64, i32, i64_arr, ptr_arr, ptr_arr, ptr_arr, vp, sz, vp]
     lib.gemm_ag.argtypes = [vp, i64, i64, i32, i64_arr, ptr_arr, vp, vp, vp, sz, vp]
     lib.gemm_ar_noalloc.argtypes = [vp, i64, i64, i32, i64_arr, ptr_arr, ptr_arr, vp, vp]
+    lib.gemm_ag_flagged.argtypes = [vp, i64, i64, i32, i64_arr, ptr_arr, vp, vp, vp,
+                                    ctypes.c_uint32, vp, sz, vp]
+    lib.gemm_shard_signal.argtypes = [vp, vp, ctypes.c_uint32, vp]
     lib.gemm_shard_check_status.argtypes = [vp, vp, vp]
     lib.gsr_last_error_string.restype = ctypes.c_char_p
     lib.gemm_shard_describe.argtypes = [vp, i32, i64, i64, i64, i32, i64_arr,
@@ -307,6 +310,52 @@ def gemm_ag(plan: Plan, A_r: Sequence[torch.Tensor], W: torch.Tensor, Y: torch.T
     _check(load_library().gemm_ag(plan.handle, N, K, R, m, ap, ctypes.c_void_p(W.data_ptr()),
                                   ctypes.c_void_p(Y.data_ptr()), wsp, wsn, _stream(stream)))
     return Y
+
+
+def _ag_args(A_r, W, Y):
+    R = len(A_r)
+    if R == 0:
+        raise ValueError("need at least one shard")
+    _bf16_2d(W, "W")
+    _bf16_2d(Y, "Y")
+    N, K = W.shape
+    M_r = []
+    for r, a in enumerate(A_r):
+        if a.numel() == 0:
+            M_r.append(0)
+            continue
+        _bf16_2d(a, f"A_r[{r}]")
+        if a.shape[1] != K:
+            raise ValueError(f"A_r[{r}] must have K={K} columns")
+        M_r.append(a.shape[0])
+    if Y.shape != (sum(M_r), N):
+        raise ValueError(f"Y must be {sum(M_r)} x {N}")
+    return N, K, M_r
+
+
+def gemm_ag_flagged(plan: Plan, A_r: Sequence[torch.Tensor], W: torch.Tensor, Y: torch.Tensor,
+                    ready: torch.Tensor, epoch: int, ws: torch.Tensor, stream=None) -> torch.Tensor:
+    """gemm_ag that waits in the kernel until ready[r] reaches epoch before reading A_r.
+    `ready` is a CUDA int32/uint32 tensor of R words."""
+    N, K, M_r = _ag_args(A_r, W, Y)
+    if not ready.is_cuda or ready.numel() < len(A_r) or ready.element_size() != 4:
+        raise ValueError("ready must be a CUDA tensor of R 32-bit words")
+    m, ma = _i64s(M_r)
+    ap, aa = _ptrs([a if a.numel() else None for a in A_r])
+    wsp, wsn = _ws(ws)
+    _check(load_library().gemm_ag_flagged(plan.handle, N, K, len(A_r), m, ap,
+                                          ctypes.c_void_p(W.data_ptr()),
+                                          ctypes.c_void_p(Y.data_ptr()),
+                                          ctypes.c_void_p(ready.data_ptr()),
+                                          ctypes.c_uint32(epoch & 0xFFFFFFFF), wsp, wsn,
+                                          _stream(stream)))
+    return Y
+
+
+def gemm_shard_signal(plan: Plan, flag_ptr: int, value: int, stream=None) -> None:
+    """Enqueue a write of `value` to the device word at `flag_ptr` on `stream`."""
+    _check(load_library().gemm_shard_signal(plan.handle, ctypes.c_void_p(int(flag_ptr)),
+                                            ctypes.c_uint32(value & 0xFFFFFFFF), _stream(stream)))
 
 
 def gemm_shard_check_status(plan: Plan, ws: torch.Tensor, stream=None) -> None:

@@ -83,6 +83,24 @@ EncodeTiledFn encode_fn() {
   return g_encode;
 }
 
+// cuStreamWriteValue32: a stream memory operation that writes a word without
+// running a kernel.
+typedef CUresult (*WriteValueFn)(CUstream, CUdeviceptr, cuuint32_t, unsigned int);
+WriteValueFn g_write_value = nullptr;
+std::once_flag g_write_value_once;
+
+WriteValueFn write_value_fn() {
+  std::call_once(g_write_value_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuStreamWriteValue32", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_write_value = reinterpret_cast<WriteValueFn>(fn);
+  });
+  return g_write_value;
+}
+
 // Restores the caller's current device on scope exit.
 struct DeviceScope {
   int prev = -1;
@@ -582,9 +600,9 @@ gsr_status gemm_rs(const gemm_shard_plan* plan, int64_t M, int64_t N, int R, con
                       stream);
 }
 
-gsr_status gemm_ag(const gemm_shard_plan* P, int64_t N, int64_t K, int R, const int64_t* M_r,
-                   const void* const* A_r, const void* W, void* Y, void* ws, size_t ws_bytes,
-                   gsr_stream_t stream) {
+static gsr_status run_ag(const gemm_shard_plan* P, int64_t N, int64_t K, int R, const int64_t* M_r,
+                         const void* const* A_r, const void* W, void* Y, const uint32_t* ready,
+                         uint32_t epoch, void* ws, size_t ws_bytes, gsr_stream_t stream) {
   gsr_status s = check_plan(P);
   if (s) return s;
   if (N < 8 || N % 8)
@@ -641,7 +659,42 @@ gsr_status gemm_ag(const gemm_shard_plan* P, int64_t N, int64_t K, int R, const 
   CUresult cr = encode_kmajor(&p.tmap_b[0], W, N, K, c.block_n / c.cta_group);
   if (cr != CUDA_SUCCESS) return fail(GSR_ERR_CUDA, "encoding the W descriptor failed (%d)", (int)cr);
   p.y = static_cast<uint16_t*>(Y);
+  p.ready = ready;
+  p.epoch = epoch;
   return launch(P, p, c, stream);
+}
+
+gsr_status gemm_ag(const gemm_shard_plan* P, int64_t N, int64_t K, int R, const int64_t* M_r,
+                   const void* const* A_r, const void* W, void* Y, void* ws, size_t ws_bytes,
+                   gsr_stream_t stream) {
+  return run_ag(P, N, K, R, M_r, A_r, W, Y, nullptr, 0, ws, ws_bytes, stream);
+}
+
+gsr_status gemm_ag_flagged(const gemm_shard_plan* P, int64_t N, int64_t K, int R,
+                           const int64_t* M_r, const void* const* A_r, const void* W, void* Y,
+                           const uint32_t* ready, uint32_t epoch, void* ws, size_t ws_bytes,
+                           gsr_stream_t stream) {
+  if (!ready || (reinterpret_cast<uintptr_t>(ready) & 3u))
+    return fail(GSR_ERR_INVALID_VALUE, "ready must be a non-NULL, 4-byte aligned device array");
+  return run_ag(P, N, K, R, M_r, A_r, W, Y, ready, epoch, ws, ws_bytes, stream);
+}
+
+gsr_status gemm_shard_signal(const gemm_shard_plan* P, uint32_t* flag, uint32_t value,
+                             gsr_stream_t stream) {
+  gsr_status s = check_plan(P);
+  if (s) return s;
+  if (!flag || (reinterpret_cast<uintptr_t>(flag) & 3u))
+    return fail(GSR_ERR_INVALID_VALUE, "flag must be a non-NULL, 4-byte aligned device word");
+  if (P->device < 0) return fail(GSR_ERR_UNSUPPORTED, "host plan: nothing to signal");
+  WriteValueFn fn = write_value_fn();
+  if (!fn) return fail(GSR_ERR_UNSUPPORTED, "cuStreamWriteValue32 is unavailable");
+  DeviceScope scope(P->device);
+  if (scope.err != cudaSuccess) return cuda_fail(scope.err, "selecting the plan's device");
+  // CU_STREAM_WRITE_VALUE_DEFAULT (0): the write is preceded by a system-wide
+  // memory fence, so data written by earlier work on the stream is visible first.
+  CUresult r = fn(reinterpret_cast<CUstream>(stream), reinterpret_cast<CUdeviceptr>(flag), value, 0);
+  if (r != CUDA_SUCCESS) return fail(GSR_ERR_CUDA, "cuStreamWriteValue32 failed (%d)", (int)r);
+  return ok();
 }
 
 gsr_status gemm_shard_check_status(const gemm_shard_plan* P, void* ws, gsr_stream_t stream) {

@@ -328,20 +328,54 @@ struct Ctl {
 // Role ids stored in the timeout code.
 enum : uint32_t { kRoleProducer = 1, kRoleMma = 2, kRoleEpilogue = 3 };
 
-__device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const Ctl& c,
-                                          uint32_t site) {
-  if (mbar_try_wait(bar, parity)) return true;
+// Limits grow along the dependency chain (producer x1, MMA x2, epilogue x3),
+// so when something upstream never arrives the wait closest to the cause runs
+// out first and its site is the one recorded.
+__device__ __noinline__ bool wait_bounded_slow(uint32_t bar, uint32_t parity, const Ctl& c,
+                                               uint32_t site) {
   const uint64_t t0 = global_timer_ns();
+  const uint64_t limit = c.timeout_ns * (site >> 8);
   for (uint32_t spin = 1;; ++spin) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((spin & 31u) == 0) {
       if (*c.abort) return false;
-      if (global_timer_ns() - t0 > c.timeout_ns) {
+      if (global_timer_ns() - t0 > limit) {
         *c.abort = 1;
         atomicCAS(c.status, 0u, kStatusTimeout | site);
         return false;
       }
     }
+  }
+}
+
+// The common case (the phase already complete) costs one try_wait and no call.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const Ctl& c,
+                                             uint32_t site) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_bounded_slow(bar, parity, c, site);
+}
+
+// Wait until the arrival word `flag` reaches `epoch` (wrap-around compare),
+// bounded like every other wait. The word is written by another agent (a copy
+// stream's memory operation), so it is read with acquire semantics at GPU scope,
+// and the async proxy is fenced before TMA reads the data it guards.
+__device__ __noinline__ bool wait_flag(const uint32_t* flag, uint32_t epoch, const Ctl& c,
+                                       uint32_t site) {
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t spin = 0;; ++spin) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+    if (static_cast<int32_t>(v - epoch) >= 0) {
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      return true;
+    }
+    if (*c.abort) return false;
+    if (global_timer_ns() - t0 > c.timeout_ns) {
+      *c.abort = 1;
+      atomicCAS(c.status, 0u, kStatusTimeout | site);
+      return false;
+    }
+    __nanosleep(spin < 64 ? 32 : 256);
   }
 }
 
@@ -508,10 +542,18 @@ __device__ void run_producer(const Params& p, uint32_t tiles_base, uint32_t bars
   const uint64_t pol_a = make_l2_policy(p.policy_a);
   const uint64_t pol_b = make_l2_policy(p.policy_b);
   uint32_t issued = 0;
+  uint32_t arrived = 0;   // AG with arrival flags: shards seen ready (bit r)
   bool ok = true;
   Sched sch = sched_begin<CG>(p);
   Unit t;
   while (ok && sched_next<BN, CG>(p, sch, t)) {
+    if (p.ready != nullptr && !(arrived & (1u << t.shard))) {
+      if (!wait_flag(p.ready + t.shard, p.epoch, ctl, (kRoleProducer << 8) | 3)) {
+        ok = false;
+        break;
+      }
+      arrived |= 1u << t.shard;
+    }
     // This CTA's rows of A, and its columns of B: with a CTA pair the MMA's N
     // columns are split in halves between the two CTAs.
     const int a_row = t.m0 + BM * static_cast<int>(rank);

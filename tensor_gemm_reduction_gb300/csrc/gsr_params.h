@@ -42,6 +42,9 @@ struct Params {  // 128-byte aligned through its CUtensorMap members
 
   uint16_t* y;                  // AR, AG: output rows x N (bf16 bits)
   uint16_t* y_r[kMaxShards];    // RS: shard outputs, rps x N each
+  const uint32_t* ready;        // AG with arrival flags: ready[r] reaches epoch when
+                                // shard r's rows are in memory (NULL: no waiting)
+  uint32_t epoch;
   uint32_t* status;             // workspace status word
   uint32_t* counters;           // workspace per-tile arrival counters
   float* partials;              // workspace split-K partial tiles

@@ -220,6 +220,7 @@ def test_small_m_splits_pair_tiles(host):
 def test_uniform_schedule_splits_small_m(lib):
     h = Host(lib)
     B.gemm_shard_plan_set_option(h.plan, B.GSR_OPT_SCHEDULE, 1)
+    B.gemm_shard_plan_set_option(h.plan, B.GSR_OPT_CTA_GROUP, 1)
     d = h.describe(B.MODE_AR, 128, 7168, 0, [896] * 8)
     assert (d["schedule"], d["split"], d["ctas"], d["cta_group"]) == (1, 5, 140, 1)
     assert d["workspace_bytes"] <= B.gemm_shard_workspace_size(h.plan)
@@ -290,3 +291,17 @@ def test_host_plan_has_no_device_status(host):
         st = host.lib.gemm_shard_check_status(host.plan.handle, ctypes.c_void_p(0x20000000), None)
         B._check(st)
     assert e.value.status == B.GSR_ERR_UNSUPPORTED
+
+
+def test_flagged_ag_and_signal_validation(host):
+    lib = host.lib
+    M_r = (ctypes.c_int64 * 2)(16, 16)
+    A = (ctypes.c_void_p * 2)(0x100000, 0x200000)
+    args = lambda ready: (host.plan.handle, 256, 128, 2, M_r, A, ctypes.c_void_p(0x700000),
+                          ctypes.c_void_p(0x10000), ctypes.c_void_p(ready), ctypes.c_uint32(1),
+                          ctypes.c_void_p(0x20000000), host.ws_bytes, None)
+    assert lib.gemm_ag_flagged(*args(0)) == B.GSR_ERR_INVALID_VALUE
+    assert lib.gemm_ag_flagged(*args(0x30000002)) == B.GSR_ERR_INVALID_VALUE
+    assert lib.gemm_ag_flagged(*args(0x30000000)) == B.GSR_ERR_UNSUPPORTED   # host plan: valid
+    assert lib.gemm_shard_signal(host.plan.handle, ctypes.c_void_p(0), 1, None) == B.GSR_ERR_INVALID_VALUE
+    assert lib.gemm_shard_signal(host.plan.handle, ctypes.c_void_p(0x30000000), 1, None) == B.GSR_ERR_UNSUPPORTED
