@@ -440,36 +440,94 @@ def main():
 
 
 def e2e(run, w, steps, world):
-    """Same metric through the public call with host buffers: each step copies the
-    inputs from pinned host memory, runs the call and copies the output back."""
+    """Same metric through the public calls with host buffers: every step copies
+    all inputs from pinned host memory and reads the whole output back.
+
+    AG uses gemm_ag_flagged: W is copied first and the kernel is launched behind
+    it; the activation shards follow on a copy stream, each signalled with
+    gemm_shard_signal, so their copies overlap the GEMM on the shards already
+    in. The next step's copies wait for the previous kernel. Other modes copy,
+    call and read back in order on one stream."""
     import torch
+    from tensor_gemm_reduction_gb300 import binding as B
     dev_in = run.inputs()
     dev_out = run.outputs()
     host_in = [t.cpu().pin_memory() for t in dev_in]
     host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in dev_out]
     h2d = sum(t.numel() * t.element_size() for t in host_in)
     d2h = sum(t.numel() * t.element_size() for t in host_out)
+    dev = dev_in[0].device
 
-    def step():
-        for d, h in zip(dev_in, host_in):
-            d.copy_(h, non_blocking=True)
-        run()
-        for h, d in zip(host_out, dev_out):
-            h.copy_(d, non_blocking=True)
+    if w.mode == "ag":
+        R = w.R
+        A_dev, W_dev = dev_in[:R], dev_in[R]
+        A_host, W_host = host_in[:R], host_in[R]
+        ready = torch.zeros(R, dtype=torch.int32, device=dev)
+        gemm_s, copy_s = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+        state = {"epoch": 0, "done": None}
 
-    for _ in range(3):
-        step()
-    torch.cuda.synchronize()
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record()
-    for _ in range(steps):
-        step()
-    t1.record()
-    torch.cuda.synchronize()
+        def step():
+            state["epoch"] += 1
+            ep = state["epoch"]
+            with torch.cuda.stream(copy_s):
+                if state["done"] is not None:
+                    copy_s.wait_event(state["done"])      # previous kernel done with A, W
+                W_dev.copy_(W_host, non_blocking=True)
+                w_in = torch.cuda.Event()
+                w_in.record(copy_s)
+            with torch.cuda.stream(gemm_s):
+                gemm_s.wait_event(w_in)
+                B.gemm_ag_flagged(run.plan, A_dev, W_dev, run.Y, ready, ep, run.ws)
+                done = torch.cuda.Event()
+                done.record(gemm_s)
+                state["done"] = done
+            with torch.cuda.stream(copy_s):
+                for r in range(R):
+                    A_dev[r].copy_(A_host[r], non_blocking=True)
+                    B.gemm_shard_signal(run.plan, ready.data_ptr() + 4 * r, ep, stream=copy_s)
+            with torch.cuda.stream(gemm_s):
+                host_out[0].copy_(run.Y, non_blocking=True)
+
+        def sync_all():
+            gemm_s.synchronize()
+            copy_s.synchronize()
+
+        for _ in range(3):
+            step()
+        sync_all()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(copy_s)
+        gemm_s.wait_event(t0)
+        for _ in range(steps):
+            step()
+        t1.record(gemm_s)
+        torch.cuda.synchronize()
+        B.gemm_shard_check_status(run.plan, run.ws, stream=gemm_s)
+        how = "shard copies overlap the kernel (gemm_ag_flagged + gemm_shard_signal)"
+    else:
+        def step():
+            for d, h in zip(dev_in, host_in):
+                d.copy_(h, non_blocking=True)
+            run()
+            for h, d in zip(host_out, dev_out):
+                h.copy_(d, non_blocking=True)
+
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for _ in range(steps):
+            step()
+        t1.record()
+        torch.cuda.synchronize()
+        how = "copy in, call, copy out on one stream"
     s = t0.elapsed_time(t1) * 1e-3
     return {"value": w.flops * steps / s / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": s / steps * 1e3}
+            "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": s / steps * 1e3,
+            "schedule": how}
 
 
 if __name__ == "__main__":
