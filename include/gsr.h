@@ -9,6 +9,7 @@
  *   gemm_rs  Y_s = rows [s*rps, min(M,(s+1)*rps)) of sum_r X_r . W_r^T
  *                  with rps = ceil(M / R)           (reduce-scatter by rows)
  *   gemm_ag  Y   = concat_r(A_r) . W^T              (all-gather of M-shards)
+ *   gemm_ar_replicated  the AR sum written into each of R output buffers
  *
  * Sources of the definitions: vLLM PR #53053 summary ("Extend GEMM-RS to
  * GEMM-AR"), implementation breakdown step 1 (one kernel serves RS and AR;
@@ -172,6 +173,23 @@ gsr_status gemm_ar(const gemm_shard_plan *plan, int64_t M, int64_t N, int R,
 gsr_status gemm_rs(const gemm_shard_plan *plan, int64_t M, int64_t N, int R,
                    const int64_t *K_r, const void *const *X_r, const void *const *W_r,
                    void *const *Y_r, void *ws, size_t ws_bytes, gsr_stream_t stream);
+
+/*
+ * AR with replicated outputs: the AR sum written whole into each of R output
+ * buffers, Y_r[r] = sum_q X_q . W_q^T for every r. This is the one-GPU
+ * statement of an all-reduce whose result every rank holds: the GEMM-AR page
+ * reduces each row once and multicasts it to all ranks (PR #53053 summary,
+ * implementation breakdown step 1, and key source snippets: AR mode takes
+ * local_M = partial_uc.shape[0] // num_ranks and stores through
+ * multimem_st_16B). Here the reduced tile is rounded once and stored R times
+ * from the same epilogue. Y_r[r] must each hold M x N bf16. Every written
+ * element is bit-identical to gemm_ar's on the same inputs. Arguments otherwise
+ * as gemm_ar.
+ */
+gsr_status gemm_ar_replicated(const gemm_shard_plan *plan, int64_t M, int64_t N, int R,
+                              const int64_t *K_r, const void *const *X_r,
+                              const void *const *W_r, void *const *Y_r, void *ws,
+                              size_t ws_bytes, gsr_stream_t stream);
 
 /*
  * AG: Y = concat_r(A_r) . W^T.

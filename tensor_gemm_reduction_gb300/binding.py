@@ -49,7 +49,7 @@ EXPORTED = (
     "gemm_shard_plan_create", "gemm_shard_plan_create_host", "gemm_shard_plan_destroy", "gemm_shard_plan_set_option",
     "gemm_shard_workspace_size", "gemm_shard_workspace_init", "gemm_ar", "gemm_rs",
     "gemm_ag", "gemm_shard_check_status", "gsr_last_error_string", "gemm_shard_describe",
-    "gemm_ar_noalloc", "gemm_ag_flagged", "gemm_shard_signal",
+    "gemm_ar_noalloc", "gemm_ag_flagged", "gemm_shard_signal", "gemm_ar_replicated",
 )
 
 
@@ -96,6 +96,8 @@ def load_library() -> ctypes.CDLL:
     lib.gemm_shard_workspace_init.argtypes = [vp, vp, sz, vp]
     lib.gemm_ar.argtypes = [vp, i64, i64, i32, i64_arr, ptr_arr, ptr_arr, vp, vp, sz, vp]
     lib.gemm_rs.argtypes = [vp, i64, i64, i32, i64_arr, ptr_arr, ptr_arr, ptr_arr, vp, sz, vp]
+    lib.gemm_ar_replicated.argtypes = [vp, i64, i64, i32, i64_arr, ptr_arr, ptr_arr, ptr_arr, vp,
+                                       sz, vp]
     lib.gemm_ag.argtypes = [vp, i64, i64, i32, i64_arr, ptr_arr, vp, vp, vp, sz, vp]
     lib.gemm_ar_noalloc.argtypes = [vp, i64, i64, i32, i64_arr, ptr_arr, ptr_arr, vp, vp]
     lib.gemm_ag_flagged.argtypes = [vp, i64, i64, i32, i64_arr, ptr_arr, vp, vp, vp,
@@ -168,7 +170,7 @@ def gemm_shard_workspace_size(plan: Plan) -> int:
 
 def _stream(stream) -> ctypes.c_void_p:
     if stream is None:
-        stream = torch.cuda.current_stream()
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     if isinstance(stream, torch.cuda.Stream):
         stream = stream.cuda_stream
     return ctypes.c_void_p(int(stream))
@@ -191,9 +193,29 @@ def gemm_shard_workspace_init(plan: Plan, ws: torch.Tensor, stream=None) -> None
     _check(load_library().gemm_shard_workspace_init(plan.handle, p, n, _stream(stream)))
 
 
+_BF16 = torch.bfloat16
+
+
 def _bf16_2d(t: torch.Tensor, name: str) -> None:
-    if t.dtype != torch.bfloat16 or not t.is_cuda or t.dim() != 2 or not t.is_contiguous():
+    if t.dtype is not _BF16 or not t.is_cuda or t.dim() != 2 or not t.is_contiguous():
         raise ValueError(f"{name} must be a contiguous 2-D bf16 CUDA tensor")
+
+
+class PreparedCall:
+    """A validated, marshalled call of one entry point on fixed buffers.
+
+    Serving loops reuse the same shard, output and workspace buffers every
+    step; preparing the call once moves the per-call Python cost to a single
+    ctypes call. The buffers must stay alive and keep their shapes; their
+    contents may change. The stream is read at each call unless fixed."""
+
+    def __init__(self, fn, args, keep, stream=None):
+        self._fn, self._args, self._keep = fn, args, keep
+        self._stream = None if stream is None else _stream(stream)
+
+    def __call__(self, stream=None):
+        st = self._stream if stream is None and self._stream is not None else _stream(stream)
+        _check(self._fn(*self._args, st))
 
 
 def _ptrs(ts: Sequence[Optional[torch.Tensor]]):
@@ -206,28 +228,59 @@ def _i64s(vals: Sequence[int]):
     return ctypes.cast(arr, ctypes.POINTER(ctypes.c_int64)), arr
 
 
-def gemm_ar(plan: Plan, X_r: Sequence[torch.Tensor], W_r: Sequence[torch.Tensor],
-            Y: torch.Tensor, ws: torch.Tensor, stream=None) -> torch.Tensor:
-    """Y = sum_r X_r @ W_r.T (X_r: M x K_r, W_r: N x K_r, Y: M x N, all bf16)."""
+def _ar_args(plan, X_r, W_r, Y, ws):
     R = len(X_r)
     if R != len(W_r) or R == 0:
         raise ValueError("X_r and W_r need the same, non-zero number of shards")
-    for r in range(R):
-        _bf16_2d(X_r[r], f"X_r[{r}]")
-        _bf16_2d(W_r[r], f"W_r[{r}]")
     _bf16_2d(Y, "Y")
     M, N = Y.shape
-    K_r = [x.shape[1] for x in X_r]
+    K_r = []
     for r in range(R):
-        if X_r[r].shape[0] != M or W_r[r].shape != (N, K_r[r]):
+        x, w = X_r[r], W_r[r]
+        _bf16_2d(x, f"X_r[{r}]")
+        _bf16_2d(w, f"W_r[{r}]")
+        k = x.shape[1]
+        if x.shape[0] != M or w.shape[0] != N or w.shape[1] != k:
             raise ValueError(f"shard {r}: X_r must be {M} x K_r and W_r {N} x K_r")
+        K_r.append(k)
     k, ka = _i64s(K_r)
     xp, xa = _ptrs(X_r)
     wp, wa = _ptrs(W_r)
     wsp, wsn = _ws(ws)
-    _check(load_library().gemm_ar(plan.handle, M, N, R, k, xp, wp, ctypes.c_void_p(Y.data_ptr()),
-                                  wsp, wsn, _stream(stream)))
+    args = (plan.handle, M, N, R, k, xp, wp, ctypes.c_void_p(Y.data_ptr()), wsp, wsn)
+    return args, (ka, xa, wa, X_r, W_r, Y, ws)
+
+
+def gemm_ar(plan: Plan, X_r: Sequence[torch.Tensor], W_r: Sequence[torch.Tensor],
+            Y: torch.Tensor, ws: torch.Tensor, stream=None) -> torch.Tensor:
+    """Y = sum_r X_r @ W_r.T (X_r: M x K_r, W_r: N x K_r, Y: M x N, all bf16)."""
+    args, keep = _ar_args(plan, X_r, W_r, Y, ws)
+    _check(load_library().gemm_ar(*args, _stream(stream)))
     return Y
+
+
+def prepare_ar(plan: Plan, X_r, W_r, Y, ws, stream=None) -> PreparedCall:
+    """gemm_ar on fixed buffers, validated and marshalled once."""
+    args, keep = _ar_args(plan, X_r, W_r, Y, ws)
+    return PreparedCall(load_library().gemm_ar, args, keep, stream)
+
+
+def gemm_ar_replicated(plan: Plan, X_r: Sequence[torch.Tensor], W_r: Sequence[torch.Tensor],
+                       Y_r: Sequence[torch.Tensor], ws: torch.Tensor, stream=None):
+    """Y_r[r] = sum_q X_q @ W_q.T for every r (R outputs of M x N, all bf16)."""
+    R = len(X_r)
+    if len(Y_r) != R:
+        raise ValueError("need one output per shard")
+    for r in range(R):
+        _bf16_2d(Y_r[r], f"Y_r[{r}]")
+        if Y_r[r].shape != Y_r[0].shape:
+            raise ValueError("all outputs must have the same shape")
+    args, keep = _ar_args(plan, X_r, W_r, Y_r[0], ws)
+    yp, ya = _ptrs(Y_r)
+    # same marshalling as gemm_ar, with the output pointer array in place of Y
+    args = args[:7] + (yp,) + args[8:]
+    _check(load_library().gemm_ar_replicated(*args, _stream(stream)))
+    return Y_r
 
 
 def gemm_ar_noalloc(plan: Plan, X_r: Sequence[torch.Tensor], W_r: Sequence[torch.Tensor],
@@ -255,61 +308,70 @@ def gemm_ar_noalloc(plan: Plan, X_r: Sequence[torch.Tensor], W_r: Sequence[torch
     return Y
 
 
-def gemm_rs(plan: Plan, X_r: Sequence[torch.Tensor], W_r: Sequence[torch.Tensor],
-            Y_r: Sequence[torch.Tensor], ws: torch.Tensor, M: Optional[int] = None,
-            stream=None) -> Sequence[torch.Tensor]:
-    """Y_r[s] = rows [s*rps, min(M,(s+1)*rps)) of sum_r X_r @ W_r.T, rps = ceil(M/R)."""
+def _rs_args(plan, X_r, W_r, Y_r, ws, M=None):
     R = len(X_r)
     if R != len(W_r) or R != len(Y_r) or R == 0:
         raise ValueError("X_r, W_r and Y_r need the same, non-zero number of shards")
+    M = X_r[0].shape[0] if M is None else int(M)
+    N = W_r[0].shape[0]
+    rps = -(-M // R)
+    K_r = []
     for r in range(R):
         _bf16_2d(X_r[r], f"X_r[{r}]")
         _bf16_2d(W_r[r], f"W_r[{r}]")
         _bf16_2d(Y_r[r], f"Y_r[{r}]")
-    M = X_r[0].shape[0] if M is None else int(M)
-    N = W_r[0].shape[0]
-    rps = -(-M // R)
-    K_r = [x.shape[1] for x in X_r]
-    for r in range(R):
-        if X_r[r].shape[0] != M or W_r[r].shape != (N, K_r[r]):
+        k = X_r[r].shape[1]
+        if X_r[r].shape[0] != M or W_r[r].shape != (N, k):
             raise ValueError(f"shard {r}: X_r must be {M} x K_r and W_r {N} x K_r")
         if Y_r[r].shape[0] < rps or Y_r[r].shape[1] != N:
             raise ValueError(f"Y_r[{r}] must hold at least {rps} rows of {N}")
+        K_r.append(k)
     k, ka = _i64s(K_r)
     xp, xa = _ptrs(X_r)
     wp, wa = _ptrs(W_r)
     yp, ya = _ptrs(Y_r)
     wsp, wsn = _ws(ws)
-    _check(load_library().gemm_rs(plan.handle, M, N, R, k, xp, wp, yp, wsp, wsn, _stream(stream)))
+    args = (plan.handle, M, N, R, k, xp, wp, yp, wsp, wsn)
+    return args, (ka, xa, wa, ya, X_r, W_r, Y_r, ws)
+
+
+def gemm_rs(plan: Plan, X_r: Sequence[torch.Tensor], W_r: Sequence[torch.Tensor],
+            Y_r: Sequence[torch.Tensor], ws: torch.Tensor, M: Optional[int] = None,
+            stream=None) -> Sequence[torch.Tensor]:
+    """Y_r[s] = rows [s*rps, min(M,(s+1)*rps)) of sum_r X_r @ W_r.T, rps = ceil(M/R)."""
+    args, keep = _rs_args(plan, X_r, W_r, Y_r, ws, M)
+    _check(load_library().gemm_rs(*args, _stream(stream)))
     return Y_r
+
+
+def prepare_rs(plan: Plan, X_r, W_r, Y_r, ws, M=None, stream=None) -> PreparedCall:
+    """gemm_rs on fixed buffers, validated and marshalled once."""
+    args, keep = _rs_args(plan, X_r, W_r, Y_r, ws, M)
+    return PreparedCall(load_library().gemm_rs, args, keep, stream)
+
+
+def _ag_call_args(plan, A_r, W, Y, ws):
+    N, K, M_r = _ag_args(A_r, W, Y)
+    m, ma = _i64s(M_r)
+    ap, aa = _ptrs([a if a.numel() else None for a in A_r])
+    wsp, wsn = _ws(ws)
+    args = (plan.handle, N, K, len(A_r), m, ap, ctypes.c_void_p(W.data_ptr()),
+            ctypes.c_void_p(Y.data_ptr()), wsp, wsn)
+    return args, (ma, aa, A_r, W, Y, ws)
 
 
 def gemm_ag(plan: Plan, A_r: Sequence[torch.Tensor], W: torch.Tensor, Y: torch.Tensor,
             ws: torch.Tensor, stream=None) -> torch.Tensor:
     """Y = cat(A_r) @ W.T (A_r: M_r x K, W: N x K, Y: sum(M_r) x N, all bf16)."""
-    R = len(A_r)
-    if R == 0:
-        raise ValueError("need at least one shard")
-    _bf16_2d(W, "W")
-    _bf16_2d(Y, "Y")
-    N, K = W.shape
-    M_r = []
-    for r, a in enumerate(A_r):
-        if a.numel() == 0:
-            M_r.append(0)
-            continue
-        _bf16_2d(a, f"A_r[{r}]")
-        if a.shape[1] != K:
-            raise ValueError(f"A_r[{r}] must have K={K} columns")
-        M_r.append(a.shape[0])
-    if Y.shape != (sum(M_r), N):
-        raise ValueError(f"Y must be {sum(M_r)} x {N}")
-    m, ma = _i64s(M_r)
-    ap, aa = _ptrs([a if a.numel() else None for a in A_r])
-    wsp, wsn = _ws(ws)
-    _check(load_library().gemm_ag(plan.handle, N, K, R, m, ap, ctypes.c_void_p(W.data_ptr()),
-                                  ctypes.c_void_p(Y.data_ptr()), wsp, wsn, _stream(stream)))
+    args, keep = _ag_call_args(plan, A_r, W, Y, ws)
+    _check(load_library().gemm_ag(*args, _stream(stream)))
     return Y
+
+
+def prepare_ag(plan: Plan, A_r, W, Y, ws, stream=None) -> PreparedCall:
+    """gemm_ag on fixed buffers, validated and marshalled once."""
+    args, keep = _ag_call_args(plan, A_r, W, Y, ws)
+    return PreparedCall(load_library().gemm_ag, args, keep, stream)
 
 
 def _ag_args(A_r, W, Y):

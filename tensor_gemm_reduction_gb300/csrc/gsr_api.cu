@@ -389,7 +389,8 @@ gsr_status run_ksharded(const gemm_shard_plan* P, int mode, int64_t M, int64_t N
       if ((M > 0 && !Y_r[r]) || !aligned16(Y_r[r]))
         return fail(GSR_ERR_INVALID_VALUE, "Y_r[%d] must be non-NULL and 16-byte aligned", r);
   }
-  const Config c = choose_config(P, mode, M, N, 0, R, K_r);
+  // Replicated AR is AR with another epilogue: the same configuration.
+  const Config c = choose_config(P, mode == gsr::kModeARRep ? gsr::kModeAR : mode, M, N, 0, R, K_r);
   s = check_ws(c, ws, ws_bytes);
   if (s) return s;
   if (M == 0) return ok();
@@ -415,6 +416,7 @@ gsr_status run_ksharded(const gemm_shard_plan* P, int mode, int64_t M, int64_t N
     p.rps = static_cast<int>(cdiv(M, R));
     for (int r = 0; r < R; ++r) p.y_r[r] = static_cast<uint16_t*>(Y_r[r]);
   }
+  if (mode == gsr::kModeARRep) p.mode = gsr::kModeARRep;
   return launch(P, p, c, stream);
 }
 
@@ -591,6 +593,13 @@ gsr_status gemm_ar(const gemm_shard_plan* plan, int64_t M, int64_t N, int R, con
                    const void* const* X_r, const void* const* W_r, void* Y, void* ws,
                    size_t ws_bytes, gsr_stream_t stream) {
   return run_ksharded(plan, gsr::kModeAR, M, N, R, K_r, X_r, W_r, Y, nullptr, ws, ws_bytes, stream);
+}
+
+gsr_status gemm_ar_replicated(const gemm_shard_plan* plan, int64_t M, int64_t N, int R,
+                              const int64_t* K_r, const void* const* X_r, const void* const* W_r,
+                              void* const* Y_r, void* ws, size_t ws_bytes, gsr_stream_t stream) {
+  return run_ksharded(plan, gsr::kModeARRep, M, N, R, K_r, X_r, W_r, nullptr, Y_r, ws, ws_bytes,
+                      stream);
 }
 
 gsr_status gemm_rs(const gemm_shard_plan* plan, int64_t M, int64_t N, int R, const int64_t* K_r,

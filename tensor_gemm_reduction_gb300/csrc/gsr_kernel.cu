@@ -710,9 +710,11 @@ __device__ void run_epilogue(const Params& p, uint32_t bars, uint32_t tmem_base,
     const int chunks = (n_valid + 31) >> 5;
     const int m0 = t.m0 + BM * static_cast<int>(rank);   // this CTA's first row
 
-    // Where this thread's output row goes.
+    // Where this thread's output row goes (with replicated outputs: the same
+    // offset in every one of the R buffers).
     bool row_ok;
     uint16_t* row_ptr;
+    size_t rep_off = 0;
     if (p.mode == kModeAG) {
       const int lr = m0 + row_in_tile;
       row_ok = lr < p.shard_rows[t.shard];
@@ -723,10 +725,20 @@ __device__ void run_epilogue(const Params& p, uint32_t bars, uint32_t tmem_base,
       if (p.mode == kModeRS) {
         const int s = row_ok ? gr / p.rps : 0;
         row_ptr = p.y_r[s] + static_cast<size_t>(gr - s * p.rps) * p.N + t.n0;
+      } else if (p.mode == kModeARRep) {
+        rep_off = static_cast<size_t>(gr) * p.N + t.n0;
+        row_ptr = p.y_r[0] + rep_off;
       } else {
         row_ptr = p.y + static_cast<size_t>(gr) * p.N + t.n0;
       }
     }
+    auto emit = [&](int col, const uint32_t (&v)[32]) {
+      if (p.mode == kModeARRep) {
+        for (int i = 0; i < p.R; ++i) store_row_chunk(p.y_r[i] + rep_off, col, n_valid, v, row_ok);
+      } else {
+        store_row_chunk(row_ptr, col, n_valid, v, row_ok);
+      }
+    };
 
     // Hands the accumulator back to the MMA issuer (the leader's barrier with a
     // pair): one arrival per warp once its TMEM reads are complete.
@@ -746,7 +758,7 @@ __device__ void run_epilogue(const Params& p, uint32_t bars, uint32_t tmem_base,
         uint32_t v[32];
         tmem_ld_32cols(taddr + 32 * c, v);
         tmem_ld_wait(v);
-        store_row_chunk(row_ptr, 32 * c, n_valid, v, row_ok);
+        emit(32 * c, v);
       }
       release_accumulator();
       continue;
@@ -825,7 +837,7 @@ __device__ void run_epilogue(const Params& p, uint32_t bars, uint32_t tmem_base,
         uint32_t v[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(a[j]);
-        store_row_chunk(row_ptr, 32 * c, n_valid, v, row_ok);
+        emit(32 * c, v);
       }
       if (et == 0) atomicExch(&p.counters[half], 0u);  // ready for the next call
     }

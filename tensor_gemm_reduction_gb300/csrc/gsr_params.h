@@ -13,7 +13,8 @@ constexpr int BK = 64;           // k-block: 64 bf16 = one 128-byte swizzle row
 constexpr int kThreads = 192;    // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
 constexpr int kEpilogueThreads = 128;
 
-enum Mode : int { kModeAR = 0, kModeRS = 1, kModeAG = 2 };
+// kModeARRep: the AR sum written whole into each of R output buffers.
+enum Mode : int { kModeAR = 0, kModeRS = 1, kModeAG = 2, kModeARRep = 3 };
 
 // Work schedules. Uniform: unit u = tile * splits + piece, dealt round-robin.
 // Stream-K: tiles [0, dp_tiles) are dealt whole, round-robin; the k-blocks of
@@ -41,7 +42,8 @@ struct Params {  // 128-byte aligned through its CUtensorMap members
   CUtensorMap tmap_b[kMaxShards];
 
   uint16_t* y;                  // AR, AG: output rows x N (bf16 bits)
-  uint16_t* y_r[kMaxShards];    // RS: shard outputs, rps x N each
+  uint16_t* y_r[kMaxShards];    // RS: shard outputs, rps x N each; AR replicated:
+                                // R outputs, M x N each
   const uint32_t* ready;        // AG with arrival flags: ready[r] reaches epoch when
                                 // shard r's rows are in memory (NULL: no waiting)
   uint32_t epoch;

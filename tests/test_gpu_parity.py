@@ -263,3 +263,53 @@ def test_heuristic_split_small_m_matches_oracle():
     inp = gi.gaussian_ar(128, 7168, [896] * 8, seed=99)
     Y, _, _ = run_ar(inp)
     assert_close(to_f64(Y.out), oracle.ar(inp.X_r, inp.W_r), "ar m128 split")
+
+
+def test_prepared_calls_match_plain_calls():
+    """prepare_ar/rs/ag validate and marshal once; each call gives the same bits."""
+    p, ws = plan()
+    dev = device()
+    inp = gi.gaussian_ar(257, 520, [128, 72])
+    X = [x.to(dev) for x in inp.X_r]
+    W = [w.to(dev) for w in inp.W_r]
+    Y0 = torch.empty(257, 520, dtype=torch.bfloat16, device=dev)
+    Y1 = torch.empty_like(Y0)
+    B.gemm_ar(p, X, W, Y0, ws)
+    call = B.prepare_ar(p, X, W, Y1, ws)
+    call()
+    call()
+    rps = 129
+    R0 = [torch.empty(rps, 520, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    B.prepare_rs(p, X, W, R0, ws)()
+    ag = gi.gaussian_ag([100, 200], 264, 128)
+    A = [a.to(dev) for a in ag.A_r]
+    Wa = ag.W.to(dev)
+    Ya0 = torch.empty(300, 264, dtype=torch.bfloat16, device=dev)
+    Ya1 = torch.empty_like(Ya0)
+    B.gemm_ag(p, A, Wa, Ya0, ws)
+    B.prepare_ag(p, A, Wa, Ya1, ws)()
+    B.gemm_shard_check_status(p, ws)
+    assert np.array_equal(bits_of(Y1), bits_of(Y0))
+    assert np.array_equal(bits_of(torch.cat(R0)[:257]), bits_of(Y0))
+    assert np.array_equal(bits_of(Ya1), bits_of(Ya0))
+
+
+@pytest.mark.parametrize("variant", ["auto", "uniform", "sk8", "pair256", "pairsk8"])
+@pytest.mark.parametrize("M,N,K_r", [(129, 520, [64, 200, 72]), (300, 7168, [448] * 4), (5, 136, [8, 8])])
+def test_ar_replicated_outputs_equal_ar_bitwise(M, N, K_r, variant):
+    """Every one of the R outputs holds the whole AR result, bit for bit."""
+    p, ws = vplan(variant)
+    inp = gi.gaussian_ar(M, N, K_r)
+    dev = device()
+    X = [x.to(dev) for x in inp.X_r]
+    W = [w.to(dev) for w in inp.W_r]
+    Y = Guarded(M, N)
+    B.gemm_ar(p, X, W, Y.out, ws)
+    reps = [Guarded(M, N) for _ in K_r]
+    B.gemm_ar_replicated(p, X, W, [g.out for g in reps], ws)
+    B.gemm_shard_check_status(p, ws)
+    ref = bits_of(Y.out)
+    for g in reps:
+        assert np.array_equal(bits_of(g.out), ref)
+        assert g.guards_intact()
+    assert_close(to_f64(reps[-1].out), oracle.ar(inp.X_r, inp.W_r), "replicated")
