@@ -397,16 +397,17 @@ struct Unit {
   int npieces;    // pieces the tile is cut into (1 = whole tile)
   int slot0;      // partial slot of the tile's piece 0 (pieces are consecutive)
   int n0;         // first output column of the tile
-  int m0;         // first row of the tile in the A operand: AR/RS global, AG
-                  // local to the shard (a CTA pair's tile spans 2 x BM rows)
-  int shard;      // AG: M-shard of the tile
+  int m0;         // first row of THIS CTA's 128 rows in its A operand: AR/RS
+                  // global, AG local to the CTA's shard
+  int shard;      // AG: M-shard of this CTA's rows (-1: the idle half of an odd
+                  // last pair tile, which reads zeros and stores nothing)
   int kb_begin;   // k-blocks [kb_begin, kb_end) of this piece
   int kb_end;
 };
 
 // Position of the tile in the output (raster order) and its shard.
 template <int BN, int CG>
-__device__ __forceinline__ void place_tile(const Params& p, Unit& t) {
+__device__ __forceinline__ void place_tile(const Params& p, Unit& t, uint32_t rank) {
   // Raster: groups of group_m m-tiles; inside a group the m index runs fastest,
   // so CTAs working at the same time share W (B) panels and A rows in L2.
   const int span = p.group_m * p.n_tiles;
@@ -417,14 +418,23 @@ __device__ __forceinline__ void place_tile(const Params& p, Unit& t) {
   const int mt = first_m + in_g % gm;
   const int nt = in_g / gm;
   t.n0 = nt * BN;
+  // This CTA's 128 rows: half-tile h. AG half-tiles are numbered over all
+  // shards, each inside one shard, so the two halves of a pair tile may come
+  // from neighbouring shards and no rows are wasted on shard boundaries.
+  const int h = mt * CG + static_cast<int>(rank);
   if (p.mode == kModeAG) {
-    int r = 0;
-    while (r + 1 < p.R && p.shard_mt_begin[r + 1] <= mt) ++r;
-    t.shard = r;
-    t.m0 = (mt - p.shard_mt_begin[r]) * (BM * CG);
+    if (h >= p.ag_halves) {
+      t.shard = -1;
+      t.m0 = 0;
+    } else {
+      int r = 0;
+      while (r + 1 < p.R && p.shard_mt_begin[r + 1] <= h) ++r;
+      t.shard = r;
+      t.m0 = (h - p.shard_mt_begin[r]) * BM;
+    }
   } else {
     t.shard = 0;
-    t.m0 = mt * (BM * CG);
+    t.m0 = h * BM;
   }
 }
 
@@ -455,7 +465,7 @@ __device__ __forceinline__ int sk_worker_of(long long it, long long I, int G) {
 }
 
 template <int BN, int CG>
-__device__ __forceinline__ bool sched_next(const Params& p, Sched& s, Unit& t) {
+__device__ __forceinline__ bool sched_next(const Params& p, Sched& s, Unit& t, uint32_t rank) {
   if (p.sched == kSchedUniform) {
     if (s.next >= p.units) return false;
     const int u = s.next;
@@ -466,7 +476,7 @@ __device__ __forceinline__ bool sched_next(const Params& p, Sched& s, Unit& t) {
     t.slot0 = t.tile * p.splits;
     t.kb_begin = static_cast<int>((static_cast<long long>(t.piece) * p.kb_total) / p.splits);
     t.kb_end = static_cast<int>((static_cast<long long>(t.piece + 1) * p.kb_total) / p.splits);
-    place_tile<BN, CG>(p, t);
+    place_tile<BN, CG>(p, t, rank);
     return true;
   }
   if (s.next < p.dp_tiles) {           // a whole tile
@@ -477,7 +487,7 @@ __device__ __forceinline__ bool sched_next(const Params& p, Sched& s, Unit& t) {
     t.slot0 = 0;
     t.kb_begin = 0;
     t.kb_end = p.kb_total;
-    place_tile<BN, CG>(p, t);
+    place_tile<BN, CG>(p, t, rank);
     return true;
   }
   if (s.it >= s.it_end) return false;  // the next piece of this worker's range
@@ -496,7 +506,7 @@ __device__ __forceinline__ bool sched_next(const Params& p, Sched& s, Unit& t) {
   t.slot0 = sk_tile + first_w;
   t.kb_begin = k_lo;
   t.kb_end = k_hi;
-  place_tile<BN, CG>(p, t);
+  place_tile<BN, CG>(p, t, rank);
   return true;
 }
 
@@ -546,8 +556,8 @@ __device__ void run_producer(const Params& p, uint32_t tiles_base, uint32_t bars
   bool ok = true;
   Sched sch = sched_begin<CG>(p);
   Unit t;
-  while (ok && sched_next<BN, CG>(p, sch, t)) {
-    if (p.ready != nullptr && !(arrived & (1u << t.shard))) {
+  while (ok && sched_next<BN, CG>(p, sch, t, rank)) {
+    if (p.ready != nullptr && t.shard >= 0 && !(arrived & (1u << t.shard))) {
       if (!wait_flag(p.ready + t.shard, p.epoch, ctl, (kRoleProducer << 8) | 3)) {
         ok = false;
         break;
@@ -556,7 +566,10 @@ __device__ void run_producer(const Params& p, uint32_t tiles_base, uint32_t bars
     }
     // This CTA's rows of A, and its columns of B: with a CTA pair the MMA's N
     // columns are split in halves between the two CTAs.
-    const int a_row = t.m0 + BM * static_cast<int>(rank);
+    // The idle half of an odd last pair tile reads rows past the end of a
+    // non-empty shard: the TMA unit fills them with zeros.
+    const int a_shard = t.shard >= 0 ? t.shard : p.ag_pad_shard;
+    const int a_row = t.shard >= 0 ? t.m0 : p.shard_rows[p.ag_pad_shard];
     const int b_row = t.n0 + static_cast<int>(rank * (tile_mma_n<BN>(p, t) / CG));
     int r = 0;
     if (p.mode != kModeAG)
@@ -575,7 +588,7 @@ __device__ void run_producer(const Params& p, uint32_t tiles_base, uint32_t bars
       const CUtensorMap* mb;
       int kx;
       if (p.mode == kModeAG) {
-        ma = &p.tmap_a[t.shard];
+        ma = &p.tmap_a[a_shard];
         mb = &p.tmap_b[0];
         kx = kb * BK;
       } else {
@@ -614,11 +627,12 @@ __device__ void run_mma(const Params& p, uint32_t tiles_base, uint32_t bars, uin
   using L = Layout<BN, STAGES, CG>;
   const uint32_t full0 = bars, tfull0 = bars + 16 * STAGES, tempty0 = tfull0 + 16;
   const uint32_t empty0 = bars + 8 * STAGES, drain = tempty0 + 16;
+  const uint32_t rank = 0;   // only the leader issues MMAs; tile k ranges do not depend on rank
   uint32_t consumed = 0, local = 0;
   bool ok = true, issued_any = false;
   Sched sch = sched_begin<CG>(p);
   Unit t;
-  for (; ok && sched_next<BN, CG>(p, sch, t); ++local) {
+  for (; ok && sched_next<BN, CG>(p, sch, t, rank); ++local) {
     const uint32_t acc = local & 1u;
     const uint32_t acc_parity = ((local >> 1) & 1u) ^ 1u;
     if (!wait_bounded(tempty0 + 8 * acc, acc_parity, ctl, (kRoleMma << 8) | 1)) {
@@ -698,7 +712,7 @@ __device__ void run_epilogue(const Params& p, uint32_t bars, uint32_t tmem_base,
   uint32_t local = 0;
   Sched sch = sched_begin<CG>(p);
   Unit t;
-  for (; sched_next<BN, CG>(p, sch, t); ++local) {
+  for (; sched_next<BN, CG>(p, sch, t, rank); ++local) {
     const uint32_t acc = local & 1u;
     const uint32_t acc_parity = (local >> 1) & 1u;
     bool ok = wait_bounded(tfull0 + 8 * acc, acc_parity, ctl, (kRoleEpilogue << 8) | 1);
@@ -708,7 +722,7 @@ __device__ void run_epilogue(const Params& p, uint32_t bars, uint32_t tmem_base,
     const uint32_t taddr = tmem_base + lane_addr + acc * BN;
     const int n_valid = min(BN, p.N - t.n0);
     const int chunks = (n_valid + 31) >> 5;
-    const int m0 = t.m0 + BM * static_cast<int>(rank);   // this CTA's first row
+    const int m0 = t.m0;   // this CTA's first row
 
     // Where this thread's output row goes (with replicated outputs: the same
     // offset in every one of the R buffers).
@@ -716,9 +730,10 @@ __device__ void run_epilogue(const Params& p, uint32_t bars, uint32_t tmem_base,
     uint16_t* row_ptr;
     size_t rep_off = 0;
     if (p.mode == kModeAG) {
+      const int sh = t.shard >= 0 ? t.shard : 0;
       const int lr = m0 + row_in_tile;
-      row_ok = lr < p.shard_rows[t.shard];
-      row_ptr = p.y + (static_cast<size_t>(p.shard_row_begin[t.shard]) + lr) * p.N + t.n0;
+      row_ok = t.shard >= 0 && lr < p.shard_rows[sh];
+      row_ptr = p.y + (static_cast<size_t>(p.shard_row_begin[sh]) + lr) * p.N + t.n0;
     } else {
       const int gr = m0 + row_in_tile;
       row_ok = gr < p.M;

@@ -56,7 +56,7 @@ struct Params {  // 128-byte aligned through its CUtensorMap members
   int R;
   int M;                        // AR/RS: rows; AG: sum of M_r
   int N;
-  int m_tiles;                  // AR/RS: ceil(M/BM); AG: sum_r ceil(M_r/BM)
+  int m_tiles;                  // AR/RS: ceil(M/(BM*CG)); AG: ceil(halves/CG)
   int n_tiles;                  // ceil(N/BN)
   int tiles;                    // m_tiles * n_tiles
   int kb_total;                 // k-blocks per tile (AR/RS: sum_r ceil(K_r/BK))
@@ -70,7 +70,10 @@ struct Params {  // 128-byte aligned through its CUtensorMap members
   int policy_b;                 // L2 policy of B-operand loads (kPolicy*)
   int rps;                      // RS: rows per shard = ceil(M/R)
   int shard_kb_begin[kMaxShards + 1];  // AR/RS: first k-block of shard r
-  int shard_mt_begin[kMaxShards + 1];  // AG: first m-tile of shard r
+  int shard_mt_begin[kMaxShards + 1];  // AG: first 128-row half-tile of shard r
+  int ag_halves;                // AG: 128-row half-tiles over all shards
+  int ag_pad_shard;             // AG: a non-empty shard, read out of range (zeros)
+                                // by the idle half of an odd last pair tile
   int shard_row_begin[kMaxShards + 1]; // AG: first output row of shard r
   int shard_rows[kMaxShards];          // AG: M_r
 };

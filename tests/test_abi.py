@@ -241,9 +241,12 @@ def test_large_m_uses_cta_pairs_and_a_stream_k_tail(host):
     # 448-row shards: two pair tiles each, 87.5 % of rows used, as with 128-row tiles
     d = host.describe(B.MODE_AG, 0, 3648, 7168, [448] * 8)
     assert d["cta_group"] == 2 and d["tiles"] == 8 * 2 * 15
-    # 384-row shards would leave a quarter of every pair's rows empty: single CTAs
+    # 384-row shards: 24 half-tiles of 128 rows, paired across shard boundaries
     d = host.describe(B.MODE_AG, 0, 3648, 7168, [384] * 8)
-    assert d["cta_group"] == 1 and d["tiles"] == 8 * 3 * 15
+    assert d["cta_group"] == 2 and d["tiles"] == 12 * 15
+    # an odd number of half-tiles leaves the last pair's second half idle
+    d = host.describe(B.MODE_AG, 0, 6288, 7168, [384] * 7)
+    assert d["cta_group"] == 2 and d["tiles"] == 11 * 25
 
 
 def test_whole_waves_have_no_stream_k(lib):

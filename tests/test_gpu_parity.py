@@ -207,6 +207,9 @@ AG_SHAPES = [
     ([256] * 8, 6288, 1024),
     ([448, 384], 3648, 512),
     ([300, 5, 700], 520, 256),
+    ([384, 384, 384], 264, 128),        # pair tiles across shard boundaries
+    ([384, 0, 200, 0], 520, 136),       # odd half-tile count, empty shards
+    ([0, 0, 130], 136, 64),             # leading empty shards, idle last half
 ]
 
 
