@@ -87,7 +87,9 @@ typedef enum {
                                partial last wave), 1 = uniform (every tile cut
                                into the same number of pieces), 2 = stream-K
                                over the last one or two waves, 3 = stream-K
-                               over the partial last wave                        */
+                               over the partial last wave, each worker's
+                               stream-K range before its whole tiles, 4 = as 3
+                               with the whole tiles first                        */
 } gsr_option;
 
 /*

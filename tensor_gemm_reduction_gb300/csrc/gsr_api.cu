@@ -145,6 +145,7 @@ struct Config {
   int splits = 1;
   int64_t m_tiles = 0, n_tiles = 0, tiles = 0, kb_total = 0, units = 0;
   int64_t dp_tiles = 0, sk_iters = 0, slots = 0;   // slots: fp32 partial tiles per CTA half
+  int sk_last = 0;
   int ctas = 0;
   int group_m = 1;
   int policy_a = gsr::kPolicyNormal;
@@ -237,7 +238,7 @@ Config choose_config(const gemm_shard_plan* P, int mode, int64_t M, int64_t N, i
     if (rem != 0) {
       if (P->opt_schedule == 2)
         dp = full >= 2 ? (full - 1) * workers : 0;    // the last one or two waves
-      else
+      else                                            // 0, 3, 4
         dp = full * workers;                          // only the partial last wave
     }
     int64_t sk_iters = (c.tiles - dp) * c.kb_total;
@@ -247,6 +248,7 @@ Config choose_config(const gemm_shard_plan* P, int mode, int64_t M, int64_t N, i
     }
     c.dp_tiles = dp;
     c.sk_iters = sk_iters;
+    c.sk_last = P->opt_schedule == 4 ? 1 : 0;
     c.units = c.tiles;
     c.slots = sk_iters > 0 ? (c.tiles - dp) + workers - 1 : 0;
     c.ctas = static_cast<int>(c.cta_group *
@@ -318,6 +320,7 @@ void fill_common(gsr::Params& p, const gemm_shard_plan* P, const Config& c, int 
   p.sched = c.sched;
   p.dp_tiles = static_cast<int>(c.dp_tiles);
   p.sk_iters = c.sk_iters;
+  p.sk_last = c.sk_last;
   p.group_m = c.group_m;
   p.policy_a = c.policy_a;
   p.policy_b = c.policy_b;
@@ -543,7 +546,7 @@ gsr_status gemm_shard_plan_set_option(gemm_shard_plan* plan, gsr_option option, 
       plan->opt_cta_group = static_cast<int>(value);
       return ok();
     case GSR_OPT_SCHEDULE:
-      if (value < 0 || value > 3) return fail(GSR_ERR_INVALID_VALUE, "schedule must be 0..3");
+      if (value < 0 || value > 4) return fail(GSR_ERR_INVALID_VALUE, "schedule must be 0..4");
       plan->opt_schedule = static_cast<int>(value);
       return ok();
   }

@@ -189,6 +189,28 @@ __device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t* p) {
   return v;
 }
 
+// Wait for two batches of tcgen05.ld results at once.
+__device__ __forceinline__ void tmem_ld_wait2(uint32_t (&v)[32], uint32_t (&u)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]),
+                 "+r"(v[6]), "+r"(v[7]), "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]),
+                 "+r"(v[12]), "+r"(v[13]), "+r"(v[14]), "+r"(v[15]), "+r"(v[16]), "+r"(v[17]),
+                 "+r"(v[18]), "+r"(v[19]), "+r"(v[20]), "+r"(v[21]), "+r"(v[22]), "+r"(v[23]),
+                 "+r"(v[24]), "+r"(v[25]), "+r"(v[26]), "+r"(v[27]), "+r"(v[28]), "+r"(v[29]),
+                 "+r"(v[30]), "+r"(v[31])
+               :
+               : "memory");
+  asm volatile(""
+               : "+r"(u[0]), "+r"(u[1]), "+r"(u[2]), "+r"(u[3]), "+r"(u[4]), "+r"(u[5]),
+                 "+r"(u[6]), "+r"(u[7]), "+r"(u[8]), "+r"(u[9]), "+r"(u[10]), "+r"(u[11]),
+                 "+r"(u[12]), "+r"(u[13]), "+r"(u[14]), "+r"(u[15]), "+r"(u[16]), "+r"(u[17]),
+                 "+r"(u[18]), "+r"(u[19]), "+r"(u[20]), "+r"(u[21]), "+r"(u[22]), "+r"(u[23]),
+                 "+r"(u[24]), "+r"(u[25]), "+r"(u[26]), "+r"(u[27]), "+r"(u[28]), "+r"(u[29]),
+                 "+r"(u[30]), "+r"(u[31])
+               :
+               : "memory");
+}
+
 // Named barrier over the 128 epilogue threads.
 __device__ __forceinline__ void epilogue_bar_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kEpilogueThreads) : "memory");
@@ -479,8 +501,12 @@ __device__ __forceinline__ bool sched_next(const Params& p, Sched& s, Unit& t, u
     place_tile<BN, CG>(p, t, rank);
     return true;
   }
-  if (s.next < p.dp_tiles) {           // a whole tile
-    t.tile = s.next;
+  // By default the stream-K range comes first: the pieces that need summing
+  // finish early, and their sums overlap the main loops of the whole tiles that
+  // follow instead of trailing at the end of the kernel.
+  if (s.it >= s.it_end || (p.sk_last && s.next < p.dp_tiles)) {
+    if (s.next >= p.dp_tiles) return false;
+    t.tile = s.next;                   // a whole tile
     s.next += s.G;
     t.piece = 0;
     t.npieces = 1;
@@ -490,7 +516,7 @@ __device__ __forceinline__ bool sched_next(const Params& p, Sched& s, Unit& t, u
     place_tile<BN, CG>(p, t, rank);
     return true;
   }
-  if (s.it >= s.it_end) return false;  // the next piece of this worker's range
+  // the next piece of this worker's stream-K range
   const long long kt = p.kb_total;
   const int sk_tile = static_cast<int>(s.it / kt);
   const int k_lo = static_cast<int>(s.it - sk_tile * kt);
@@ -769,11 +795,14 @@ __device__ void run_epilogue(const Params& p, uint32_t bars, uint32_t tmem_base,
     };
 
     if (t.npieces == 1) {
-      for (int c = 0; c < chunks; ++c) {
-        uint32_t v[32];
+      // Two 32-column TMEM loads per wait halve the load round trips.
+      for (int c = 0; c < chunks; c += 2) {
+        uint32_t v[32], u[32];
         tmem_ld_32cols(taddr + 32 * c, v);
-        tmem_ld_wait(v);
+        if (c + 1 < chunks) tmem_ld_32cols(taddr + 32 * (c + 1), u);
+        tmem_ld_wait2(v, u);
         emit(32 * c, v);
+        if (c + 1 < chunks) emit(32 * (c + 1), u);
       }
       release_accumulator();
       continue;
@@ -813,46 +842,49 @@ __device__ void run_epilogue(const Params& p, uint32_t bars, uint32_t tmem_base,
     }
     if (last) {
       __threadfence();
-      // The tile's pieces sit in consecutive slots from slot0, in k order.
+      // The tile's pieces sit in consecutive slots from slot0, in k order. Each
+      // step reads 64 columns of one piece (its own from TMEM, another's from
+      // its slot: 16 independent float4 loads in flight per thread).
       const float4* base = reinterpret_cast<const float4*>(p.partials);
       const size_t slot_f4 = static_cast<size_t>(BM) * BN / 4;
-      auto load_piece = [&](int s, int c, float (&d)[32]) {
+      auto load_piece = [&](int s, int c, float (&d)[64]) {
         if (s == t.piece) {
-          uint32_t v[32];
+          uint32_t v[32], u[32];
           tmem_ld_32cols(taddr + 32 * c, v);
-          tmem_ld_wait(v);
+          if (c + 1 < chunks) tmem_ld_32cols(taddr + 32 * (c + 1), u);
+          tmem_ld_wait2(v, u);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) d[j] = __uint_as_float(v[j]);
+          for (int j = 0; j < 32; ++j) {
+            d[j] = __uint_as_float(v[j]);
+            d[32 + j] = __uint_as_float(u[j]);
+          }
         } else {
           const float4* src = base + ((static_cast<size_t>(t.slot0) + s) * CG + rank) * slot_f4;
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
+          for (int j = 0; j < 16; ++j) {
+            // chunk c covers column groups 8c .. 8c+15 over two chunks
             const float4 f = __ldcg(src + (8 * c + j) * BM + row_in_tile);
             d[4 * j] = f.x; d[4 * j + 1] = f.y; d[4 * j + 2] = f.z; d[4 * j + 3] = f.w;
           }
         }
       };
-      for (int c = 0; c < chunks; ++c) {
-        float a[32], b[32], d[32];
+      for (int c = 0; c < chunks; c += 2) {
+        float a[64], b[64];
         load_piece(0, c, a);
-        int s = 1;
-        for (; s + 1 < t.npieces; s += 2) {   // two pieces in flight, summed in order
-          load_piece(s, c, b);
-          load_piece(s + 1, c, d);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) a[j] += b[j];
-#pragma unroll
-          for (int j = 0; j < 32; ++j) a[j] += d[j];
-        }
-        if (s < t.npieces) {
+        for (int s = 1; s < t.npieces; ++s) {
           load_piece(s, c, b);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) a[j] += b[j];
+          for (int j = 0; j < 64; ++j) a[j] += b[j];
         }
         uint32_t v[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(a[j]);
         emit(32 * c, v);
+        if (c + 1 < chunks) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(a[32 + j]);
+          emit(32 * (c + 1), v);
+        }
       }
       if (et == 0) atomicExch(&p.counters[half], 0u);  // ready for the next call
     }

@@ -275,7 +275,7 @@ def test_forced_options(lib):
     d = h.describe(B.MODE_AR, 64, 256, 0, [64])
     assert d["split"] == 1
     for opt, bad in ((B.GSR_OPT_SPLIT_K, 17), (B.GSR_OPT_BLOCK_N, 64), (B.GSR_OPT_TIMEOUT_NS, -1),
-                     (B.GSR_OPT_MAX_CTAS, -5), (B.GSR_OPT_SCHEDULE, 4), (B.GSR_OPT_CTA_GROUP, 3),
+                     (B.GSR_OPT_MAX_CTAS, -5), (B.GSR_OPT_SCHEDULE, 5), (B.GSR_OPT_CTA_GROUP, 3),
                      (99, 1)):
         with pytest.raises(B.GsrError) as e:
             B.gemm_shard_plan_set_option(h.plan, opt, bad)

@@ -27,6 +27,7 @@ VARIANTS = {
     "pair128": dict(cta_group=2, block_n=128, schedule=1),
     "pair256": dict(cta_group=2, block_n=256, schedule=1),
     "pairsk8": dict(cta_group=2, schedule=2, max_ctas=8),
+    "pairsk8last": dict(cta_group=2, schedule=4, max_ctas=8),
     "pairsplit": dict(max_M=4096, max_N=8192, max_K=8192, max_R=16, cta_group=2, split_k=3),
 }
 
