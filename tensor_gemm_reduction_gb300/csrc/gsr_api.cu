@@ -185,6 +185,14 @@ Config choose_config(const gemm_shard_plan* P, int mode, int64_t M, int64_t N, i
   c.n_tiles = cdiv(N, c.block_n);
   const int64_t mt1 = count_m_tiles(1), mt2 = count_m_tiles(2);
   const int cap = P->opt_max_ctas ? std::min(P->opt_max_ctas, P->sm_count) : P->sm_count;
+  // One 128-row tile of rows (M <= 128, decode-like): single CTAs with
+  // 128-column tiles, cut into uniform pieces, measured fastest (every CTA
+  // streams its slice of W; no pair half sits idle).
+  const bool one_row_tile = mt1 == 1 && mt1 * c.n_tiles < P->sm_count;
+  if (one_row_tile && !P->opt_block_n && !P->opt_cta_group) {
+    c.block_n = 128;
+    c.n_tiles = cdiv(N, c.block_n);
+  }
 
   // CTA pairs halve each SM's bytes of B per flop and deepen the smem ring; they
   // run when there are at least as many single-CTA tiles as SMs and 256-row
@@ -198,7 +206,7 @@ Config choose_config(const gemm_shard_plan* P, int mode, int64_t M, int64_t N, i
   if (P->opt_cta_group) {
     c.cta_group = (P->opt_cta_group == 2 && pairs_fit) ? 2 : 1;
   } else if (small) {
-    c.cta_group = pairs_fit && c.block_n == 256 ? 2 : 1;
+    c.cta_group = pairs_fit && c.block_n == 256 && !one_row_tile ? 2 : 1;
   } else {
     const double eff1 = static_cast<double>(rows) / (mt1 * BM);
     const double eff2 = static_cast<double>(rows) / (mt2 * 2 * BM);

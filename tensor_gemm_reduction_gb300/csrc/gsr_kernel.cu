@@ -794,6 +794,16 @@ __device__ void run_epilogue(const Params& p, uint32_t bars, uint32_t tmem_base,
       }
     };
 
+    // A CTA half with no valid row (the second half of a pair tile past M, or
+    // the idle half of an odd AG pair) stores nothing and, with a cut tile,
+    // skips the partial/counter protocol: every piece of this half is idle
+    // alike, and its counter stays at zero.
+    const bool idle = p.mode == kModeAG ? t.shard < 0 : t.m0 >= p.M;
+    if (idle) {
+      release_accumulator();
+      continue;
+    }
+
     if (t.npieces == 1) {
       // Two 32-column TMEM loads per wait halve the load round trips.
       for (int c = 0; c < chunks; c += 2) {

@@ -203,11 +203,16 @@ def test_config_is_independent_of_mode(host):
             assert a == r
 
 
-def test_small_m_splits_pair_tiles(host):
-    # 28 single-CTA tiles < 148 SMs: 28 pair tiles (256 x 256, half the rows
-    # empty), each cut into 74 // 28 = 2 pieces of 56 k-blocks: 112 CTAs
+def test_small_m_splits_tiles(host):
+    # M = 128, one row tile: 56 single-CTA tiles of 128 x 128, each cut into
+    # 148 // 56 = 2 pieces of 56 k-blocks: 112 CTAs
     d = host.describe(B.MODE_AR, 128, 7168, 0, [896] * 8)
-    assert (d["cta_group"], d["schedule"], d["split"], d["tiles"], d["ctas"]) == (2, 1, 2, 28, 112)
+    assert (d["cta_group"], d["block_n"], d["schedule"], d["split"], d["tiles"], d["ctas"]) == \
+        (1, 128, 1, 2, 56, 112)
+    # M = 129: one 256-row pair tile keeps W read once: 28 pair tiles x 2 pieces
+    d = host.describe(B.MODE_AR, 129, 7168, 0, [896] * 8)
+    assert (d["cta_group"], d["block_n"], d["schedule"], d["split"], d["tiles"], d["ctas"]) == \
+        (2, 256, 1, 2, 28, 112)
     # stream-K on demand: every tile's 112 k-blocks shared out over all SMs
     plan2 = B.gemm_shard_plan_create_host(148, 32768, 8192, 8192, 16)
     B.gemm_shard_plan_set_option(plan2, B.GSR_OPT_SCHEDULE, 3)
