@@ -953,6 +953,14 @@ __global__ void __launch_bounds__(kThreads, 1) gsr_gemm_kernel(const __grid_cons
   tc_fence_after_sync();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
 
+  // Programmatic dependent launch: everything above (barriers, TMEM, cluster
+  // sync) may overlap the tail of the previous kernel in the stream; nothing
+  // below touches global memory before that kernel has completed and its
+  // writes are visible. A kernel launched after this one may likewise start
+  // its own set-up now; it waits for this grid the same way.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
   Ctl ctl{abort_flag, p.status, p.timeout_ns};
   if (warp == 0) {
     if (lane == 0) run_producer<BN, STAGES, CG>(p, tiles_base, bars, rank, ctl);
@@ -998,17 +1006,26 @@ cudaError_t set_smem_limit() {
 template <int BN, int CG>
 cudaError_t launch_instance(const Params& p, int ctas, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = CG;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  // May start while the previous kernel in the stream finishes (the kernel
+  // waits for it with griddepcontrol.wait before touching global memory).
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (CG == 2) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = CG;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
   cfg.gridDim = dim3(ctas, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = KernelLayout<BN, CG>::kSmem;
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = CG == 2 ? 1 : 0;
+  cfg.numAttrs = n;
   return cudaLaunchKernelEx(&cfg, gsr_gemm_kernel<BN, Stages<BN, CG>::value, CG>, p);
 }
 
