@@ -466,52 +466,70 @@ def e2e(run, w, steps, world):
     dev = dev_in[0].device
 
     if w.mode == "ag":
+        # Two device buffer sets alternate between steps, and three streams
+        # overlap: the copy stream uploads step N+1's W and shards while the
+        # GEMM stream runs step N and the readback stream returns step N-1's Y.
         R = w.R
-        A_dev, W_dev = dev_in[:R], dev_in[R]
         A_host, W_host = host_in[:R], host_in[R]
-        ready = torch.zeros(R, dtype=torch.int32, device=dev)
-        gemm_s, copy_s = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-        state = {"epoch": 0, "done": None}
+        sets = []
+        for b in range(2):
+            A_b = dev_in[:R] if b == 0 else [torch.empty_like(a) for a in dev_in[:R]]
+            W_b = dev_in[R] if b == 0 else torch.empty_like(dev_in[R])
+            Y_b = run.Y if b == 0 else torch.empty_like(run.Y)
+            sets.append({"A": A_b, "W": W_b, "Y": Y_b,
+                         "ready": torch.zeros(R, dtype=torch.int32, device=dev),
+                         "kernel_done": None, "d2h_done": None})
+        gemm_s = torch.cuda.Stream(device=dev)
+        copy_s = torch.cuda.Stream(device=dev)
+        d2h_s = torch.cuda.Stream(device=dev)
+        state = {"epoch": 0}
 
         def step():
             state["epoch"] += 1
             ep = state["epoch"]
+            bs = sets[ep % 2]
             with torch.cuda.stream(copy_s):
-                if state["done"] is not None:
-                    copy_s.wait_event(state["done"])      # previous kernel done with A, W
-                W_dev.copy_(W_host, non_blocking=True)
+                if bs["kernel_done"] is not None:
+                    copy_s.wait_event(bs["kernel_done"])   # the kernel two steps back is done reading
+                bs["W"].copy_(W_host, non_blocking=True)
                 w_in = torch.cuda.Event()
                 w_in.record(copy_s)
             with torch.cuda.stream(gemm_s):
                 gemm_s.wait_event(w_in)
-                B.gemm_ag_flagged(run.plan, A_dev, W_dev, run.Y, ready, ep, run.ws)
+                if bs["d2h_done"] is not None:
+                    gemm_s.wait_event(bs["d2h_done"])     # its output buffer has been read back
+                B.gemm_ag_flagged(run.plan, bs["A"], bs["W"], bs["Y"], bs["ready"], ep, run.ws)
                 done = torch.cuda.Event()
                 done.record(gemm_s)
-                state["done"] = done
+                bs["kernel_done"] = done
             with torch.cuda.stream(copy_s):
                 for r in range(R):
-                    A_dev[r].copy_(A_host[r], non_blocking=True)
-                    B.gemm_shard_signal(run.plan, ready.data_ptr() + 4 * r, ep, stream=copy_s)
-            with torch.cuda.stream(gemm_s):
-                host_out[0].copy_(run.Y, non_blocking=True)
+                    bs["A"][r].copy_(A_host[r], non_blocking=True)
+                    B.gemm_shard_signal(run.plan, bs["ready"].data_ptr() + 4 * r, ep, stream=copy_s)
+            with torch.cuda.stream(d2h_s):
+                d2h_s.wait_event(done)
+                host_out[0].copy_(bs["Y"], non_blocking=True)
+                out = torch.cuda.Event()
+                out.record(d2h_s)
+                bs["d2h_done"] = out
 
-        def sync_all():
-            gemm_s.synchronize()
-            copy_s.synchronize()
-
-        for _ in range(3):
+        for _ in range(4):
             step()
-        sync_all()
+        torch.cuda.synchronize()
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
         t0.record(copy_s)
         gemm_s.wait_event(t0)
+        d2h_s.wait_event(t0)
         for _ in range(steps):
             step()
+        gemm_s.wait_event(sets[state["epoch"] % 2]["d2h_done"])
+        copy_s.wait_stream(gemm_s)
         t1.record(gemm_s)
         torch.cuda.synchronize()
         B.gemm_shard_check_status(run.plan, run.ws, stream=gemm_s)
-        how = "shard copies overlap the kernel (gemm_ag_flagged + gemm_shard_signal)"
+        how = ("double-buffered: uploads, gemm_ag_flagged (shards signalled with "
+               "gemm_shard_signal) and read-backs of successive steps overlap")
     else:
         def step():
             for d, h in zip(dev_in, host_in):
