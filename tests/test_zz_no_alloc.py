@@ -58,3 +58,20 @@ def test_noalloc_rejects_oversized_scratch(setup):
         B.gemm_ar_noalloc(plan, X, W, Y)
     assert e.value.status == B.GSR_ERR_WORKSPACE
     assert "built-in scratch" in str(e.value)
+
+
+def test_noalloc_falls_back_when_the_heuristic_needs_more_scratch(setup):
+    """M=1000, N=7168: the plan's stream-K configuration needs more scratch than
+    the built-in array holds, so the call runs the uniform schedule; results
+    agree with gemm_ar within the test tolerance, on two calls in a row."""
+    plan, ws = setup
+    d = B.gemm_shard_describe(plan, B.MODE_AR, 1000, 7168, 0, [896] * 8)
+    assert d["workspace_bytes"] > 24 << 20
+    for seed in (31, 32):
+        X, W = _device_inputs(1000, 7168, [896] * 8, seed)
+        y_ref = torch.empty(1000, 7168, dtype=torch.bfloat16, device="cuda:0")
+        y_new = torch.full((1000, 7168), float("nan"), dtype=torch.bfloat16, device="cuda:0")
+        B.gemm_ar(plan, X, W, y_ref, ws)
+        B.gemm_ar_noalloc(plan, X, W, y_new)
+        torch.cuda.synchronize()
+        assert_close(to_f64(y_new), to_f64(y_ref), f"noalloc fallback, seed {seed}")
