@@ -342,6 +342,39 @@ def sweep(plan, ws, dev, pk, names):
     return rows
 
 
+def run_context_mm(args, w):
+    """torch.mm (a library GEMM, cuBLAS) on contiguous operands of the same
+    shapes: the fused path's context row, not its target. One JSON line per
+    workload (--sweep-only names, else --workload), timed like the sweep: a
+    median of --steps launches, each after an L2 flush."""
+    import torch
+    dev = torch.device("cuda:0")
+    flush_buf = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    names = [s for s in args.sweep_only.split(",") if s] or [w.name]
+    for name in names:
+        wl = workload_by_name(name)
+        g = torch.Generator(device=dev)
+        g.manual_seed(0)
+        A = torch.randn(wl.M, wl.K, generator=g, device=dev).to(torch.bfloat16)
+        W = (torch.randn(wl.N, wl.K, generator=g, device=dev) / math.sqrt(wl.K)).to(torch.bfloat16)
+        Y = torch.empty(wl.M, wl.N, dtype=torch.bfloat16, device=dev)
+        fn = lambda: torch.mm(A, W.t(), out=Y)
+        times, _ = time_launches(fn, steps=args.steps, warmup=args.warmup,
+                                 flush=lambda: flush_buf.fill_(1))
+        if args.profile_window:
+            torch.cuda.synchronize()
+            torch.cuda.cudart().cudaProfilerStart()
+            fn()
+            torch.cuda.synchronize()
+            torch.cuda.cudart().cudaProfilerStop()
+        t = statistics.median(times) * 1e-3
+        print(json.dumps({"context": "torch_mm", "workload": wl.name, "M": wl.M, "N": wl.N, "K": wl.K,
+                          "us": round(t * 1e6, 2), "tflops": round(wl.flops / t / 1e12, 1),
+                          "steps": args.steps, "l2": "flushed before every launch"}), flush=True)
+        del A, W, Y
+        torch.cuda.empty_cache()
+
+
 def B_describe(plan, w):
     from tensor_gemm_reduction_gb300 import binding as B
     mode = {"ar": B.MODE_AR, "rs": B.MODE_RS, "ag": B.MODE_AG}[w.mode]
@@ -362,10 +395,18 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--ref-rows", type=int, default=4, help="output rows per reference step")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--context", choices=("torch_mm",), default=None,
+                    help="time torch.mm (cuBLAS) on the concatenated operands instead (context only)")
+    ap.add_argument("--profile-window", action="store_true",
+                    help="with --context: bracket one warm launch with cudaProfilerStart/Stop")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
     w = workload_by_name(args.workload)
+
+    if args.context is not None:
+        run_context_mm(args, w)
+        return
 
     if args.impl == "reference":
         run_reference(args, w)

@@ -6,15 +6,17 @@
 // AR differing only in where the reduced rows go; PR #54151 "[Kimi-K3] AG-GEMM
 // for Sequence Parallelism", Purpose: GEMM over gathered activation shards):
 //
-//   warp 0      TMA producer: for each work unit, walks its k-blocks; in AR/RS
+//   warp 0      TMA producer (the whole warp walks the schedule; one elected
+//               lane issues each copy): for each work unit, walks its k-blocks; in AR/RS
 //               mode a k-block belongs to one K-shard and is fetched through
 //               that shard's descriptors (X_r, W_r) straight from the shard's
 //               own allocation; in AG mode the unit's M-shard descriptor A_r
 //               and the single W descriptor are used. No operand is copied or
 //               padded: rows or columns past a shard's extent are zero-filled
 //               by the TMA unit.
-//   warp 1      MMA issuer: one thread issues tcgen05.mma (kind::f16, bf16 in,
-//               fp32 accumulate) into a TMEM accumulator. In AR/RS mode the
+//   warp 1      MMA issuer: the whole warp walks the schedule with warp-uniform
+//               values and one elected lane issues tcgen05.mma (kind::f16, bf16
+//               in, fp32 accumulate) into a TMEM accumulator. In AR/RS mode the
 //               accumulator runs across every shard's k-blocks, so the
 //               cross-shard sum happens inside the tensor-core accumulator.
 //               Two accumulators (2 x BN TMEM columns) let the epilogue of one
@@ -58,9 +60,14 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
 
+// The producer helpers (expect_tx, TMA loads, descriptor prefetch) are called
+// by a whole converged warp with warp-uniform operands; one elected lane acts.
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n\t}" ::"r"(bar), "r"(bytes)
+      : "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
@@ -79,22 +86,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return done != 0;
 }
 
-// 2-D tiled TMA load into this CTA's shared memory, completing on `bar`.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                            int x, int y) {
+// Non-blocking test of the same phase condition.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t done;
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
       : "memory");
+  return done != 0;
 }
 
-// Same load with an L2 cache policy (from createpolicy) attached.
+// 2-D tiled TMA load into this CTA's shared memory, completing on `bar`, with
+// an L2 cache policy (from createpolicy) attached.
 __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                                  int x, int y, uint64_t policy) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4}], [%2], %5;\n\t}" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "l"(policy)
       : "memory");
 }
@@ -111,7 +124,11 @@ __device__ __forceinline__ uint64_t make_l2_policy(int kind) {
 }
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
-  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e prefetch.tensormap [%0];\n\t}" ::"l"(reinterpret_cast<uint64_t>(map))
+      : "memory");
 }
 
 __device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
@@ -138,20 +155,25 @@ __device__ __forceinline__ void tc_fence_after_sync() {
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, both K-major bf16, fp32 accumulate.
+// Called by a whole converged warp with warp-uniform operands; one elected
+// lane issues the MMA (the MMA and commit helpers below all work this way).
 __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                             uint32_t idesc, uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
+      "{\n\t.reg .pred e, p;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
-// Arrive once on `bar` when every tcgen05 op this thread issued so far is done.
+// Arrive once on `bar` when every tcgen05 op the elected lane issued so far is done.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
       : "memory");
 }
 
@@ -267,8 +289,10 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
                                                  uint32_t bar_cluster, int x, int y,
                                                  uint64_t policy) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;\n\t}" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y), "l"(policy)
       : "memory");
 }
@@ -292,19 +316,22 @@ __device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols
 __device__ __forceinline__ void mma_bf16_ss_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                                  uint32_t idesc, uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
+      "{\n\t.reg .pred e, p;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
 // Arrive once on the mbarrier at offset `bar` in every CTA of `mask` when all
-// tcgen05 ops this thread issued so far are done.
+// tcgen05 ops the elected lane issued so far are done.
 __device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t mask) {
   asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(bar),
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;\n\t}" ::"r"(bar),
       "h"(mask)
       : "memory");
 }
@@ -578,13 +605,16 @@ __device__ void run_producer(const Params& p, uint32_t tiles_base, uint32_t bars
   const uint64_t pol_a = make_l2_policy(p.policy_a);
   const uint64_t pol_b = make_l2_policy(p.policy_b);
   uint32_t issued = 0;
+  uint32_t slot = 0, slot_parity = 1;   // ring slot of the next load; its free-wait parity
   uint32_t arrived = 0;   // AG with arrival flags: shards seen ready (bit r)
   bool ok = true;
   Sched sch = sched_begin<CG>(p);
   Unit t;
   while (ok && sched_next<BN, CG>(p, sch, t, rank)) {
     if (p.ready != nullptr && t.shard >= 0 && !(arrived & (1u << t.shard))) {
-      if (!wait_flag(p.ready + t.shard, p.epoch, ctl, (kRoleProducer << 8) | 3)) {
+      const bool here = wait_flag(p.ready + t.shard, p.epoch, ctl, (kRoleProducer << 8) | 3);
+      __syncwarp();
+      if (!here) {
         ok = false;
         break;
       }
@@ -601,9 +631,10 @@ __device__ void run_producer(const Params& p, uint32_t tiles_base, uint32_t bars
     if (p.mode != kModeAG)
       while (p.shard_kb_begin[r + 1] <= t.kb_begin) ++r;
     for (int kb = t.kb_begin; kb < t.kb_end; ++kb) {
-      const uint32_t stage = issued % STAGES;
-      const uint32_t parity = ((issued / STAGES) & 1u) ^ 1u;
-      if (!wait_bounded(empty0 + 8 * stage, parity, ctl, (kRoleProducer << 8) | 1)) {
+      const uint32_t stage = slot;
+      const bool free_slot = wait_bounded(empty0 + 8 * stage, slot_parity, ctl, (kRoleProducer << 8) | 1);
+      __syncwarp();
+      if (!free_slot) {
         ok = false;
         break;
       }
@@ -636,6 +667,10 @@ __device__ void run_producer(const Params& p, uint32_t tiles_base, uint32_t bars
         tma_load_2d_pair(sb, mb, lead_full, kx, b_row, pol_b);
       }
       ++issued;
+      if (++slot == STAGES) {
+        slot = 0;
+        slot_parity ^= 1u;
+      }
     }
   }
   if (!ok && (CG == 1 || rank == 0)) {
@@ -654,30 +689,45 @@ __device__ void run_mma(const Params& p, uint32_t tiles_base, uint32_t bars, uin
   const uint32_t full0 = bars, tfull0 = bars + 16 * STAGES, tempty0 = tfull0 + 16;
   const uint32_t empty0 = bars + 8 * STAGES, drain = tempty0 + 16;
   const uint32_t rank = 0;   // only the leader issues MMAs; tile k ranges do not depend on rank
-  uint32_t consumed = 0, local = 0;
+  uint32_t stage = 0, phase = 0, local = 0;   // next ring slot and its fill phase
   bool ok = true, issued_any = false;
   Sched sch = sched_begin<CG>(p);
   Unit t;
   for (; ok && sched_next<BN, CG>(p, sch, t, rank); ++local) {
     const uint32_t acc = local & 1u;
     const uint32_t acc_parity = ((local >> 1) & 1u) ^ 1u;
-    if (!wait_bounded(tempty0 + 8 * acc, acc_parity, ctl, (kRoleMma << 8) | 1)) {
+    const bool free_acc = wait_bounded(tempty0 + 8 * acc, acc_parity, ctl, (kRoleMma << 8) | 1);
+    __syncwarp();
+    if (!free_acc) {
       ok = false;
       break;
     }
     tc_fence_after_sync();
     const uint32_t d_tmem = tmem_base + acc * BN;
     const uint32_t idesc = make_idesc(BM * CG, tile_mma_n<BN>(p, t));
+    // The next slot's barrier is tested (without blocking) before this slot's
+    // MMAs are issued, so the test overlaps the tensor pipe's work instead of
+    // sitting between the MMAs of two consecutive k-blocks. The slot's bytes
+    // were written by TMA and read by the MMAs, both in the async proxy; the
+    // barrier's completion orders them.
+    bool ready = mbar_test_wait(full0 + 8 * stage, phase);
     for (int kb = t.kb_begin; kb < t.kb_end; ++kb) {
-      const uint32_t stage = consumed % STAGES;
-      const uint32_t parity = (consumed / STAGES) & 1u;
-      if (!wait_bounded(full0 + 8 * stage, parity, ctl, (kRoleMma << 8) | 2)) {
-        ok = false;
-        break;
+      if (!ready) {
+        const bool got = wait_bounded(full0 + 8 * stage, phase, ctl, (kRoleMma << 8) | 2);
+        __syncwarp();
+        if (!got) {
+          ok = false;
+          break;
+        }
       }
-      tc_fence_after_sync();
-      const uint64_t a_desc = smem_desc_sw128(tiles_base + stage * L::kABytes);
-      const uint64_t b_desc = smem_desc_sw128(tiles_base + STAGES * L::kABytes + stage * L::kBBytes);
+      const uint32_t cur = stage;
+      if (++stage == STAGES) {
+        stage = 0;
+        phase ^= 1u;
+      }
+      ready = kb + 1 < t.kb_end && mbar_test_wait(full0 + 8 * stage, phase);
+      const uint64_t a_desc = smem_desc_sw128(tiles_base + cur * L::kABytes);
+      const uint64_t b_desc = smem_desc_sw128(tiles_base + STAGES * L::kABytes + cur * L::kBBytes);
 #pragma unroll
       for (int k = 0; k < BK / 16; ++k) {
         // advance 16 elements (32 bytes) along K inside the swizzled 128-byte rows
@@ -689,10 +739,9 @@ __device__ void run_mma(const Params& p, uint32_t tiles_base, uint32_t bars, uin
       }
       issued_any = true;
       if constexpr (CG == 1)
-        mma_commit(empty0 + 8 * stage);
+        mma_commit(empty0 + 8 * cur);
       else
-        mma_commit_pair(empty0 + 8 * stage, 0x3);   // frees the stage in both CTAs
-      ++consumed;
+        mma_commit_pair(empty0 + 8 * cur, 0x3);     // frees the slot in both CTAs
     }
     if (!ok) break;
     if constexpr (CG == 1)
@@ -963,10 +1012,12 @@ __global__ void __launch_bounds__(kThreads, 1) gsr_gemm_kernel(const __grid_cons
 
   Ctl ctl{abort_flag, p.status, p.timeout_ns};
   if (warp == 0) {
-    if (lane == 0) run_producer<BN, STAGES, CG>(p, tiles_base, bars, rank, ctl);
+    run_producer<BN, STAGES, CG>(p, tiles_base, bars, rank, ctl);   // whole warp, elected issue
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0 && rank == 0) run_mma<BN, STAGES, CG>(p, tiles_base, bars, tmem_base, ctl);
+    // The whole warp walks the MMA loop (its values stay warp-uniform); one
+    // elected lane issues each MMA and commit.
+    if (rank == 0) run_mma<BN, STAGES, CG>(p, tiles_base, bars, tmem_base, ctl);
     __syncwarp();
   } else {
     run_epilogue<BN, STAGES, CG>(p, bars, tmem_base, rank, last_flag, ctl);
