@@ -83,13 +83,23 @@ typedef enum {
                                3 = A evict-first / B evict-last                     */
     GSR_OPT_CTA_GROUP = 7,  /* CTAs per MMA tile: 0 = heuristic, 1 = one CTA per
                                128-row tile, 2 = a CTA pair per 256-row tile        */
-    GSR_OPT_SCHEDULE = 8    /* work schedule: 0 = heuristic (stream-K over the
+    GSR_OPT_SCHEDULE = 8,   /* work schedule: 0 = heuristic (stream-K over the
                                partial last wave), 1 = uniform (every tile cut
                                into the same number of pieces), 2 = stream-K
                                over the last one or two waves, 3 = stream-K
                                over the partial last wave, each worker's
                                stream-K range before its whole tiles, 4 = as 3
                                with the whole tiles first                        */
+    GSR_OPT_SMALL_M = 9     /* the small-M kernel (AR/RS, M <= 256): 0 = heuristic
+                               (used when M <= 256 and no other option above
+                               forces a configuration), 1 = never, 2 = whenever
+                               M <= 256 and the K range has at least two
+                               k-blocks of 64. It streams W in 128-row tiles
+                               against all M rows at once (the activation rows
+                               are the MMA's N), each tile split over K between
+                               the two CTAs of a cluster and summed in
+                               distributed shared memory; it needs no workspace
+                               beyond the status word                            */
 } gsr_option;
 
 /*
@@ -295,7 +305,9 @@ const char *gsr_last_error_string(void);
 typedef struct {
     int block_n;            /* output tile width: 128 or 256                        */
     int cta_group;          /* 1: a CTA per 128-row tile; 2: a CTA pair per 256 rows */
-    int schedule;           /* 1 = uniform pieces, 2 = stream-K hybrid              */
+    int schedule;           /* 1 = uniform pieces, 2 = stream-K hybrid, 3 = the
+                               small-M kernel (block_n = 128 W rows per tile, split
+                               = 2 halves of K per tile on a cluster of two CTAs) */
     int split;              /* uniform schedule: pieces per tile                    */
     int64_t tiles;          /* output tiles                                         */
     int64_t dp_tiles;       /* stream-K: tiles run whole                            */

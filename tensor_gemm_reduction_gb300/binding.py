@@ -33,6 +33,7 @@ GSR_OPT_RASTER_M = 5
 GSR_OPT_L2_HINTS = 6
 GSR_OPT_CTA_GROUP = 7
 GSR_OPT_SCHEDULE = 8
+GSR_OPT_SMALL_M = 9
 
 MODE_AR, MODE_RS, MODE_AG = 0, 1, 2
 

@@ -37,6 +37,7 @@ struct gemm_shard_plan {
   int opt_cta_group;   // 0 = heuristic
   int opt_schedule;    // 0 = heuristic (stream-K hybrid), 1 = uniform, 2 = stream-K hybrid,
                        // 3 = stream-K only for a partial last wave
+  int opt_small;       // 0 = heuristic, 1 = never use the small-M kernel, 2 = always when it applies
   int pair_clusters;   // CTA pairs that can be resident at once
   uint64_t timeout_ns;
 };
@@ -151,6 +152,9 @@ struct Config {
   int policy_a = gsr::kPolicyNormal;
   int policy_b = gsr::kPolicyNormal;
   size_t ws_bytes = 0;
+  int small = 0;      // the small-M kernel (K-pair clusters, operands swapped)
+  int m_pad = 0;      // small-M: activation rows rounded up to 16 (the MMA's N)
+  int stages = 0;     // small-M: ring depth
 };
 
 
@@ -160,6 +164,41 @@ struct Config {
 Config choose_config(const gemm_shard_plan* P, int mode, int64_t M, int64_t N, int64_t K_ag, int R,
                      const int64_t* sizes) {
   Config c;
+  // Small M (AR/RS, a decode-like batch of at most 256 rows): streaming W is
+  // the whole cost, so the small-M kernel runs every activation row against
+  // 128-row tiles of W, each tile split over K between the two CTAs of a
+  // cluster. Like every choice here it depends on the shape, not on the mode.
+  if (mode != gsr::kModeAG && M >= 1 && M <= gsr::kSmallMaxM && P->opt_small != 1) {
+    int64_t kb = 0;
+    for (int r = 0; r < R; ++r) kb += cdiv(sizes[r], BK);
+    const bool forced = P->opt_split || P->opt_block_n || P->opt_cta_group || P->opt_schedule;
+    if (kb >= 2 && (P->opt_small == 2 || !forced)) {
+      c.small = 1;
+      c.m_pad = static_cast<int>(std::max<int64_t>(16, cdiv(M, 16) * 16));
+      c.stages = gsr::small_stages(c.m_pad);
+      c.block_n = gsr::kSmallTileN;
+      c.cta_group = 1;
+      c.sched = gsr::kSchedKPair;
+      c.splits = 2;
+      c.kb_total = kb;
+      c.m_tiles = 1;
+      c.n_tiles = cdiv(N, gsr::kSmallTileN);
+      c.tiles = c.n_tiles;
+      c.units = 2 * c.tiles;
+      const int cap = P->opt_max_ctas ? std::min(P->opt_max_ctas, P->sm_count) : P->sm_count;
+      c.ctas = static_cast<int>(2 * std::min<int64_t>(c.tiles, std::max(cap / 2, 1)));
+      // Every cluster reads all of X and a disjoint slice of W.
+      const int hints = P->opt_l2_hints;
+      c.policy_a = (hints == 0 || hints == 2) ? gsr::kPolicyEvictLast
+                   : hints == 3               ? gsr::kPolicyEvictFirst
+                                              : gsr::kPolicyNormal;
+      c.policy_b = (hints == 0 || hints == 2) ? gsr::kPolicyEvictFirst
+                   : hints == 3               ? gsr::kPolicyEvictLast
+                                              : gsr::kPolicyNormal;
+      c.ws_bytes = gsr::kWsHeader + counters_bytes(P);
+      return c;
+    }
+  }
   c.block_n = P->opt_block_n ? P->opt_block_n : (N <= 128 ? 128 : 256);
   // Tile rows: 128 per CTA; a CTA pair (cta_group 2) covers 256. AG tiles never
   // cross a shard.
@@ -332,6 +371,8 @@ void fill_common(gsr::Params& p, const gemm_shard_plan* P, const Config& c, int 
   p.group_m = c.group_m;
   p.policy_a = c.policy_a;
   p.policy_b = c.policy_b;
+  p.m_pad = c.m_pad;
+  p.stages = c.stages;
   p.timeout_ns = P->timeout_ns;
   uint8_t* w = static_cast<uint8_t*>(ws);
   p.status = reinterpret_cast<uint32_t*>(w);
@@ -344,8 +385,9 @@ gsr_status launch(const gemm_shard_plan* P, const gsr::Params& p, const Config& 
   if (P->device < 0) return fail(GSR_ERR_UNSUPPORTED, "host plan: arguments are valid, nothing launched");
   DeviceScope scope(P->device);
   if (scope.err != cudaSuccess) return cuda_fail(scope.err, "selecting the plan's device");
-  cudaError_t e = gsr::launch_gemm(p, c.block_n, c.cta_group, c.ctas,
-                                   reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t e = c.small ? gsr::launch_small(p, c.ctas, reinterpret_cast<cudaStream_t>(stream))
+                          : gsr::launch_gemm(p, c.block_n, c.cta_group, c.ctas,
+                                             reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
   return ok();
 }
@@ -417,7 +459,8 @@ gsr_status run_ksharded(const gemm_shard_plan* P, int mode, int64_t M, int64_t N
   for (int r = 0; r < R; ++r) {
     p.shard_kb_begin[r] = kb;
     kb += static_cast<int>(cdiv(K_r[r], BK));
-    CUresult cr = encode_kmajor(&p.tmap_a[r], X_r[r], M, K_r[r], BM);
+    // The small-M kernel loads all m_pad activation rows at once.
+    CUresult cr = encode_kmajor(&p.tmap_a[r], X_r[r], M, K_r[r], c.small ? c.m_pad : BM);
     if (cr != CUDA_SUCCESS) return fail(GSR_ERR_CUDA, "encoding X_r[%d] descriptor failed (%d)", r, (int)cr);
     cr = encode_kmajor(&p.tmap_b[r], W_r[r], N, K_r[r], c.block_n / c.cta_group);
     if (cr != CUDA_SUCCESS) return fail(GSR_ERR_CUDA, "encoding W_r[%d] descriptor failed (%d)", r, (int)cr);
@@ -469,6 +512,7 @@ static gemm_shard_plan* new_plan(int device, int sm_count, int64_t max_M, int64_
   P->opt_l2_hints = 0;
   P->opt_cta_group = 0;
   P->opt_schedule = 0;
+  P->opt_small = 0;
   P->pair_clusters = sm_count / 2;   // host plans: every SM pairs up
   P->timeout_ns = 2000000000ull;
   return P;
@@ -508,6 +552,7 @@ gsr_status gemm_shard_plan_create(gemm_shard_plan** out, int device, int64_t max
       return fail(GSR_ERR_UNSUPPORTED, "device allows %zu bytes of shared memory per block; %zu needed",
                   static_cast<size_t>(prop.sharedMemPerBlockOptin), need);
     e = gsr::prepare_kernels(device, &pair_clusters);
+    if (e == cudaSuccess) e = gsr::prepare_small_kernel();
     if (e != cudaSuccess) return cuda_fail(e, "configuring the kernels");
   }
   *out = new_plan(device, prop.multiProcessorCount, max_M, max_N, max_K, max_R);
@@ -556,6 +601,10 @@ gsr_status gemm_shard_plan_set_option(gemm_shard_plan* plan, gsr_option option, 
     case GSR_OPT_SCHEDULE:
       if (value < 0 || value > 4) return fail(GSR_ERR_INVALID_VALUE, "schedule must be 0..4");
       plan->opt_schedule = static_cast<int>(value);
+      return ok();
+    case GSR_OPT_SMALL_M:
+      if (value < 0 || value > 2) return fail(GSR_ERR_INVALID_VALUE, "small_m must be 0..2");
+      plan->opt_small = static_cast<int>(value);
       return ok();
   }
   return fail(GSR_ERR_INVALID_VALUE, "unknown option %d", static_cast<int>(option));
@@ -753,7 +802,7 @@ gsr_status gemm_shard_describe(const gemm_shard_plan* P, int mode, int64_t M, in
   const Config c = choose_config(P, mode, M, N, K, R, sizes);
   out->block_n = c.block_n;
   out->cta_group = c.cta_group;
-  out->schedule = c.sched == gsr::kSchedStreamK ? 2 : 1;
+  out->schedule = c.small ? 3 : c.sched == gsr::kSchedStreamK ? 2 : 1;
   out->split = c.splits;
   out->tiles = c.tiles;
   out->dp_tiles = c.sched == gsr::kSchedStreamK ? c.dp_tiles : c.tiles;

@@ -39,404 +39,11 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "gsr_device.cuh"
 #include "gsr_params.h"
 
 namespace gsr {
 namespace {
-
-// ------------------------------------------------------------------ PTX glue
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ uint64_t global_timer_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-// The producer helpers (expect_tx, TMA loads, descriptor prefetch) are called
-// by a whole converged warp with warp-uniform operands; one elected lane acts.
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile(
-      "{\n\t.reg .pred e;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "@e mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n\t}" ::"r"(bar), "r"(bytes)
-      : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t done;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(done)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return done != 0;
-}
-
-// Non-blocking test of the same phase condition.
-__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
-  uint32_t done;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(done)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return done != 0;
-}
-
-// 2-D tiled TMA load into this CTA's shared memory, completing on `bar`, with
-// an L2 cache policy (from createpolicy) attached.
-__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                                 int x, int y, uint64_t policy) {
-  asm volatile(
-      "{\n\t.reg .pred e;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "@e cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%3, %4}], [%2], %5;\n\t}" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "l"(policy)
-      : "memory");
-}
-
-__device__ __forceinline__ uint64_t make_l2_policy(int kind) {
-  uint64_t pol;
-  if (kind == kPolicyEvictLast)
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
-  else if (kind == kPolicyEvictFirst)
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-  else
-    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
-  return pol;
-}
-
-__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
-  asm volatile(
-      "{\n\t.reg .pred e;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "@e prefetch.tensormap [%0];\n\t}" ::"l"(reinterpret_cast<uint64_t>(map))
-      : "memory");
-}
-
-__device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem),
-               "r"(ncols)
-               : "memory");
-}
-
-__device__ __forceinline__ void tmem_relinquish() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-               : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before_sync() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-
-__device__ __forceinline__ void tc_fence_after_sync() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-// D[tmem] (+)= A[smem] * B[smem]^T, both K-major bf16, fp32 accumulate.
-// Called by a whole converged warp with warp-uniform operands; one elected
-// lane issues the MMA (the MMA and commit helpers below all work this way).
-__device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                            uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred e, p;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// Arrive once on `bar` when every tcgen05 op the elected lane issued so far is done.
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile(
-      "{\n\t.reg .pred e;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
-      : "memory");
-}
-
-// Each thread of the warp reads 32 consecutive fp32 columns of its own TMEM lane.
-__device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, uint32_t (&v)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
-        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
-        "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]),
-        "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
-        "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
-      : "r"(taddr));
-}
-
-// Wait for this thread's tcgen05.ld results; the registers are tied to the wait so
-// that no use of them can be scheduled before it.
-__device__ __forceinline__ void tmem_ld_wait(uint32_t (&v)[32]) {
-  asm volatile("tcgen05.wait::ld.sync.aligned;"
-               : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]),
-                 "+r"(v[6]), "+r"(v[7]), "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]),
-                 "+r"(v[12]), "+r"(v[13]), "+r"(v[14]), "+r"(v[15]), "+r"(v[16]), "+r"(v[17]),
-                 "+r"(v[18]), "+r"(v[19]), "+r"(v[20]), "+r"(v[21]), "+r"(v[22]), "+r"(v[23]),
-                 "+r"(v[24]), "+r"(v[25]), "+r"(v[26]), "+r"(v[27]), "+r"(v[28]), "+r"(v[29]),
-                 "+r"(v[30]), "+r"(v[31])
-               :
-               : "memory");
-}
-
-__device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-// Wait for two batches of tcgen05.ld results at once.
-__device__ __forceinline__ void tmem_ld_wait2(uint32_t (&v)[32], uint32_t (&u)[32]) {
-  asm volatile("tcgen05.wait::ld.sync.aligned;"
-               : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]),
-                 "+r"(v[6]), "+r"(v[7]), "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]),
-                 "+r"(v[12]), "+r"(v[13]), "+r"(v[14]), "+r"(v[15]), "+r"(v[16]), "+r"(v[17]),
-                 "+r"(v[18]), "+r"(v[19]), "+r"(v[20]), "+r"(v[21]), "+r"(v[22]), "+r"(v[23]),
-                 "+r"(v[24]), "+r"(v[25]), "+r"(v[26]), "+r"(v[27]), "+r"(v[28]), "+r"(v[29]),
-                 "+r"(v[30]), "+r"(v[31])
-               :
-               : "memory");
-  asm volatile(""
-               : "+r"(u[0]), "+r"(u[1]), "+r"(u[2]), "+r"(u[3]), "+r"(u[4]), "+r"(u[5]),
-                 "+r"(u[6]), "+r"(u[7]), "+r"(u[8]), "+r"(u[9]), "+r"(u[10]), "+r"(u[11]),
-                 "+r"(u[12]), "+r"(u[13]), "+r"(u[14]), "+r"(u[15]), "+r"(u[16]), "+r"(u[17]),
-                 "+r"(u[18]), "+r"(u[19]), "+r"(u[20]), "+r"(u[21]), "+r"(u[22]), "+r"(u[23]),
-                 "+r"(u[24]), "+r"(u[25]), "+r"(u[26]), "+r"(u[27]), "+r"(u[28]), "+r"(u[29]),
-                 "+r"(u[30]), "+r"(u[31])
-               :
-               : "memory");
-}
-
-// Named barrier over the 128 epilogue threads.
-__device__ __forceinline__ void epilogue_bar_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kEpilogueThreads) : "memory");
-}
-
-// Named barrier over the epilogue threads that also ANDs a predicate.
-__device__ __forceinline__ bool epilogue_bar_and(bool v) {
-  uint32_t out;
-  asm volatile(
-      "{\n\t.reg .pred pi, po;\n\t"
-      "setp.ne.u32 pi, %1, 0;\n\t"
-      "bar.red.and.pred po, 1, %2, pi;\n\t"
-      "selp.u32 %0, 1, 0, po;\n\t}"
-      : "=r"(out)
-      : "r"(static_cast<uint32_t>(v)), "n"(kEpilogueThreads)
-      : "memory");
-  return out != 0;
-}
-
-// ------------------------------------------------------------ CTA-pair glue
-// A CTA pair is a cluster of two CTAs (ranks 0 and 1); rank 0 issues the
-// pair's MMAs (cta_group::2), each CTA holds half of A (rows) and half of B
-// (columns of the output) in its own shared memory and TMEM.
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-// Shared-memory address `addr` of this CTA, as seen in CTA `rank` of the cluster.
-__device__ __forceinline__ uint32_t map_shared_to_rank(uint32_t addr, uint32_t rank) {
-  uint32_t out;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(addr), "r"(rank));
-  return out;
-}
-
-__device__ __forceinline__ void cluster_barrier() {
-  asm volatile(
-      "barrier.cluster.arrive.release.aligned;\n\t"
-      "barrier.cluster.wait.acquire.aligned;" ::
-          : "memory");
-}
-
-// Arrive on an mbarrier given by its shared::cluster address (possibly the peer's).
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-               : "memory");
-}
-
-// TMA load into this CTA's shared memory whose completion is counted on an
-// mbarrier of either CTA of the pair (the leader's).
-__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map,
-                                                 uint32_t bar_cluster, int x, int y,
-                                                 uint64_t policy) {
-  asm volatile(
-      "{\n\t.reg .pred e;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "@e cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;\n\t}" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y), "l"(policy)
-      : "memory");
-}
-
-__device__ __forceinline__ void tmem_alloc_pair(uint32_t slot_smem, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem),
-               "r"(ncols)
-               : "memory");
-}
-
-__device__ __forceinline__ void tmem_relinquish_pair() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-               : "memory");
-}
-
-// D (256 rows split over the pair's TMEM) (+)= A (pair halves) * B (pair halves)^T.
-__device__ __forceinline__ void mma_bf16_ss_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                                 uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred e, p;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// Arrive once on the mbarrier at offset `bar` in every CTA of `mask` when all
-// tcgen05 ops the elected lane issued so far are done.
-__device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t mask) {
-  asm volatile(
-      "{\n\t.reg .pred e;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;\n\t}" ::"r"(bar),
-      "h"(mask)
-      : "memory");
-}
-
-// ------------------------------------------------------------ descriptors
-
-// Shared-memory matrix descriptor of a K-major bf16 tile written by TMA with
-// 128-byte swizzling: rows of 64 elements (128 B), 8-row groups 1024 B apart.
-// Fields: start address >> 4 in bits 0-13; leading byte offset (unused for
-// swizzled K-major, set to 1) in 16-29; stride byte offset 1024 >> 4 in
-// 32-45; descriptor version 1 in 46-47; base offset 0 (tiles are 1024-byte
-// aligned); swizzle mode 2 (128-byte) in 61-63.
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-  d |= static_cast<uint64_t>(1) << 16;
-  d |= static_cast<uint64_t>(1024 >> 4) << 32;
-  d |= static_cast<uint64_t>(1) << 46;
-  d |= static_cast<uint64_t>(2) << 61;
-  return d;
-}
-
-// Instruction descriptor for kind::f16: D fp32 (bits 4-5 = 1), A bf16 (7-9 = 1),
-// B bf16 (10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 in 17-22,
-// M >> 4 in 24-28.
-__device__ __forceinline__ uint32_t make_idesc(uint32_t mma_m, uint32_t mma_n) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((mma_n >> 3) << 17) | ((mma_m >> 4) << 24);
-}
-
-__device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo_bits, uint32_t hi_bits) {
-  __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(lo_bits), __uint_as_float(hi_bits));
-  return *reinterpret_cast<uint32_t*>(&h);
-}
-
-// ------------------------------------------------------------ bounded waits
-
-struct Ctl {
-  volatile int* abort;    // shared: set by the first role whose wait runs out
-  uint32_t* status;       // global: workspace status word
-  uint64_t timeout_ns;
-};
-
-// Role ids stored in the timeout code.
-enum : uint32_t { kRoleProducer = 1, kRoleMma = 2, kRoleEpilogue = 3 };
-
-// Limits grow along the dependency chain (producer x1, MMA x2, epilogue x3),
-// so when something upstream never arrives the wait closest to the cause runs
-// out first and its site is the one recorded.
-__device__ __noinline__ bool wait_bounded_slow(uint32_t bar, uint32_t parity, const Ctl& c,
-                                               uint32_t site) {
-  const uint64_t t0 = global_timer_ns();
-  const uint64_t limit = c.timeout_ns * (site >> 8);
-  for (uint32_t spin = 1;; ++spin) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((spin & 31u) == 0) {
-      if (*c.abort) return false;
-      if (global_timer_ns() - t0 > limit) {
-        *c.abort = 1;
-        atomicCAS(c.status, 0u, kStatusTimeout | site);
-        return false;
-      }
-    }
-  }
-}
-
-// The common case (the phase already complete) costs one try_wait and no call.
-__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const Ctl& c,
-                                             uint32_t site) {
-  if (mbar_try_wait(bar, parity)) return true;
-  return wait_bounded_slow(bar, parity, c, site);
-}
-
-// Wait until the arrival word `flag` reaches `epoch` (wrap-around compare),
-// bounded like every other wait. The word is written by another agent (a copy
-// stream's memory operation), so it is read with acquire semantics at GPU scope,
-// and the async proxy is fenced before TMA reads the data it guards.
-__device__ __noinline__ bool wait_flag(const uint32_t* flag, uint32_t epoch, const Ctl& c,
-                                       uint32_t site) {
-  const uint64_t t0 = global_timer_ns();
-  for (uint32_t spin = 0;; ++spin) {
-    uint32_t v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
-    if (static_cast<int32_t>(v - epoch) >= 0) {
-      asm volatile("fence.proxy.async.global;" ::: "memory");
-      return true;
-    }
-    if (*c.abort) return false;
-    if (global_timer_ns() - t0 > c.timeout_ns) {
-      *c.abort = 1;
-      atomicCAS(c.status, 0u, kStatusTimeout | site);
-      return false;
-    }
-    __nanosleep(spin < 64 ? 32 : 256);
-  }
-}
-
-// Used only on the way out after an abort: wait for copies or MMAs already
-// issued, ignoring the abort flag, for at most limit_ns.
-__device__ __noinline__ bool wait_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
-  const uint64_t t0 = global_timer_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (global_timer_ns() - t0 > limit_ns) return false;
-  }
-  return true;
-}
 
 // ------------------------------------------------------------ scheduling
 

@@ -21,7 +21,10 @@ enum Mode : int { kModeAR = 0, kModeRS = 1, kModeAG = 2, kModeARRep = 3 };
 // the remaining tiles, in tile order, are cut into one contiguous range per
 // worker (a CTA, or a CTA pair), and a tile cut by a worker boundary is
 // summed by the last of its pieces to finish, in k order.
-enum Sched : int { kSchedUniform = 0, kSchedStreamK = 1 };
+// K-pair (small-M kernel): each output tile is computed by the two CTAs of a
+// cluster, each over half of the k-blocks, and the two halves are added in
+// distributed shared memory.
+enum Sched : int { kSchedUniform = 0, kSchedStreamK = 1, kSchedKPair = 2 };
 
 // L2 eviction priority requested for an operand's TMA loads.
 enum Policy : int { kPolicyNormal = 0, kPolicyEvictFirst = 1, kPolicyEvictLast = 2 };
@@ -77,7 +80,59 @@ struct Params {  // 128-byte aligned through its CUtensorMap members
                                 // by the idle half of an odd last pair tile
   int shard_row_begin[kMaxShards + 1]; // AG: first output row of shard r
   int shard_rows[kMaxShards];          // AG: M_r
+  int m_pad;                    // small-M kernel: activation rows rounded up to 16
+                                // (the MMA's N); 0 for the main kernel
+  int stages;                   // small-M kernel: depth of the shared-memory ring
 };
+
+// ---------------------------------------------------------------- small M
+// The small-M kernel (M <= kSmallMaxM, AR/RS) swaps the operands: a tile is
+// kSmallTileN rows of W (output columns, the MMA's M) against all m_pad
+// activation rows (the MMA's N). Its shared memory, from a 1024-aligned base:
+// the W ring, the X ring, the staging area that receives the peer CTA's
+// partial for the output rows this CTA finishes, four per-warp transpose
+// buffers (32 x 32 bf16), the mbarriers and a few words. Host and device share
+// this layout.
+constexpr int kSmallTileN = 128;
+constexpr int kSmallMaxM = 256;
+constexpr int kGranule = 16;                 // output rows per exchange granule
+constexpr int kSmallMaxStages = 16;
+constexpr uint32_t kSmallSmemLimit = 232448; // 227 KB per CTA
+
+struct SmallLayout {
+  uint32_t w_bytes, x_bytes, stages;
+  uint32_t x_off, staging_off, transpose_off, bars_off, misc_off, total;  // total includes 1024 of alignment slack
+  uint32_t tmem_cols, acc_stride;
+};
+
+__host__ __device__ inline uint32_t small_owned_granules(int m_pad) {
+  return static_cast<uint32_t>((m_pad / kGranule + 1) / 2);
+}
+
+__host__ __device__ inline SmallLayout small_layout(int m_pad, int stages) {
+  SmallLayout L;
+  L.w_bytes = kSmallTileN * BK * 2;
+  L.x_bytes = static_cast<uint32_t>(m_pad) * BK * 2;
+  L.stages = static_cast<uint32_t>(stages);
+  L.x_off = L.stages * L.w_bytes;
+  L.staging_off = L.x_off + L.stages * L.x_bytes;
+  L.transpose_off = L.staging_off + small_owned_granules(m_pad) * kGranule * kSmallTileN * 4;
+  L.bars_off = L.transpose_off + 4 * 32 * 32 * 2;
+  L.misc_off = L.bars_off + (2 * L.stages + 7) * 8;
+  L.total = 1024 + L.misc_off + 16;
+  uint32_t cols = 32;
+  while (cols < 2u * static_cast<uint32_t>(m_pad)) cols *= 2;
+  L.tmem_cols = cols;
+  L.acc_stride = cols / 2;
+  return L;
+}
+
+// Deepest ring that fits the shared-memory limit for m_pad activation rows.
+__host__ __device__ inline int small_stages(int m_pad) {
+  int s = kSmallMaxStages;
+  while (s > 2 && small_layout(m_pad, s).total > kSmallSmemLimit) --s;
+  return s;
+}
 
 // Host-side launcher (defined with the kernel).
 // cta_group 1: one CTA per 128-row tile; 2: a CTA pair (cluster of two) per
@@ -86,5 +141,8 @@ cudaError_t launch_gemm(const Params& p, int block_n, int cta_group, int ctas, c
 // Sets shared-memory limits and reports how many CTA pairs can be resident.
 cudaError_t prepare_kernels(int device, int* pair_clusters);
 size_t kernel_smem_bytes(int block_n, int cta_group);
+// The small-M kernel (gsr_small.cu): `ctas` is even (clusters of two).
+cudaError_t launch_small(const Params& p, int ctas, cudaStream_t stream);
+cudaError_t prepare_small_kernel();
 
 }  // namespace gsr

@@ -203,14 +203,50 @@ def test_config_is_independent_of_mode(host):
             assert a == r
 
 
-def test_small_m_splits_tiles(host):
+def test_small_m_uses_the_k_pair_kernel(host):
+    # M <= 256 (AR/RS): the small-M kernel, 128-row tiles of W (block_n = 128)
+    # against all rows, each tile split over K between the two CTAs of a
+    # cluster: N = 7168 gives 56 tiles on 112 CTAs, whatever M up to 256.
+    for M in (1, 16, 127, 128, 129, 200, 256):
+        d = host.describe(B.MODE_AR, M, 7168, 0, [896] * 8)
+        assert (d["cta_group"], d["block_n"], d["schedule"], d["split"], d["tiles"], d["ctas"]) == \
+            (1, 128, 3, 2, 56, 112), M
+        # no split-K partials or counters: the workspace is the fixed minimum
+        assert d["workspace_bytes"] <= host.describe(B.MODE_AR, 4096, 7168, 0, [896] * 8)["workspace_bytes"]
+    # more tiles than clusters: one cluster per SM pair, tiles walked in turn
+    d = host.describe(B.MODE_AR, 64, 32768 - 128, 0, [896] * 8)
+    assert d["schedule"] == 3 and d["tiles"] == 255 and d["ctas"] == 148
+    # a capped grid keeps whole clusters
+    h = Host(host.lib)
+    B.gemm_shard_plan_set_option(h.plan, B.GSR_OPT_MAX_CTAS, 9)
+    assert h.describe(B.MODE_AR, 64, 7168, 0, [896] * 8)["ctas"] == 8
+    # above 256 rows, or with a single k-block, or in AG mode: the main kernel
+    assert host.describe(B.MODE_AR, 257, 7168, 0, [896] * 8)["schedule"] != 3
+    assert host.describe(B.MODE_AR, 64, 7168, 0, [64])["schedule"] != 3
+    assert host.describe(B.MODE_AR, 64, 7168, 0, [8])["schedule"] != 3
+    # two shards of one (ragged) k-block each: one per CTA of the pair
+    assert host.describe(B.MODE_AR, 64, 7168, 0, [8, 8])["schedule"] == 3
+    assert host.describe(B.MODE_AG, 0, 7168, 7168, [16] * 8)["schedule"] != 3
+    # a forced configuration option selects the main kernel unless small_m = 2
+    h = Host(host.lib)
+    B.gemm_shard_plan_set_option(h.plan, B.GSR_OPT_BLOCK_N, 256)
+    assert h.describe(B.MODE_AR, 128, 7168, 0, [896] * 8)["schedule"] != 3
+    B.gemm_shard_plan_set_option(h.plan, B.GSR_OPT_SMALL_M, 2)
+    assert h.describe(B.MODE_AR, 128, 7168, 0, [896] * 8)["schedule"] == 3
+    with pytest.raises(B.GsrError):
+        B.gemm_shard_plan_set_option(h.plan, B.GSR_OPT_SMALL_M, 3)
+
+
+def test_small_m_off_splits_tiles(lib):
+    h = Host(lib)
+    B.gemm_shard_plan_set_option(h.plan, B.GSR_OPT_SMALL_M, 1)
     # M = 128, one row tile: 56 single-CTA tiles of 128 x 128, each cut into
     # 148 // 56 = 2 pieces of 56 k-blocks: 112 CTAs
-    d = host.describe(B.MODE_AR, 128, 7168, 0, [896] * 8)
+    d = h.describe(B.MODE_AR, 128, 7168, 0, [896] * 8)
     assert (d["cta_group"], d["block_n"], d["schedule"], d["split"], d["tiles"], d["ctas"]) == \
         (1, 128, 1, 2, 56, 112)
     # M = 129: one 256-row pair tile keeps W read once: 28 pair tiles x 2 pieces
-    d = host.describe(B.MODE_AR, 129, 7168, 0, [896] * 8)
+    d = h.describe(B.MODE_AR, 129, 7168, 0, [896] * 8)
     assert (d["cta_group"], d["block_n"], d["schedule"], d["split"], d["tiles"], d["ctas"]) == \
         (2, 256, 1, 2, 28, 112)
     # stream-K on demand: every tile's 112 k-blocks shared out over all SMs
