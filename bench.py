@@ -59,8 +59,9 @@ def peaks():
 
 
 def kernel_source_hash() -> str:
+    """Hash of the sources the main kernel (the headline workload's) is built from."""
     h = hashlib.sha256()
-    for f in ("gsr_kernel.cu", "gsr_params.h"):
+    for f in ("gsr_kernel.cu", "gsr_device.cuh", "gsr_params.h"):
         with open(os.path.join(ROOT, "tensor_gemm_reduction_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -336,7 +337,8 @@ def sweep(plan, ws, dev, pk, names):
                      "hbm_gbs": round(w.bytes / t / 1e9, 1),
                      "roofline_frac": round(t_roof / t, 3),
                      "bound": "tensor" if w.flops / (pk["bf16_burst"] * 1e12) >= w.bytes / (pk["hbm_gbs"] * 1e9) else "hbm",
-                     "split": d["split"], "block_n": d["block_n"]})
+                     "split": d["split"], "block_n": d["block_n"],
+                     "kernel": "small_m" if d["schedule"] == 3 else "main"})
         del r
         torch.cuda.empty_cache()
     return rows
