@@ -15,6 +15,8 @@ Purpose):
 * ``rs_rows(M, R, s)``       (first row, row count) owned by shard s
 * ``ag(A_r, W)``             Y = concat_r(A_r) . W^T, fp64
 * ``ag_at(A_r, W, rows, cols)``     the same at listed points
+* ``pack_gather(S, rows_out)``  the packed gather of per-rank states (PR #51070
+  summary "Kimi K3 SP: pack the per-layer all-gathers into one"): rows_out x T*H
 * ``bf16_to_f64(bits)``      exact widening of one bf16 bit pattern
 
 Every function's pin (brute force, invariants, special cases) is in
@@ -69,8 +71,9 @@ def _load():
     lib.gsr_oracle_rs.argtypes = [i64, i64, i32, dp, dp, dp, dp]
     lib.gsr_oracle_ag.argtypes = [i64, i64, i32, dp, dp, dp, dp]
     lib.gsr_oracle_ag_at.argtypes = [i64, i64, i32, dp, dp, dp, i64, dp, dp, dp]
+    lib.gsr_oracle_pack_gather.argtypes = [i32, dp, i32, i64, dp, i64, dp]
     for f in ("gsr_oracle_ar", "gsr_oracle_ar_at", "gsr_oracle_rs_rows",
-              "gsr_oracle_rs", "gsr_oracle_ag", "gsr_oracle_ag_at"):
+              "gsr_oracle_rs", "gsr_oracle_ag", "gsr_oracle_ag_at", "gsr_oracle_pack_gather"):
         getattr(lib, f).restype = None
     _lib = lib
     return lib
@@ -198,3 +201,28 @@ def ag_at(A_r, W, rows, cols) -> np.ndarray:
                              rows.size, rows.ctypes.data, cols.ctypes.data,
                              out.ctypes.data)
     return out
+
+
+def pack_gather(S, rows_out: int) -> np.ndarray:
+    """S[r][t]: rank r's state t (M_r x H bf16 bits). Returns P (rows_out x T*H,
+    uint16): the ranks' states concatenated along the last dimension, stacked in
+    rank order and cut to rows_out rows."""
+    R = len(S)
+    if R == 0 or any(len(s) != len(S[0]) for s in S) or not S[0]:
+        raise ValueError("need R >= 1 ranks with the same T >= 1 states each")
+    T = len(S[0])
+    flat = [_bits(a) for s in S for a in s]
+    H = flat[0].shape[1]
+    M_r = []
+    for r in range(R):
+        shapes = {flat[r * T + t].shape for t in range(T)}
+        if len(shapes) != 1 or flat[r * T].ndim != 2 or flat[r * T].shape[1] != H:
+            raise ValueError("state shapes disagree")
+        M_r.append(flat[r * T].shape[0])
+    if not 0 <= rows_out <= sum(M_r):
+        raise ValueError("rows_out outside 0 .. sum of M_r")
+    P = np.empty((rows_out, T * H), dtype=np.uint16)
+    m = _i64(M_r)
+    _load().gsr_oracle_pack_gather(R, m.ctypes.data, T, H, _ptrs(flat), rows_out,
+                                   P.ctypes.data)
+    return P

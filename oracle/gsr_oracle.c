@@ -21,6 +21,13 @@
  *   AG  Each rank holds a row slice A_r (M_r x K) of the activation; the
  *       all-gather concatenates them and one GEMM with W (N x K) follows:
  *       Y = concat_r(A_r) . W^T. Shard r's rows start at sum_{q<r} M_q.
+ *   Packed gather (page "Kimi K3 SP: pack the per-layer all-gathers into one",
+ *       implementation steps 2-3 and its model.py snippet): rank r holds T
+ *       states of M_r rows x H columns (its hidden state, then its auxiliary
+ *       states in list order); it concatenates them along the last dimension
+ *       (M_r x T*H), one all-gather stacks the ranks' packed rows in rank
+ *       order, and the result keeps its first rows_out rows (the token count
+ *       before sequence-parallel padding). A copy: no arithmetic.
  *
  * Arithmetic: inputs are bf16 bit patterns; each is widened exactly to double
  * (bf16 is the upper half of an IEEE binary32). Every product and sum is done in
@@ -174,4 +181,29 @@ void gsr_oracle_ag_at(int64_t N, int64_t K, int R, const int64_t *M_r,
 #pragma omp parallel for schedule(dynamic, 64)
     for (int64_t i = 0; i < count; ++i)
         out[i] = gathered_element(K, R, M_r, A_r, W, rows[i], cols[i]);
+}
+
+/* Packed gather: P (rows_out x T*H, row-major) with output row g, for g in rank
+ * r's range offset_r <= g < offset_r + M_r (offset_r = sum_{q<r} M_q), equal to
+ * the concatenation [S[r][0][g - offset_r, :], ..., S[r][T-1][g - offset_r, :]].
+ * S holds R*T pointers, S[r*T + t] being rank r's state t (M_r x H, row-major).
+ * The caller guarantees rows_out <= sum_r M_r. Bit patterns are copied as they are. */
+void gsr_oracle_pack_gather(int R, const int64_t *M_r, int T, int64_t H,
+                            const uint16_t *const *S, int64_t rows_out, uint16_t *P)
+{
+    (void)R;
+    for (int64_t g = 0; g < rows_out; ++g) {
+        int r = 0;
+        int64_t offset = 0;
+        while (g >= offset + M_r[r]) {
+            offset += M_r[r];
+            ++r;
+        }
+        for (int t = 0; t < T; ++t) {
+            const uint16_t *src = S[r * T + t] + (g - offset) * H;
+            uint16_t *dst = P + g * (T * H) + t * H;
+            for (int64_t h = 0; h < H; ++h)
+                dst[h] = src[h];
+        }
+    }
 }

@@ -6,7 +6,10 @@ definitions (tests/golden/), exact brute force in Python integers, the bf16
 format and torch's own bf16 widening, invariants (sum of per-shard partials =
 full-K product; AG over shards = GEMM on the concatenation), special cases
 (R = 1 is a textbook GEMM, identity and one-hot weights, zero and negated
-inputs), and mutants of the oracle source that each pin must catch.
+inputs), and mutants of the oracle source that each pin must catch. The packed
+gather (a copy) is pinned by a hand-worked example, brute force in Python lists,
+the page's split-back symmetry checked with numpy.concatenate, and its special
+cases (T = 1 is a plain gather, R = 1 a plain concatenation).
 """
 import json
 import math
@@ -243,6 +246,70 @@ def test_point_queries_match_full(oracle_mod):
     assert np.array_equal(oracle_mod.ag_at(ag.A_r, ag.W, rows, cols), Ya[rows, cols])
 
 
+# ---------------------------------------------------------------- packed gather
+
+def _bits_of(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def py_pack(S, rows_out):
+    """The packed gather in plain Python lists (no oracle code): every rank's rows
+    in rank order, each row the concatenation of the rank's T states."""
+    rows = []
+    for states in S:
+        for i in range(len(states[0])):
+            rows.append([v for st in states for v in st[i]])
+    return rows[:rows_out]
+
+
+def _random_states(M_r, T, H, seed):
+    g = torch.Generator().manual_seed(seed)
+    return [[_bits_of(torch.randn(m, H, generator=g).to(torch.bfloat16)) for _ in range(T)]
+            for m in M_r]
+
+
+def test_pack_gather_hand_worked(oracle_mod):
+    gold = json.load(open(os.path.join(GOLDEN, "pack_gather.json")))
+    S = [[_bits_of(_bf16(st)) for st in rank] for rank in gold["S"]]
+    P = oracle_mod.pack_gather(S, gold["rows_out"])
+    assert np.array_equal(P, _bits_of(_bf16(gold["P"])))
+
+
+PACK_SHAPES = [([3, 0, 5, 2], 2, 8, 10), ([4, 4], 1, 16, 7), ([1], 4, 8, 1),
+               ([0, 6], 3, 8, 6), ([5, 5, 5], 2, 24, 11), ([2, 3], 5, 8, 5)]
+
+
+@pytest.mark.parametrize("M_r,T,H,rows_out", PACK_SHAPES)
+def test_pack_gather_bruteforce(oracle_mod, M_r, T, H, rows_out):
+    S = _random_states(M_r, T, H, seed=sum(M_r) + T + H)
+    P = oracle_mod.pack_gather(S, rows_out)
+    assert P.tolist() == py_pack([[s.tolist() for s in st] for st in S], rows_out)
+
+
+@pytest.mark.parametrize("M_r,T,H,rows_out", PACK_SHAPES)
+def test_pack_gather_splits_back_into_the_gathered_states(oracle_mod, M_r, T, H, rows_out):
+    """The page's symmetry: splitting the packed rows by H gives, for every state
+    t, the ranks' state-t rows concatenated in rank order and cut to rows_out."""
+    S = _random_states(M_r, T, H, seed=7 * T + H)
+    P = oracle_mod.pack_gather(S, rows_out)
+    for t in range(T):
+        gathered = np.concatenate([S[r][t] for r in range(len(M_r))], axis=0)[:rows_out]
+        assert np.array_equal(P[:, t * H:(t + 1) * H], gathered)
+
+
+def test_pack_gather_special_cases(oracle_mod):
+    S = _random_states([3, 2], 1, 8, seed=3)
+    # T = 1: a plain all-gather of the hidden state
+    assert np.array_equal(oracle_mod.pack_gather(S, 5), np.concatenate([S[0][0], S[1][0]]))
+    # R = 1: a plain concatenation along the last dimension
+    S1 = _random_states([4], 3, 8, seed=4)
+    assert np.array_equal(oracle_mod.pack_gather(S1, 4), np.concatenate(S1[0], axis=1))
+    # nothing kept
+    assert oracle_mod.pack_gather(S, 0).shape == (0, 8)
+    with pytest.raises(ValueError):
+        oracle_mod.pack_gather(S, 6)
+
+
 # ---------------------------------------------------------------- mutants
 
 # Plausible slips in the oracle source; each must make at least one pin fail.
@@ -256,6 +323,11 @@ MUTANTS = {
     "widen_shift": ("((uint32_t)bits) << 16", "((uint32_t)bits) << 15"),
     "ag_shard_order": ("const uint16_t *a = A_r[r] + (g - offset) * K;",
                        "const uint16_t *a = A_r[R - 1 - r] + (g - offset) * K;"),
+    "pack_state_order": ("const uint16_t *src = S[r * T + t] + (g - offset) * H;",
+                         "const uint16_t *src = S[r * T + (T - 1 - t)] + (g - offset) * H;"),
+    "pack_rank_order": ("const uint16_t *src = S[r * T + t] + (g - offset) * H;",
+                        "const uint16_t *src = S[(R - 1 - r) * T + t] + (g - offset) * H;"),
+    "pack_reversed_columns": ("dst[h] = src[h];", "dst[h] = src[H - 1 - h];"),
 }
 
 
@@ -273,6 +345,11 @@ def _pins_pass(oracle_mod) -> bool:
         # an AG case with equal shard sizes, so that a shard-order slip stays in bounds
         inp = gi.integer_ag([3, 3, 3], 5, 8, amp=3, seed=12)
         assert np.array_equal(oracle_mod.ag(inp.A_r, inp.W), py_ag(inp.A_r, inp.W))
+        # packed gather: the hand-worked case first (equal shard sizes, so that a
+        # rank-order slip stays in bounds), then the brute-force shapes
+        test_pack_gather_hand_worked(oracle_mod)
+        for M_r, T, H, rows_out in PACK_SHAPES:
+            test_pack_gather_bruteforce(oracle_mod, M_r, T, H, rows_out)
     except AssertionError:
         return False
     return True
@@ -294,7 +371,7 @@ def test_pins_catch_mutant(oracle_mod, tmp_path, monkeypatch, name):
     lib = ctypes.CDLL(str(so))
     for fname in ("gsr_oracle_bf16_to_f64", "gsr_oracle_threads", "gsr_oracle_ar",
                   "gsr_oracle_ar_at", "gsr_oracle_rs_rows", "gsr_oracle_rs",
-                  "gsr_oracle_ag", "gsr_oracle_ag_at"):
+                  "gsr_oracle_ag", "gsr_oracle_ag_at", "gsr_oracle_pack_gather"):
         f, g = getattr(real, fname), getattr(lib, fname)
         g.argtypes, g.restype = f.argtypes, f.restype
     assert _pins_pass(oracle_mod), "pins must pass on the real oracle"
