@@ -344,6 +344,29 @@ def sweep(plan, ws, dev, pk, names):
     return rows
 
 
+def sweep_pack(plan, ws, dev, pk):
+    """The packed gather of per-shard states (HBM-bound copy), timed like the
+    GEMM rows: median of 10 launches, an L2 flush before each."""
+    import torch
+    from tensor_gemm_reduction_gb300 import binding as B
+    from tensor_gemm_reduction_gb300 import inputs as gi
+    w = gi.PACK_SP
+    flush_buf = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    S = gi.gaussian_states([w.M_r] * w.R, w.T, w.H, seed=w.seed, device=dev)
+    P = torch.empty(w.rows_out, w.T * w.H, dtype=torch.bfloat16, device=dev)
+    call = B.prepare_pack_gather(plan, S, w.rows_out, P, ws)
+    times, _ = time_launches(call, steps=10, warmup=3, flush=lambda: flush_buf.fill_(1))
+    B.gemm_shard_check_status(plan, ws)
+    t = statistics.median(times) * 1e-3
+    row = {"workload": w.name, "mode": "pack", "R": w.R, "M_r": w.M_r, "T": w.T, "H": w.H,
+           "rows_out": w.rows_out, "us": round(t * 1e6, 2), "hbm_gbs": round(w.bytes / t / 1e9, 1),
+           "roofline_frac": round(w.bytes / (pk["hbm_gbs"] * 1e9) / t, 3), "bound": "hbm",
+           "kernel": "pack"}
+    del S, P, flush_buf
+    torch.cuda.empty_cache()
+    return row
+
+
 def run_context_mm(args, w):
     """torch.mm (a library GEMM, cuBLAS) on contiguous operands of the same
     shapes: the fused path's context row, not its target. One JSON line per
@@ -482,6 +505,8 @@ def main():
         torch.cuda.empty_cache()
         names = [s for s in args.sweep_only.split(",") if s]
         result["per_config"] = sweep(plan, ws, dev, pk, names)
+        if not names or "pack_sp_t4" in names:
+            result["per_config"].append(sweep_pack(plan, ws, dev, pk))
     if rank == 0:
         print(json.dumps(result), flush=True)
     if world > 1:

@@ -290,6 +290,40 @@ gsr_status gemm_ar_noalloc(const gemm_shard_plan *plan, int64_t M, int64_t N, in
                            const void *const *W_r, void *Y, gsr_stream_t stream);
 
 /*
+ * Packed gather of per-shard states (the pages' "Kimi K3 SP: pack the per-layer
+ * all-gathers into one", PR #51070 summary, implementation steps 2-3 and its
+ * model.py snippet: each rank concatenates its hidden state and auxiliary
+ * states along the last dimension, one all-gather stacks the ranks' packed
+ * rows, and the result keeps the first full_num_tokens rows; splitting it by
+ * the hidden size gives the gathered states back). Here the ranks are R sets of
+ * buffers on this GPU and the whole thing is one pass of copies:
+ *     P[g, t*H : (t+1)*H] = S[r*T + t][g - row_begin_r, :]      for g < rows_out,
+ * where row_begin_r = M_0 + ... + M_{r-1} and g lies in [row_begin_r,
+ * row_begin_r + M_r). Bits are copied unchanged (bf16 in, bf16 out).
+ *   R         shards, 1..the plan's max_R
+ *   M_r       host array of R row counts (>= 0; the sequence-parallel shards)
+ *   T         states per shard, 1..16 (the hidden state, then the aux states)
+ *   H         columns of every state (the hidden size), a positive multiple of 8
+ *   S         host array of R*T device pointers, S[r*T + t] = shard r's state t,
+ *             M_r x H row-major bf16, 16-byte aligned; read in place. A shard
+ *             with no kept row (all of its rows at or past rows_out) is not
+ *             read and its pointers may be NULL.
+ *   rows_out  rows kept (full_num_tokens), 0..sum of M_r
+ *   P         device output, rows_out x (T*H) row-major bf16, 16-byte aligned,
+ *             caller-owned; every element is written, nothing else is. The
+ *             split-back state t is the strided view P[:, t*H : (t+1)*H].
+ *   ws        the plan's workspace (only its status word is used; a bounded
+ *             wait that runs out is reported by gemm_shard_check_status)
+ * Errors: GSR_ERR_INVALID_VALUE for the shapes and pointers above,
+ * GSR_ERR_WORKSPACE for a NULL, misaligned or too small workspace,
+ * GSR_ERR_UNSUPPORTED on a host plan (after validation), GSR_ERR_CUDA when the
+ * launch fails. rows_out == 0 returns GSR_OK with no launch. Stream-ordered.
+ */
+gsr_status gemm_shard_pack_gather(const gemm_shard_plan *plan, int R, const int64_t *M_r, int T,
+                                  int64_t H, const void *const *S, int64_t rows_out, void *P,
+                                  void *ws, size_t ws_bytes, gsr_stream_t stream);
+
+/*
  * Synchronise `stream`, read the workspace status word, clear it and return
  * GSR_OK or GSR_ERR_TIMEOUT (the code of the first wait that ran out is
  * available through gsr_last_error_string). After a timeout, re-run

@@ -51,6 +51,7 @@ EXPORTED = (
     "gemm_shard_workspace_size", "gemm_shard_workspace_init", "gemm_ar", "gemm_rs",
     "gemm_ag", "gemm_shard_check_status", "gsr_last_error_string", "gemm_shard_describe",
     "gemm_ar_noalloc", "gemm_ag_flagged", "gemm_shard_signal", "gemm_ar_replicated",
+    "gemm_shard_pack_gather",
 )
 
 
@@ -104,6 +105,7 @@ def load_library() -> ctypes.CDLL:
     lib.gemm_ag_flagged.argtypes = [vp, i64, i64, i32, i64_arr, ptr_arr, vp, vp, vp,
                                     ctypes.c_uint32, vp, sz, vp]
     lib.gemm_shard_signal.argtypes = [vp, vp, ctypes.c_uint32, vp]
+    lib.gemm_shard_pack_gather.argtypes = [vp, i32, i64_arr, i32, i64, ptr_arr, i64, vp, vp, sz, vp]
     lib.gemm_shard_check_status.argtypes = [vp, vp, vp]
     lib.gsr_last_error_string.restype = ctypes.c_char_p
     lib.gemm_shard_describe.argtypes = [vp, i32, i64, i64, i64, i32, i64_arr,
@@ -434,3 +436,46 @@ def gemm_shard_describe(plan: Plan, mode: int, M: int, N: int, K: int,
     _check(lib.gemm_shard_describe(plan.handle, int(mode), int(M), int(N), int(K), len(sizes), s,
                                    ctypes.byref(cfg)))
     return {name: getattr(cfg, name) for name, _ in GsrConfig._fields_}
+
+
+def _pack_args(plan, S, rows_out, P, ws):
+    R = len(S)
+    if R == 0 or any(len(s) != len(S[0]) for s in S) or not S[0]:
+        raise ValueError("S must hold R >= 1 shards with the same T >= 1 states each")
+    T = len(S[0])
+    _bf16_2d(P, "P")
+    H = P.shape[1] // T
+    if P.shape != (rows_out, T * H) or H * T != P.shape[1]:
+        raise ValueError(f"P must be rows_out x (T*H) = {rows_out} x {T}*H")
+    M_r, flat = [], []
+    for r, states in enumerate(S):
+        m = states[0].shape[0]
+        for t, st in enumerate(states):
+            if st.numel() == 0 and m == 0:
+                flat.append(None)
+                continue
+            _bf16_2d(st, f"S[{r}][{t}]")
+            if st.shape != (m, H):
+                raise ValueError(f"S[{r}][{t}] must be {m} x {H}")
+            flat.append(st)
+        M_r.append(m)
+    m, ma = _i64s(M_r)
+    sp, sa = _ptrs(flat)
+    wsp, wsn = _ws(ws)
+    args = (plan.handle, R, m, T, H, sp, rows_out, ctypes.c_void_p(P.data_ptr()), wsp, wsn)
+    return args, (ma, sa, S, P, ws)
+
+
+def gemm_shard_pack_gather(plan: Plan, S: Sequence[Sequence[torch.Tensor]], rows_out: int,
+                           P: torch.Tensor, ws: torch.Tensor, stream=None) -> torch.Tensor:
+    """P[g, t*H:(t+1)*H] = cat_r(S[r][t])[g] for g < rows_out (S[r][t]: M_r x H, bf16;
+    P: rows_out x T*H). Returns P; the state-t view is P[:, t*H:(t+1)*H]."""
+    args, keep = _pack_args(plan, S, rows_out, P, ws)
+    _check(load_library().gemm_shard_pack_gather(*args, _stream(stream)))
+    return P
+
+
+def prepare_pack_gather(plan: Plan, S, rows_out, P, ws, stream=None) -> PreparedCall:
+    """gemm_shard_pack_gather on fixed buffers, validated and marshalled once."""
+    args, keep = _pack_args(plan, S, rows_out, P, ws)
+    return PreparedCall(load_library().gemm_shard_pack_gather, args, keep, stream)

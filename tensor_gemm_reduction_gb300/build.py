@@ -22,7 +22,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUT_DIR, "libgsr.so")
-SOURCES = ["gsr_kernel.cu", "gsr_small.cu", "gsr_api.cu"]
+SOURCES = ["gsr_kernel.cu", "gsr_small.cu", "gsr_pack.cu", "gsr_api.cu"]
 HEADERS = [os.path.join(CSRC, "gsr_params.h"), os.path.join(CSRC, "gsr_device.cuh"),
            os.path.join(INCLUDE, "gsr.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -553,6 +553,7 @@ gsr_status gemm_shard_plan_create(gemm_shard_plan** out, int device, int64_t max
                   static_cast<size_t>(prop.sharedMemPerBlockOptin), need);
     e = gsr::prepare_kernels(device, &pair_clusters);
     if (e == cudaSuccess) e = gsr::prepare_small_kernel();
+    if (e == cudaSuccess) e = gsr::prepare_pack_kernel();
     if (e != cudaSuccess) return cuda_fail(e, "configuring the kernels");
   }
   *out = new_plan(device, prop.multiProcessorCount, max_M, max_N, max_K, max_R);
@@ -768,6 +769,73 @@ gsr_status gemm_shard_signal(const gemm_shard_plan* P, uint32_t* flag, uint32_t 
   // memory fence, so data written by earlier work on the stream is visible first.
   CUresult r = fn(reinterpret_cast<CUstream>(stream), reinterpret_cast<CUdeviceptr>(flag), value, 0);
   if (r != CUDA_SUCCESS) return fail(GSR_ERR_CUDA, "cuStreamWriteValue32 failed (%d)", (int)r);
+  return ok();
+}
+
+gsr_status gemm_shard_pack_gather(const gemm_shard_plan* P, int R, const int64_t* M_r, int T,
+                                  int64_t H, const void* const* S, int64_t rows_out, void* Pout,
+                                  void* ws, size_t ws_bytes, gsr_stream_t stream) {
+  gsr_status s = check_plan(P);
+  if (s) return s;
+  if (R < 1 || R > P->max_R) return fail(GSR_ERR_INVALID_VALUE, "R=%d outside 1..%d", R, P->max_R);
+  if (T < 1 || T > gsr::kMaxPackStates)
+    return fail(GSR_ERR_INVALID_VALUE, "T=%d outside 1..%d", T, gsr::kMaxPackStates);
+  if (H < 8 || H % 8)
+    return fail(GSR_ERR_INVALID_VALUE, "H must be a positive multiple of 8 (got %lld)", (long long)H);
+  if (!M_r || !S) return fail(GSR_ERR_INVALID_VALUE, "M_r and S must not be NULL");
+  int64_t total = 0;
+  for (int r = 0; r < R; ++r) {
+    if (M_r[r] < 0) return fail(GSR_ERR_INVALID_VALUE, "M_r[%d] must be >= 0", r);
+    total += M_r[r];
+  }
+  if (rows_out < 0 || rows_out > total)
+    return fail(GSR_ERR_INVALID_VALUE, "rows_out=%lld outside 0..%lld (the sum of M_r)",
+                (long long)rows_out, (long long)total);
+  // States of shards that hold a kept row must be valid; the rest are not read.
+  int64_t begin = 0;
+  for (int r = 0; r < R; ++r) {
+    if (begin < rows_out && M_r[r] > 0) {
+      for (int t = 0; t < T; ++t)
+        if (!S[r * T + t] || !aligned16(S[r * T + t]))
+          return fail(GSR_ERR_INVALID_VALUE, "S[%d] (shard %d, state %d) must be non-NULL and 16-byte aligned",
+                      r * T + t, r, t);
+    }
+    begin += M_r[r];
+  }
+  if (rows_out > 0 && (!Pout || !aligned16(Pout)))
+    return fail(GSR_ERR_INVALID_VALUE, "P must be non-NULL and 16-byte aligned");
+  if (!ws) return fail(GSR_ERR_WORKSPACE, "workspace is NULL");
+  if (reinterpret_cast<uintptr_t>(ws) & 255u)
+    return fail(GSR_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  if (ws_bytes < gsr::kWsHeader)
+    return fail(GSR_ERR_WORKSPACE, "workspace too small: %zu bytes given, %zu needed", ws_bytes,
+                gsr::kWsHeader);
+  if (rows_out == 0) return ok();
+  if (P->device < 0) return fail(GSR_ERR_UNSUPPORTED, "host plan: arguments are valid, nothing launched");
+
+  gsr::PackParams p;
+  std::memset(&p, 0, sizeof p);
+  int64_t row = 0;
+  for (int r = 0; r < R; ++r) {
+    p.row_begin[r] = row;
+    row += M_r[r];
+    for (int t = 0; t < T; ++t) p.src[r * T + t] = static_cast<const uint16_t*>(S[r * T + t]);
+  }
+  for (int r = R; r <= kMaxShards; ++r) p.row_begin[r] = row;
+  p.dst = static_cast<uint16_t*>(Pout);
+  p.status = static_cast<uint32_t*>(ws);
+  p.timeout_ns = P->timeout_ns;
+  p.rows_out = rows_out;
+  p.seg_bytes = H * 2;
+  p.R = R;
+  p.T = T;
+  p.pieces_per_seg = static_cast<int>(cdiv(p.seg_bytes, gsr::kPackPieceMax));
+  const int64_t pieces = rows_out * T * p.pieces_per_seg;
+  const int ctas = static_cast<int>(std::min<int64_t>(P->sm_count, pieces));
+  DeviceScope scope(P->device);
+  if (scope.err != cudaSuccess) return cuda_fail(scope.err, "selecting the plan's device");
+  cudaError_t e = gsr::launch_pack(p, ctas, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
   return ok();
 }
 

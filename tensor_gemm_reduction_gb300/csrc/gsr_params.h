@@ -134,6 +134,24 @@ __host__ __device__ inline int small_stages(int m_pad) {
   return s;
 }
 
+// ---------------------------------------------------------------- packed gather
+// P[g, t*H .. (t+1)*H) = S[r][t][g - row_begin[r], :] for output rows g <
+// rows_out, g in shard r's rows [row_begin[r], row_begin[r+1]).
+constexpr int kMaxPackStates = 16;
+constexpr int64_t kPackPieceMax = 16384;     // bytes per bulk copy
+
+struct PackParams {
+  const uint16_t* src[kMaxShards * kMaxPackStates];  // src[r*T + t]: M_r x H, row-major
+  int64_t row_begin[kMaxShards + 1];                  // entries past R: the sum of M_r
+  uint16_t* dst;                                      // rows_out x T*H, row-major
+  uint32_t* status;                                   // workspace status word
+  uint64_t timeout_ns;
+  int64_t rows_out;
+  int64_t seg_bytes;                                  // H * 2: one state row
+  int R, T;
+  int pieces_per_seg;                                 // ceil(seg_bytes / kPackPieceMax)
+};
+
 // Host-side launcher (defined with the kernel).
 // cta_group 1: one CTA per 128-row tile; 2: a CTA pair (cluster of two) per
 // 256-row tile. block_n is 128 or 256. `ctas` counts CTAs (even for pairs).
@@ -144,5 +162,8 @@ size_t kernel_smem_bytes(int block_n, int cta_group);
 // The small-M kernel (gsr_small.cu): `ctas` is even (clusters of two).
 cudaError_t launch_small(const Params& p, int ctas, cudaStream_t stream);
 cudaError_t prepare_small_kernel();
+// The packed gather (gsr_pack.cu): one warp per CTA.
+cudaError_t launch_pack(const PackParams& p, int ctas, cudaStream_t stream);
+cudaError_t prepare_pack_kernel();
 
 }  // namespace gsr

@@ -155,6 +155,38 @@ def integer_ag(M_r: Sequence[int], N: int, K: int, amp: int = 3, seed: int = 1,
     return AGInputs(N, K, M_r, _split_rows(A, M_r), W)
 
 
+def gaussian_states(M_r: Sequence[int], T: int, H: int, seed: int = 1,
+                    device: str | torch.device = "cpu") -> List[List[torch.Tensor]]:
+    """T states per shard (the hidden state and T-1 auxiliary states of the
+    packed gather), N(0,1) in bf16: S[r][t] is M_r x H, each its own allocation."""
+    g = _gen(seed, device)
+    return [[torch.randn(int(m), H, generator=g, device=device).to(torch.bfloat16)
+             for _ in range(T)] for m in M_r]
+
+
+@dataclass(frozen=True)
+class PackWorkload:
+    """A packed gather: R shards of M_r rows, T states of H columns, the first
+    rows_out rows kept (the token count before sequence-parallel padding)."""
+    name: str
+    R: int
+    M_r: int
+    T: int
+    H: int
+    rows_out: int
+    seed: int = 7
+
+    @property
+    def bytes(self) -> int:
+        """Algorithmic bytes: every kept state row read once, P written once."""
+        return 2 * (2 * self.rows_out * self.T * self.H)
+
+
+# Kimi-K3-like: hidden size 7168, the hidden state and three auxiliary states,
+# 8 sequence-parallel shards of 4096 rows, 5 padding rows dropped.
+PACK_SP = PackWorkload("pack_sp_t4", R=8, M_r=4096, T=4, H=7168, rows_out=8 * 4096 - 5)
+
+
 def bf16_bits(t: torch.Tensor):
     """The raw bf16 bit patterns of a CPU tensor as a numpy uint16 array."""
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view("uint16")

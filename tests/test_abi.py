@@ -349,3 +349,48 @@ def test_flagged_ag_and_signal_validation(host):
     assert lib.gemm_ag_flagged(*args(0x30000000)) == B.GSR_ERR_UNSUPPORTED   # host plan: valid
     assert lib.gemm_shard_signal(host.plan.handle, ctypes.c_void_p(0), 1, None) == B.GSR_ERR_INVALID_VALUE
     assert lib.gemm_shard_signal(host.plan.handle, ctypes.c_void_p(0x30000000), 1, None) == B.GSR_ERR_UNSUPPORTED
+
+
+def _pack(lib, plan, M_r, T, H, rows_out, S=None, P=0x40000, ws=0x20000000, ws_bytes=4096):
+    R = len(M_r)
+    S = S if S is not None else [0x100000 * (i + 1) for i in range(R * T)]
+    return lib.gemm_shard_pack_gather(plan.handle, R, _arr(ctypes.c_int64, M_r), T, H,
+                                      _arr(ctypes.c_void_p, S), rows_out, ctypes.c_void_p(P),
+                                      ctypes.c_void_p(ws), ws_bytes, None)
+
+
+def test_pack_gather_validation(host):
+    lib, plan = host.lib, host.plan
+    # valid calls reach the launch point; nothing kept returns OK with no launch
+    assert _pack(lib, plan, [4096] * 8, 4, 7168, 32765) == B.GSR_ERR_UNSUPPORTED
+    assert "arguments are valid" in B.gsr_last_error_string()
+    assert _pack(lib, plan, [3, 0, 5], 2, 8, 0) == B.GSR_OK
+    # a shard with no kept row may have NULL states; a kept one may not
+    S = [0x100000, 0x200000, 0, 0]
+    assert _pack(lib, plan, [4, 4], 2, 8, 4, S=S) == B.GSR_ERR_UNSUPPORTED
+    assert _pack(lib, plan, [4, 4], 2, 8, 5, S=S) == B.GSR_ERR_INVALID_VALUE
+    assert "S[2]" in B.gsr_last_error_string()
+    # an empty shard may have NULL states even before rows_out
+    assert _pack(lib, plan, [4, 0, 4], 1, 8, 8, S=[0x100000, 0, 0x300000]) == B.GSR_ERR_UNSUPPORTED
+    bad = [
+        (dict(M_r=[4] * 17, T=1, H=8, rows_out=4), "R="),
+        (dict(M_r=[4], T=0, H=8, rows_out=4), "T="),
+        (dict(M_r=[4], T=17, H=8, rows_out=4), "T="),
+        (dict(M_r=[4], T=1, H=12, rows_out=4), "multiple of 8"),
+        (dict(M_r=[4], T=1, H=0, rows_out=4), "multiple of 8"),
+        (dict(M_r=[4, -1], T=1, H=8, rows_out=3), "M_r[1]"),
+        (dict(M_r=[4, 4], T=1, H=8, rows_out=9), "rows_out"),
+        (dict(M_r=[4], T=1, H=8, rows_out=-1), "rows_out"),
+        (dict(M_r=[4], T=1, H=8, rows_out=4, P=0x40008), "P must"),
+        (dict(M_r=[4], T=1, H=8, rows_out=4, P=0), "P must"),
+        (dict(M_r=[4], T=1, H=8, rows_out=4, S=[0x100008]), "16-byte"),
+    ]
+    for kw, frag in bad:
+        assert _pack(lib, plan, **kw) == B.GSR_ERR_INVALID_VALUE, kw
+        assert frag in B.gsr_last_error_string(), (kw, B.gsr_last_error_string())
+    assert _pack(lib, plan, [4], 1, 8, 4, ws=0) == B.GSR_ERR_WORKSPACE
+    assert _pack(lib, plan, [4], 1, 8, 4, ws=0x20000010) == B.GSR_ERR_WORKSPACE
+    assert _pack(lib, plan, [4], 1, 8, 4, ws_bytes=128) == B.GSR_ERR_WORKSPACE
+    assert lib.gemm_shard_pack_gather(None, 1, _arr(ctypes.c_int64, [4]), 1, 8,
+                                      _arr(ctypes.c_void_p, [0x100000]), 4, ctypes.c_void_p(0x40000),
+                                      ctypes.c_void_p(0x20000000), 4096, None) == B.GSR_ERR_INVALID_VALUE
