@@ -289,7 +289,11 @@ Config choose_config(const gemm_shard_plan* P, int mode, int64_t M, int64_t N, i
         dp = full * workers;                          // only the partial last wave
     }
     int64_t sk_iters = (c.tiles - dp) * c.kb_total;
-    if (sk_iters > 0 && sk_iters < 4 * workers) {   // too little to share out
+    // Too little to share out, or too much for the kernel's 32-bit stream-K
+    // arithmetic ((sk_iters + 1) * (workers + 1) must stay below 2^32): whole
+    // tiles only.
+    if ((sk_iters > 0 && sk_iters < 4 * workers) ||
+        (sk_iters + 1) * (workers + 1) >= (int64_t(1) << 32)) {
       dp = c.tiles;
       sk_iters = 0;
     }

@@ -61,9 +61,12 @@ struct Unit {
   int kb_end;
 };
 
-// Position of the tile in the output (raster order) and its shard.
+// Position of the tile in the output (raster order) and its shard. Called by
+// whole warps: `mt_begins` holds shard_mt_begin[lane] in each lane (AG), read
+// with shuffles rather than dynamically indexed kernel-parameter loads, which
+// are slow on the set-up path of every unit.
 template <int BN, int CG>
-__device__ __forceinline__ void place_tile(const Params& p, Unit& t, uint32_t rank) {
+__device__ __forceinline__ void place_tile(const Params& p, Unit& t, uint32_t rank, int mt_begins) {
   // Raster: groups of group_m m-tiles; inside a group the m index runs fastest,
   // so CTAs working at the same time share W (B) panels and A rows in L2.
   const int span = p.group_m * p.n_tiles;
@@ -84,9 +87,9 @@ __device__ __forceinline__ void place_tile(const Params& p, Unit& t, uint32_t ra
       t.m0 = 0;
     } else {
       int r = 0;
-      while (r + 1 < p.R && p.shard_mt_begin[r + 1] <= h) ++r;
+      while (r + 1 < p.R && __shfl_sync(0xffffffffu, mt_begins, r + 1) <= h) ++r;
       t.shard = r;
-      t.m0 = (h - p.shard_mt_begin[r]) * BM;
+      t.m0 = (h - __shfl_sync(0xffffffffu, mt_begins, r)) * BM;
     }
   } else {
     t.shard = 0;
@@ -95,12 +98,15 @@ __device__ __forceinline__ void place_tile(const Params& p, Unit& t, uint32_t ra
 }
 
 // Per-worker walk over the schedule; every role of a CTA walks it identically.
+// Stream-K positions are 32-bit: the host keeps (sk_iters + 1) * (G + 1) below
+// 2^32 (64-bit divisions cost about a microsecond on the set-up path).
 struct Sched {
   int w;              // this worker (CTA, or CTA pair)
   int G;              // workers
   int next;           // uniform: next unit; stream-K: next whole tile
-  long long it;       // stream-K: next k-block of this worker's range
-  long long it_end;
+  uint32_t it;        // stream-K: next k-block of this worker's range
+  uint32_t it_end;
+  int mt_begins;      // AG: shard_mt_begin[lane] (lanes 0..kMaxShards)
 };
 
 template <int CG>
@@ -109,14 +115,17 @@ __device__ __forceinline__ Sched sched_begin(const Params& p) {
   s.w = static_cast<int>(blockIdx.x) / CG;
   s.G = static_cast<int>(gridDim.x) / CG;
   s.next = s.w;
-  s.it = (static_cast<long long>(s.w) * p.sk_iters) / s.G;
-  s.it_end = (static_cast<long long>(s.w + 1) * p.sk_iters) / s.G;
+  const uint32_t I = static_cast<uint32_t>(p.sk_iters), G = static_cast<uint32_t>(s.G);
+  s.it = static_cast<uint32_t>(s.w) * I / G;
+  s.it_end = static_cast<uint32_t>(s.w + 1) * I / G;
+  const int lane = static_cast<int>(threadIdx.x) & 31;
+  s.mt_begins = p.shard_mt_begin[lane <= kMaxShards ? lane : kMaxShards];
   return s;
 }
 
 // The worker whose stream-K range holds k-block `it` (ranges are
 // [w*I/G, (w+1)*I/G), every one non-empty because I >= G).
-__device__ __forceinline__ int sk_worker_of(long long it, long long I, int G) {
+__device__ __forceinline__ int sk_worker_of(uint32_t it, uint32_t I, uint32_t G) {
   return static_cast<int>(((it + 1) * G + I - 1) / I) - 1;
 }
 
@@ -130,9 +139,9 @@ __device__ __forceinline__ bool sched_next(const Params& p, Sched& s, Unit& t, u
     t.piece = u - t.tile * p.splits;
     t.npieces = p.splits;
     t.slot0 = t.tile * p.splits;
-    t.kb_begin = static_cast<int>((static_cast<long long>(t.piece) * p.kb_total) / p.splits);
-    t.kb_end = static_cast<int>((static_cast<long long>(t.piece + 1) * p.kb_total) / p.splits);
-    place_tile<BN, CG>(p, t, rank);
+    t.kb_begin = t.piece * p.kb_total / p.splits;
+    t.kb_end = (t.piece + 1) * p.kb_total / p.splits;
+    place_tile<BN, CG>(p, t, rank, s.mt_begins);
     return true;
   }
   // By default the stream-K range comes first: the pieces that need summing
@@ -147,26 +156,27 @@ __device__ __forceinline__ bool sched_next(const Params& p, Sched& s, Unit& t, u
     t.slot0 = 0;
     t.kb_begin = 0;
     t.kb_end = p.kb_total;
-    place_tile<BN, CG>(p, t, rank);
+    place_tile<BN, CG>(p, t, rank, s.mt_begins);
     return true;
   }
   // the next piece of this worker's stream-K range
-  const long long kt = p.kb_total;
-  const int sk_tile = static_cast<int>(s.it / kt);
-  const int k_lo = static_cast<int>(s.it - sk_tile * kt);
-  const int k_hi = static_cast<int>(min(kt, k_lo + (s.it_end - s.it)));
+  const uint32_t kt = static_cast<uint32_t>(p.kb_total);
+  const uint32_t I = static_cast<uint32_t>(p.sk_iters), G = static_cast<uint32_t>(s.G);
+  const uint32_t sk_tile = s.it / kt;
+  const uint32_t k_lo = s.it - sk_tile * kt;
+  const uint32_t k_hi = min(kt, k_lo + (s.it_end - s.it));
   s.it += k_hi - k_lo;
-  const int first_w = sk_worker_of(sk_tile * kt, p.sk_iters, s.G);
-  const int last_w = sk_worker_of((sk_tile + 1) * kt - 1, p.sk_iters, s.G);
-  t.tile = p.dp_tiles + sk_tile;
+  const int first_w = sk_worker_of(sk_tile * kt, I, G);
+  const int last_w = sk_worker_of((sk_tile + 1) * kt - 1, I, G);
+  t.tile = p.dp_tiles + static_cast<int>(sk_tile);
   t.piece = s.w - first_w;
   t.npieces = last_w - first_w + 1;
   // Along the stream-K range each new piece starts a new tile, a new worker's
   // range, or both, so (tile + worker) numbers the pieces without collisions.
-  t.slot0 = sk_tile + first_w;
-  t.kb_begin = k_lo;
-  t.kb_end = k_hi;
-  place_tile<BN, CG>(p, t, rank);
+  t.slot0 = static_cast<int>(sk_tile) + first_w;
+  t.kb_begin = static_cast<int>(k_lo);
+  t.kb_end = static_cast<int>(k_hi);
+  place_tile<BN, CG>(p, t, rank, s.mt_begins);
   return true;
 }
 
@@ -199,16 +209,21 @@ __device__ void run_producer(const Params& p, uint32_t tiles_base, uint32_t bars
                              const Ctl& ctl) {
   using L = Layout<BN, STAGES, CG>;
   const uint32_t full0 = bars, empty0 = bars + 8 * STAGES;
-  if (p.mode == kModeAG) {
-    for (int r = 0; r < p.R; ++r)
-      if (p.shard_rows[r] > 0) prefetch_tensormap(&p.tmap_a[r]);
-    prefetch_tensormap(&p.tmap_b[0]);
-  } else {
-    for (int r = 0; r < p.R; ++r) {
-      prefetch_tensormap(&p.tmap_a[r]);
-      prefetch_tensormap(&p.tmap_b[r]);
+  // The descriptors of the other shards are prefetched once the first k-block
+  // is on its way (the first copies fetch their own): the first loads leave
+  // about a microsecond earlier.
+  auto prefetch_descriptors = [&]() {
+    if (p.mode == kModeAG) {
+      for (int r = 0; r < p.R; ++r)   // empty shards have no descriptor
+        if (p.shard_rows[r] > 0) prefetch_tensormap(&p.tmap_a[r]);
+      prefetch_tensormap(&p.tmap_b[0]);
+    } else {
+      for (int r = 0; r < p.R; ++r) {
+        prefetch_tensormap(&p.tmap_a[r]);
+        prefetch_tensormap(&p.tmap_b[r]);
+      }
     }
-  }
+  };
   const uint64_t pol_a = make_l2_policy(p.policy_a);
   const uint64_t pol_b = make_l2_policy(p.policy_b);
   uint32_t issued = 0;
@@ -273,7 +288,7 @@ __device__ void run_producer(const Params& p, uint32_t tiles_base, uint32_t bars
         tma_load_2d_pair(sa, ma, lead_full, kx, a_row, pol_a);
         tma_load_2d_pair(sb, mb, lead_full, kx, b_row, pol_b);
       }
-      ++issued;
+      if (++issued == 1) prefetch_descriptors();
       if (++slot == STAGES) {
         slot = 0;
         slot_parity ^= 1u;
