@@ -394,3 +394,15 @@ def test_pack_gather_validation(host):
     assert lib.gemm_shard_pack_gather(None, 1, _arr(ctypes.c_int64, [4]), 1, 8,
                                       _arr(ctypes.c_void_p, [0x100000]), 4, ctypes.c_void_p(0x40000),
                                       ctypes.c_void_p(0x20000000), 4096, None) == B.GSR_ERR_INVALID_VALUE
+
+
+def test_stream_k_range_stays_in_32_bit(lib):
+    """The kernel walks the stream-K range in 32-bit arithmetic: a range with
+    (sk_iters + 1) * (workers + 1) >= 2^32 runs as whole tiles instead."""
+    K = (1 << 31) - 128
+    h = Host(lib, max_M=32768, max_N=8192, max_K=K, max_R=1)
+    d = h.describe(B.MODE_AR, 32768, 7168, 0, [K])
+    assert d["cta_group"] == 2 and d["sk_iters"] == 0 and d["dp_tiles"] == d["tiles"]
+    # an ordinary K keeps its stream-K tail
+    d = h.describe(B.MODE_AR, 32768, 7168, 0, [7168])
+    assert d["sk_iters"] == 32 * 112 and (d["sk_iters"] + 1) * (74 + 1) < 2 ** 32
