@@ -314,8 +314,12 @@ __device__ void run_mma(const Params& p, uint32_t tiles_base, uint32_t bars, uin
   uint32_t stage = 0, phase = 0, local = 0;   // next ring slot and its fill phase
   bool ok = true, issued_any = false;
   Sched sch = sched_begin<CG>(p);
-  Unit t;
-  for (; ok && sched_next<BN, CG>(p, sch, t, rank); ++local) {
+  // The next unit is placed while the current one's first k-block runs on the
+  // tensor pipe, so the walk's arithmetic stays off the gap between units.
+  Unit t, tn;
+  bool have = sched_next<BN, CG>(p, sch, t, rank);
+  for (; ok && have; ++local) {
+    bool have_next = false, looked_ahead = false;
     const uint32_t acc = local & 1u;
     const uint32_t acc_parity = ((local >> 1) & 1u) ^ 1u;
     const bool free_acc = wait_bounded(tempty0 + 8 * acc, acc_parity, ctl, (kRoleMma << 8) | 1);
@@ -364,12 +368,19 @@ __device__ void run_mma(const Params& p, uint32_t tiles_base, uint32_t bars, uin
         mma_commit(empty0 + 8 * cur);
       else
         mma_commit_pair(empty0 + 8 * cur, 0x3);     // frees the slot in both CTAs
+      if (!looked_ahead) {
+        have_next = sched_next<BN, CG>(p, sch, tn, rank);
+        looked_ahead = true;
+      }
     }
     if (!ok) break;
     if constexpr (CG == 1)
       mma_commit(tfull0 + 8 * acc);
     else
       mma_commit_pair(tfull0 + 8 * acc, 0x3);       // both CTAs' epilogues may read
+    if (!looked_ahead) have_next = sched_next<BN, CG>(p, sch, tn, rank);
+    t = tn;
+    have = have_next;
   }
   if (!ok && issued_any) {
     // Every MMA issued so far must finish before the TMEM is released.
@@ -494,13 +505,18 @@ __device__ void run_epilogue(const Params& p, uint32_t bars, uint32_t tmem_base,
     // Otherwise it publishes its fp32 partial (slot layout [column group of
     // 4][row][4], so a warp's float4 stores are contiguous), fences, and bumps
     // the tile's counter; the piece that brings the counter to npieces - 1 is
-    // the last. The last piece sums all pieces in k order (its own from TMEM)
-    // and stores the tile. A CTA pair keeps one slot and one counter per half.
+    // the last. The last piece sums all pieces in k order and stores the tile.
+    // A piece that publishes hands its accumulator back as soon as it has read
+    // it (before the fence and the counter round trips: the MMA issuer may need
+    // it for the unit after next); if it then turns out to be the last, it reads
+    // its own partial back from its slot. A CTA pair keeps one slot and one
+    // counter per half.
     const int half = t.tile * CG + static_cast<int>(rank);
     const uint32_t others = static_cast<uint32_t>(t.npieces - 1);
     if (et == 0) *last_flag = (ld_relaxed_gpu(&p.counters[half]) == others) ? 1 : 0;
     epilogue_bar_sync();
     bool last = *last_flag != 0;
+    bool own_in_tmem = true;
     if (!last) {
       float* slot = p.partials +
                     (static_cast<size_t>(t.slot0 + t.piece) * CG + rank) * (BM * BN);
@@ -515,6 +531,8 @@ __device__ void run_epilogue(const Params& p, uint32_t bars, uint32_t tmem_base,
           __stcg(reinterpret_cast<float4*>(slot) + (8 * c + j) * BM + row_in_tile, f);
         }
       }
+      release_accumulator();
+      own_in_tmem = false;
       __threadfence();
       epilogue_bar_sync();
       if (et == 0) *last_flag = (atomicAdd(&p.counters[half], 1u) == others) ? 1 : 0;
@@ -529,7 +547,7 @@ __device__ void run_epilogue(const Params& p, uint32_t bars, uint32_t tmem_base,
       const float4* base = reinterpret_cast<const float4*>(p.partials);
       const size_t slot_f4 = static_cast<size_t>(BM) * BN / 4;
       auto load_piece = [&](int s, int c, float (&d)[64]) {
-        if (s == t.piece) {
+        if (s == t.piece && own_in_tmem) {
           uint32_t v[32], u[32];
           tmem_ld_32cols(taddr + 32 * c, v);
           if (c + 1 < chunks) tmem_ld_32cols(taddr + 32 * (c + 1), u);
@@ -569,7 +587,7 @@ __device__ void run_epilogue(const Params& p, uint32_t bars, uint32_t tmem_base,
       }
       if (et == 0) atomicExch(&p.counters[half], 0u);  // ready for the next call
     }
-    release_accumulator();  // the TMEM accumulator is free for the next tile
+    if (own_in_tmem) release_accumulator();  // the TMEM accumulator is free for the next tile
   }
 }
 
