@@ -73,7 +73,8 @@ typedef enum {
 /* Plan options (gemm_shard_plan_set_option). 0 restores the default. */
 typedef enum {
     GSR_OPT_SPLIT_K = 1,    /* pieces per output tile: 0 = heuristic, 1..16 forced */
-    GSR_OPT_BLOCK_N = 2,    /* output tile width: 0 = heuristic, 128 or 256         */
+    GSR_OPT_BLOCK_N = 2,    /* output tile width: 0 = heuristic, 128, 192 (CTA
+                               pairs only; 256 otherwise) or 256              */
     GSR_OPT_TIMEOUT_NS = 3, /* limit of every in-kernel wait, ns (default 2e9)      */
     GSR_OPT_MAX_CTAS = 4,   /* cap on persistent CTAs: 0 = one per SM               */
     GSR_OPT_RASTER_M = 5,   /* m-tiles per raster group (m runs fastest inside a
@@ -337,7 +338,7 @@ const char *gsr_last_error_string(void);
 
 /* Kernel configuration of a call, as gemm_shard_describe reports it. */
 typedef struct {
-    int block_n;            /* output tile width: 128 or 256                        */
+    int block_n;            /* output tile width: 128, 192 or 256                   */
     int cta_group;          /* 1: a CTA per 128-row tile; 2: a CTA pair per 256 rows */
     int schedule;           /* 1 = uniform pieces, 2 = stream-K hybrid, 3 = the
                                small-M kernel (block_n = 128 W rows per tile, split

@@ -251,6 +251,11 @@ Config choose_config(const gemm_shard_plan* P, int mode, int64_t M, int64_t N, i
     const double eff2 = static_cast<double>(rows) / (mt2 * 2 * BM);
     c.cta_group = (pairs_fit && eff2 >= 0.9 * eff1) ? 2 : 1;   // pairs measured 10-20 % faster
   }
+  // 192-column tiles exist for CTA pairs only.
+  if (c.block_n == 192 && c.cta_group != 2) {
+    c.block_n = 256;
+    c.n_tiles = cdiv(N, c.block_n);
+  }
   c.m_tiles = c.cta_group == 2 ? mt2 : mt1;
   c.tiles = c.m_tiles * c.n_tiles;
   const int64_t workers =
@@ -579,8 +584,8 @@ gsr_status gemm_shard_plan_set_option(gemm_shard_plan* plan, gsr_option option, 
       plan->opt_split = static_cast<int>(value);
       return ok();
     case GSR_OPT_BLOCK_N:
-      if (value != 0 && value != 128 && value != 256)
-        return fail(GSR_ERR_INVALID_VALUE, "block_n must be 0, 128 or 256");
+      if (value != 0 && value != 128 && value != 192 && value != 256)
+        return fail(GSR_ERR_INVALID_VALUE, "block_n must be 0, 128, 192 or 256");
       plan->opt_block_n = static_cast<int>(value);
       return ok();
     case GSR_OPT_TIMEOUT_NS:

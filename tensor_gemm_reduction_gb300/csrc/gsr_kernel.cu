@@ -188,6 +188,13 @@ __device__ __forceinline__ uint32_t tile_mma_n(const Params& p, const Unit& t) {
 
 // ------------------------------------------------------------ shared layout
 
+// TMEM columns of the two accumulators: a power of two (an allocation rule),
+// each accumulator at half of it (192-column tiles use 2 x 256 columns).
+template <int BN>
+__host__ __device__ constexpr uint32_t tmem_cols() { return BN <= 64 ? 128 : BN <= 128 ? 256 : 512; }
+template <int BN>
+__host__ __device__ constexpr uint32_t acc_stride() { return tmem_cols<BN>() / 2; }
+
 template <int BN, int STAGES, int CG>
 struct Layout {
   static constexpr uint32_t kABytes = BM * BK * 2;            // this CTA's rows of A
@@ -329,7 +336,7 @@ __device__ void run_mma(const Params& p, uint32_t tiles_base, uint32_t bars, uin
       break;
     }
     tc_fence_after_sync();
-    const uint32_t d_tmem = tmem_base + acc * BN;
+    const uint32_t d_tmem = tmem_base + acc * acc_stride<BN>();
     const uint32_t idesc = make_idesc(BM * CG, tile_mma_n<BN>(p, t));
     // The next slot's barrier is tested (without blocking) before this slot's
     // MMAs are issued, so the test overlaps the tensor pipe's work instead of
@@ -427,7 +434,7 @@ __device__ void run_epilogue(const Params& p, uint32_t bars, uint32_t tmem_base,
     if (!epilogue_bar_and(ok)) break;  // all 128 threads leave together
     tc_fence_after_sync();
 
-    const uint32_t taddr = tmem_base + lane_addr + acc * BN;
+    const uint32_t taddr = tmem_base + lane_addr + acc * acc_stride<BN>();
     const int n_valid = min(BN, p.N - t.n0);
     const int chunks = (n_valid + 31) >> 5;
     const int m0 = t.m0;   // this CTA's first row
@@ -627,10 +634,10 @@ __global__ void __launch_bounds__(kThreads, 1) gsr_gemm_kernel(const __grid_cons
   }
   if (warp == 1) {
     if constexpr (CG == 1) {
-      tmem_alloc(smem_u32(tmem_slot), 2 * BN);
+      tmem_alloc(smem_u32(tmem_slot), tmem_cols<BN>());
       tmem_relinquish();
     } else {
-      tmem_alloc_pair(smem_u32(tmem_slot), 2 * BN);
+      tmem_alloc_pair(smem_u32(tmem_slot), tmem_cols<BN>());
       tmem_relinquish_pair();
     }
   }
@@ -671,9 +678,9 @@ __global__ void __launch_bounds__(kThreads, 1) gsr_gemm_kernel(const __grid_cons
   if (warp == 1) {
     tc_fence_after_sync();
     if constexpr (CG == 1)
-      tmem_dealloc(tmem_base, 2 * BN);
+      tmem_dealloc(tmem_base, tmem_cols<BN>());
     else
-      tmem_dealloc_pair(tmem_base, 2 * BN);
+      tmem_dealloc_pair(tmem_base, tmem_cols<BN>());
   }
 }
 
@@ -683,6 +690,7 @@ template <> struct Stages<256, 1> { static constexpr int value = 4; };   // 48 K
 template <> struct Stages<128, 1> { static constexpr int value = 6; };   // 32 KB
 template <> struct Stages<256, 2> { static constexpr int value = 7; };   // 32 KB per CTA
 template <> struct Stages<128, 2> { static constexpr int value = 8; };   // 24 KB per CTA
+template <> struct Stages<192, 2> { static constexpr int value = 8; };   // 28 KB per CTA
 
 template <int BN, int CG>
 using KernelLayout = Layout<BN, Stages<BN, CG>::value, CG>;
@@ -724,7 +732,9 @@ cudaError_t launch_instance(const Params& p, int ctas, cudaStream_t stream) {
 
 size_t kernel_smem_bytes(int block_n, int cta_group) {
   if (cta_group == 2)
-    return block_n == 256 ? KernelLayout<256, 2>::kSmem : KernelLayout<128, 2>::kSmem;
+    return block_n == 256   ? KernelLayout<256, 2>::kSmem
+           : block_n == 192 ? KernelLayout<192, 2>::kSmem
+                            : KernelLayout<128, 2>::kSmem;
   return block_n == 256 ? KernelLayout<256, 1>::kSmem : KernelLayout<128, 1>::kSmem;
 }
 
@@ -734,6 +744,7 @@ cudaError_t prepare_kernels(int device, int* pair_clusters) {
   if (e == cudaSuccess) e = set_smem_limit<128, 1>();
   if (e == cudaSuccess) e = set_smem_limit<256, 2>();
   if (e == cudaSuccess) e = set_smem_limit<128, 2>();
+  if (e == cudaSuccess) e = set_smem_limit<192, 2>();
   if (e != cudaSuccess) return e;
   // How many CTA pairs can be resident at once (SMs pair up inside a GPC).
   cudaLaunchConfig_t cfg = {};
@@ -753,8 +764,9 @@ cudaError_t prepare_kernels(int device, int* pair_clusters) {
 
 cudaError_t launch_gemm(const Params& p, int block_n, int cta_group, int ctas, cudaStream_t stream) {
   if (cta_group == 2)
-    return block_n == 256 ? launch_instance<256, 2>(p, ctas, stream)
-                          : launch_instance<128, 2>(p, ctas, stream);
+    return block_n == 256   ? launch_instance<256, 2>(p, ctas, stream)
+           : block_n == 192 ? launch_instance<192, 2>(p, ctas, stream)
+                            : launch_instance<128, 2>(p, ctas, stream);
   return block_n == 256 ? launch_instance<256, 1>(p, ctas, stream)
                         : launch_instance<128, 1>(p, ctas, stream);
 }

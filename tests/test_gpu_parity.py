@@ -19,13 +19,14 @@ pytestmark = pytest.mark.gpu
 # the oracle): the heuristic; the uniform schedule; stream-K on only 8 CTAs (so
 # that even small shapes cut tiles into several pieces); CTA pairs with 128-
 # and 256-column whole tiles; CTA pairs with stream-K; CTA pairs with a
-# uniform 3-way split.
+# uniform 3-way split; CTA pairs with 192-column tiles.
 VARIANTS = {
     "auto": {},
     "uniform": dict(schedule=1),
     "sk8": dict(schedule=2, max_ctas=8),
     "pair128": dict(cta_group=2, block_n=128, schedule=1),
     "pair256": dict(cta_group=2, block_n=256, schedule=1),
+    "pair192": dict(cta_group=2, block_n=192),
     "pairsk8": dict(cta_group=2, schedule=2, max_ctas=8),
     "pairsk8last": dict(cta_group=2, schedule=4, max_ctas=8),
     "pairsplit": dict(max_M=4096, max_N=8192, max_K=8192, max_R=16, cta_group=2, split_k=3),
