@@ -91,7 +91,7 @@ typedef enum {
                                over the partial last wave, each worker's
                                stream-K range before its whole tiles, 4 = as 3
                                with the whole tiles first                        */
-    GSR_OPT_SMALL_M = 9     /* the small-M kernel (AR/RS, M <= 256): 0 = heuristic
+    GSR_OPT_SMALL_M = 9,    /* the small-M kernel (AR/RS, M <= 256): 0 = heuristic
                                (used when M <= 256 and no other option above
                                forces a configuration), 1 = never, 2 = whenever
                                M <= 256 and the K range has at least two
@@ -101,6 +101,10 @@ typedef enum {
                                the two CTAs of a cluster and summed in
                                distributed shared memory; it needs no workspace
                                beyond the status word                            */
+    GSR_OPT_SMALL_TILE_ROWS = 10 /* W rows per tile of the small-M kernel: 0 =
+                               heuristic (the fewest rows, in multiples of 8 up
+                               to 128, that spread N over every SM pair in the
+                               fewest waves), else a multiple of 8 in 8..128     */
 } gsr_option;
 
 /*
@@ -338,11 +342,12 @@ const char *gsr_last_error_string(void);
 
 /* Kernel configuration of a call, as gemm_shard_describe reports it. */
 typedef struct {
-    int block_n;            /* output tile width: 128, 192 or 256                   */
+    int block_n;            /* output tile width: 128, 192 or 256 (the small-M
+                               kernel: W rows per tile, a multiple of 8 <= 128)   */
     int cta_group;          /* 1: a CTA per 128-row tile; 2: a CTA pair per 256 rows */
     int schedule;           /* 1 = uniform pieces, 2 = stream-K hybrid, 3 = the
-                               small-M kernel (block_n = 128 W rows per tile, split
-                               = 2 halves of K per tile on a cluster of two CTAs) */
+                               small-M kernel (block_n W rows per tile, split = 2
+                               halves of K per tile on a cluster of two CTAs)     */
     int split;              /* uniform schedule: pieces per tile                    */
     int64_t tiles;          /* output tiles                                         */
     int64_t dp_tiles;       /* stream-K: tiles run whole                            */

@@ -38,6 +38,7 @@ struct gemm_shard_plan {
   int opt_schedule;    // 0 = heuristic (stream-K hybrid), 1 = uniform, 2 = stream-K hybrid,
                        // 3 = stream-K only for a partial last wave
   int opt_small;       // 0 = heuristic, 1 = never use the small-M kernel, 2 = always when it applies
+  int opt_small_rows;  // small-M kernel: W rows per tile (0 = heuristic)
   int pair_clusters;   // CTA pairs that can be resident at once
   uint64_t timeout_ns;
 };
@@ -166,8 +167,11 @@ Config choose_config(const gemm_shard_plan* P, int mode, int64_t M, int64_t N, i
   Config c;
   // Small M (AR/RS, a decode-like batch of at most 256 rows): streaming W is
   // the whole cost, so the small-M kernel runs every activation row against
-  // 128-row tiles of W, each tile split over K between the two CTAs of a
-  // cluster. Like every choice here it depends on the shape, not on the mode.
+  // tiles of W rows, each tile split over K between the two CTAs of a cluster.
+  // The tile height is the smallest multiple of 8 (up to 128) that covers N
+  // with every cluster in the fewest waves, so that all SMs stream W (N = 7168
+  // on 76 clusters: 96 rows, 75 tiles). Like every choice here it depends on
+  // the shape, not on the mode.
   if (mode != gsr::kModeAG && M >= 1 && M <= gsr::kSmallMaxM && P->opt_small != 1) {
     int64_t kb = 0;
     for (int r = 0; r < R; ++r) kb += cdiv(sizes[r], BK);
@@ -176,17 +180,23 @@ Config choose_config(const gemm_shard_plan* P, int mode, int64_t M, int64_t N, i
       c.small = 1;
       c.m_pad = static_cast<int>(std::max<int64_t>(16, cdiv(M, 16) * 16));
       c.stages = gsr::small_stages(c.m_pad);
-      c.block_n = gsr::kSmallTileN;
+      const int cap = P->opt_max_ctas ? std::min(P->opt_max_ctas, P->sm_count) : P->sm_count;
+      const int64_t clusters = std::max(cap / 2, 1);
+      int64_t rows = P->opt_small_rows;
+      if (!rows) {
+        const int64_t waves = cdiv(N, gsr::kSmallTileN * clusters);
+        rows = std::min<int64_t>(gsr::kSmallTileN, cdiv(cdiv(N, waves * clusters), 8) * 8);
+      }
+      c.block_n = static_cast<int>(rows);
       c.cta_group = 1;
       c.sched = gsr::kSchedKPair;
       c.splits = 2;
       c.kb_total = kb;
       c.m_tiles = 1;
-      c.n_tiles = cdiv(N, gsr::kSmallTileN);
+      c.n_tiles = cdiv(N, rows);
       c.tiles = c.n_tiles;
       c.units = 2 * c.tiles;
-      const int cap = P->opt_max_ctas ? std::min(P->opt_max_ctas, P->sm_count) : P->sm_count;
-      c.ctas = static_cast<int>(2 * std::min<int64_t>(c.tiles, std::max(cap / 2, 1)));
+      c.ctas = static_cast<int>(2 * std::min<int64_t>(c.tiles, clusters));
       // Every cluster reads all of X and a disjoint slice of W.
       const int hints = P->opt_l2_hints;
       c.policy_a = (hints == 0 || hints == 2) ? gsr::kPolicyEvictLast
@@ -382,6 +392,7 @@ void fill_common(gsr::Params& p, const gemm_shard_plan* P, const Config& c, int 
   p.policy_b = c.policy_b;
   p.m_pad = c.m_pad;
   p.stages = c.stages;
+  p.tile_rows = c.small ? c.block_n : 0;
   p.timeout_ns = P->timeout_ns;
   uint8_t* w = static_cast<uint8_t*>(ws);
   p.status = reinterpret_cast<uint32_t*>(w);
@@ -522,6 +533,7 @@ static gemm_shard_plan* new_plan(int device, int sm_count, int64_t max_M, int64_
   P->opt_cta_group = 0;
   P->opt_schedule = 0;
   P->opt_small = 0;
+  P->opt_small_rows = 0;
   P->pair_clusters = sm_count / 2;   // host plans: every SM pairs up
   P->timeout_ns = 2000000000ull;
   return P;
@@ -615,6 +627,12 @@ gsr_status gemm_shard_plan_set_option(gemm_shard_plan* plan, gsr_option option, 
     case GSR_OPT_SMALL_M:
       if (value < 0 || value > 2) return fail(GSR_ERR_INVALID_VALUE, "small_m must be 0..2");
       plan->opt_small = static_cast<int>(value);
+      return ok();
+    case GSR_OPT_SMALL_TILE_ROWS:
+      if (value < 0 || value > gsr::kSmallTileN || value % 8)
+        return fail(GSR_ERR_INVALID_VALUE, "small_tile_rows must be 0 or a multiple of 8 up to %d",
+                    gsr::kSmallTileN);
+      plan->opt_small_rows = static_cast<int>(value);
       return ok();
   }
   return fail(GSR_ERR_INVALID_VALUE, "unknown option %d", static_cast<int>(option));

@@ -289,6 +289,15 @@ __device__ __forceinline__ void cluster_barrier() {
           : "memory");
 }
 
+// The two halves of cluster_barrier, for a thread that has work to do in
+// between; each arrive is followed by its wait before the next arrive.
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // Arrive on an mbarrier given by its shared::cluster address (possibly the peer's).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)

@@ -83,12 +83,15 @@ struct Params {  // 128-byte aligned through its CUtensorMap members
   int m_pad;                    // small-M kernel: activation rows rounded up to 16
                                 // (the MMA's N); 0 for the main kernel
   int stages;                   // small-M kernel: depth of the shared-memory ring
+  int tile_rows;                // small-M kernel: W rows per tile (a multiple of 8,
+                                // at most kSmallTileN; TMEM lanes past it unused)
 };
 
 // ---------------------------------------------------------------- small M
 // The small-M kernel (M <= kSmallMaxM, AR/RS) swaps the operands: a tile is
-// kSmallTileN rows of W (output columns, the MMA's M) against all m_pad
-// activation rows (the MMA's N). Its shared memory, from a 1024-aligned base:
+// up to kSmallTileN rows of W (output columns, the MMA's M, always 128: rows
+// past the tile are stale shared memory whose TMEM lanes are never stored)
+// against all m_pad activation rows (the MMA's N). Its shared memory, from a 1024-aligned base:
 // the W ring, the X ring, the staging area that receives the peer CTA's
 // partial for the output rows this CTA finishes, four per-warp transpose
 // buffers (32 x 32 bf16), the mbarriers and a few words. Host and device share

@@ -8,9 +8,12 @@
 // rows, W (N x K) is the only large operand.
 //
 // Operands are swapped so that no tensor-core row is wasted on a short batch:
-// a tile is 128 rows of W (128 output columns; the MMA's M) against all m_pad
+// a tile is tile_rows rows of W (output columns; the MMA's M) against all m_pad
 // activation rows (M rounded up to 16; the MMA's N), Y^T[n, m] accumulated in
-// TMEM with TMEM lane = output column and TMEM column = output row.
+// TMEM with TMEM lane = output column and TMEM column = output row. The MMA is
+// always 128 rows tall; with tile_rows < 128 (a multiple of 8, chosen so that N spreads over
+// every pair of SMs) the rows past the tile read stale shared memory into TMEM
+// lanes that are never stored.
 //
 // Each tile belongs to a cluster of two CTAs. CTA rank k accumulates the
 // k-blocks of its half of the K range (over every shard's k-blocks, in shard
@@ -71,8 +74,11 @@ __device__ __forceinline__ void kpair_range(const Params& p, uint32_t rank, int&
 static_assert(kMaxShards + 1 <= 32, "the shard table must fit in the lanes of a warp");
 
 struct KCursor {
-  int n0, kb, shard, shard_begin, next_begin;
-  __device__ KCursor(int begins, int kb_lo) : n0(static_cast<int>(blockIdx.x) / 2 * kSmallTileN), kb(kb_lo) {
+  int n0, n_step, kb, shard, shard_begin, next_begin;
+  __device__ KCursor(int begins, int kb_lo, int tile_rows)
+      : n0(static_cast<int>(blockIdx.x) / 2 * tile_rows),
+        n_step(static_cast<int>(gridDim.x) / 2 * tile_rows),
+        kb(kb_lo) {
     seek(begins, 0);
   }
   __device__ __forceinline__ void seek(int begins, int from) {
@@ -85,7 +91,7 @@ struct KCursor {
   __device__ __forceinline__ void advance(int begins, int kb_lo, int kb_hi) {
     if (++kb == kb_hi) {
       kb = kb_lo;
-      n0 += static_cast<int>(gridDim.x) / 2 * kSmallTileN;
+      n0 += n_step;
       seek(begins, 0);
     } else if (next_begin <= kb) {
       seek(begins, shard);
@@ -101,20 +107,17 @@ __device__ __forceinline__ int small_tiles_of_cluster(const Params& p) {
 
 __device__ void small_producer(const Params& p, const SmallLayout& L, uint32_t base,
                                const SmallBars& b, uint32_t rank, const Ctl& ctl) {
-  for (int r = 0; r < p.R; ++r) {
-    prefetch_tensormap(&p.tmap_a[r]);
-    prefetch_tensormap(&p.tmap_b[r]);
-  }
   const uint64_t pol_x = make_l2_policy(p.policy_a);
   const uint64_t pol_w = make_l2_policy(p.policy_b);
-  const uint32_t stage_tx = L.w_bytes + L.x_bytes;   // a W slot's barrier counts both tiles
+  // A slot's barrier counts both tiles: tile_rows rows of W and m_pad rows of X.
+  const uint32_t stage_tx = static_cast<uint32_t>(p.tile_rows) * BK * 2 + L.x_bytes;
   int kb_lo, kb_hi;
   kpair_range(p, rank, kb_lo, kb_hi);
   const int total = (kb_hi - kb_lo) * small_tiles_of_cluster(p);
   // shard_kb_begin[0..kMaxShards] in lanes 0..16 (kMaxShards + 1 <= 32)
   const int lane = static_cast<int>(threadIdx.x) & 31;
   const int begins = p.shard_kb_begin[lane <= kMaxShards ? lane : kMaxShards];
-  KCursor kc(begins, kb_lo);
+  KCursor kc(begins, kb_lo, p.tile_rows);
   // This loop alone feeds the tensor pipe and shares its scheduler with a
   // waiting warp: its critical path is kept short (slot and parity advance
   // incrementally; no division or search per k-block). Each added operation
@@ -135,7 +138,13 @@ __device__ void small_producer(const Params& p, const SmallLayout& L, uint32_t b
     tma_load_2d_hint(base + slot * L.w_bytes, &p.tmap_b[kc.shard], full, kc.kx(), kc.n0, pol_w);
     tma_load_2d_hint(base + L.x_off + slot * L.x_bytes, &p.tmap_a[kc.shard], full, kc.kx(), 0, pol_x);
     kc.advance(begins, kb_lo, kb_hi);
-    ++issued;
+    if (++issued == 1) {
+      // The other shards' descriptors, once the first copies are on their way.
+      for (int r = 0; r < p.R; ++r) {
+        prefetch_tensormap(&p.tmap_a[r]);
+        prefetch_tensormap(&p.tmap_b[r]);
+      }
+    }
     if (++slot == L.stages) {
       slot = 0;
       slot_parity ^= 1u;
@@ -251,7 +260,8 @@ __device__ void small_epilogue(const Params& p, const SmallLayout& L, uint32_t b
     if (!epilogue_bar_and(ok)) break;
     tc_fence_after_sync();
     const uint32_t taddr = tmem_base + lane_addr + acc * L.acc_stride;
-    const int n0 = tile * kSmallTileN;
+    const int n0 = tile * p.tile_rows;
+    const int n_end = min(n0 + p.tile_rows, p.N);   // TMEM lanes past the tile are not output
 
     // 1. The granules the peer finishes go into the peer's staging area, once
     //    the peer has consumed what this CTA sent for the previous tile.
@@ -302,7 +312,7 @@ __device__ void small_epilogue(const Params& p, const SmallLayout& L, uint32_t b
         const int row = vi >> 2, part = vi & 3;
         const int m = g * kGranule + row;
         const int n = n0 + quad * 32 + part * 8;
-        if (row < kGranule * cnt && m < p.M && n < p.N) {
+        if (row < kGranule * cnt && m < p.M && n < n_end) {
           const uint4 val = *reinterpret_cast<const uint4*>(tb + row * 32 + part * 8);
           for (int rep = 0; rep < reps; ++rep)
             *reinterpret_cast<uint4*>(out_row(p, m, rep) + n) = val;
@@ -352,9 +362,13 @@ __global__ void __launch_bounds__(kThreads, 1) gsr_small_kernel(const __grid_con
     tmem_relinquish();
   }
   tc_fence_before_sync();
-  cluster_barrier();   // the peer's barriers exist before anyone signals them
+  __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+  // Only the epilogue touches the peer CTA (its staging area and barriers), so
+  // only the epilogue waits here for the peer's barriers to exist; the
+  // producer and the MMA issuer start at once and wait after their loops.
+  cluster_arrive();
 
   // Programmatic dependent launch, as in the main kernel: nothing above
   // touches global memory.
@@ -365,10 +379,13 @@ __global__ void __launch_bounds__(kThreads, 1) gsr_small_kernel(const __grid_con
   if (warp == 0) {
     small_producer(p, L, base, b, rank, ctl);
     __syncwarp();
+    cluster_wait();
   } else if (warp == 1) {
     small_mma(p, L, base, b, tmem_base, rank, ctl);
     __syncwarp();
+    cluster_wait();
   } else {
+    cluster_wait();
     small_epilogue(p, L, base, base_ptr, b, tmem_base, rank, ctl);
   }
 

@@ -204,18 +204,35 @@ def test_config_is_independent_of_mode(host):
 
 
 def test_small_m_uses_the_k_pair_kernel(host):
-    # M <= 256 (AR/RS): the small-M kernel, 128-row tiles of W (block_n = 128)
-    # against all rows, each tile split over K between the two CTAs of a
-    # cluster: N = 7168 gives 56 tiles on 112 CTAs, whatever M up to 256.
+    # M <= 256 (AR/RS): the small-M kernel, tiles of W rows (block_n) against
+    # all rows, each tile split over K between the two CTAs of a cluster. The
+    # tile height is the smallest multiple of 8 that spreads N over every
+    # cluster in the fewest waves: N = 7168 on 148 SMs (74 clusters) gives
+    # 104-row tiles, 69 tiles on 138 CTAs, whatever M up to 256; on 152 SMs, 96
+    # rows and 75 tiles on 150 CTAs.
     for M in (1, 16, 127, 128, 129, 200, 256):
         d = host.describe(B.MODE_AR, M, 7168, 0, [896] * 8)
         assert (d["cta_group"], d["block_n"], d["schedule"], d["split"], d["tiles"], d["ctas"]) == \
-            (1, 128, 3, 2, 56, 112), M
+            (1, 104, 3, 2, 69, 138), M
         # no split-K partials or counters: the workspace is the fixed minimum
         assert d["workspace_bytes"] <= host.describe(B.MODE_AR, 4096, 7168, 0, [896] * 8)["workspace_bytes"]
-    # more tiles than clusters: one cluster per SM pair, tiles walked in turn
+    d = Host(host.lib, sm=152).describe(B.MODE_AR, 64, 7168, 0, [896] * 8)
+    assert (d["block_n"], d["tiles"], d["ctas"]) == (96, 75, 150)
+    # more tiles than clusters: one cluster per SM pair, tiles walked in turn;
+    # N = 32640 needs four waves of at most 128 rows: 112-row tiles
     d = host.describe(B.MODE_AR, 64, 32768 - 128, 0, [896] * 8)
-    assert d["schedule"] == 3 and d["tiles"] == 255 and d["ctas"] == 148
+    assert (d["schedule"], d["block_n"], d["tiles"], d["ctas"]) == (3, 112, 292, 148)
+    # small N: one tile of 8 rows
+    d = host.describe(B.MODE_AR, 64, 8, 0, [896] * 8)
+    assert (d["block_n"], d["tiles"], d["ctas"]) == (8, 1, 2)
+    # the tile height as an option: 128 rows, 56 tiles on 112 CTAs
+    h = Host(host.lib)
+    B.gemm_shard_plan_set_option(h.plan, B.GSR_OPT_SMALL_TILE_ROWS, 128)
+    d = h.describe(B.MODE_AR, 128, 7168, 0, [896] * 8)
+    assert (d["schedule"], d["block_n"], d["tiles"], d["ctas"]) == (3, 128, 56, 112)
+    for bad in (-8, 4, 20, 136):
+        with pytest.raises(B.GsrError):
+            B.gemm_shard_plan_set_option(h.plan, B.GSR_OPT_SMALL_TILE_ROWS, bad)
     # a capped grid keeps whole clusters
     h = Host(host.lib)
     B.gemm_shard_plan_set_option(h.plan, B.GSR_OPT_MAX_CTAS, 9)

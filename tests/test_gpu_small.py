@@ -128,3 +128,22 @@ def test_small_full_o_proj_matches_oracle_rows():
         ref = oracle.ar_at(X_h, W_h, r, c).reshape(len(rows), 7168)
         assert_close(to_f64(Y.out[torch.as_tensor(rows, device=device())]), ref, f"o_proj m{M}")
         assert Y.guards_intact()
+
+
+@pytest.mark.parametrize("rows", [8, 40, 96, 120])
+def test_small_tile_rows_agree_bitwise(rows):
+    """Every tile height sums each output in the same order (the two halves of
+    K added once), so the outputs are bit-identical to 128-row tiles. The MMA
+    is always 128 rows tall: with shorter tiles its rows past the tile read
+    stale shared memory into TMEM lanes that must never be stored (guards,
+    ragged last tile of N = 1000, several tiles per cluster at 8 rows)."""
+    inp = gi.gaussian_ar(100, 1000, [448, 200, 72], seed=31)
+    ref_bits = bits_of(run(inp, small_plan(small_tile_rows=128)).out)
+    Y = run(inp, small_plan(small_tile_rows=rows))
+    assert Y.guards_intact()
+    assert np.array_equal(bits_of(Y.out), ref_bits)
+    assert_close(to_f64(Y.out), oracle.ar(inp.X_r, inp.W_r), f"small, {rows}-row tiles")
+    for s, y in enumerate(run(inp, small_plan(small_tile_rows=rows), "rs")):
+        first, count = oracle.rs_rows(100, 3, s)
+        assert y.guards_intact(valid_rows=count)
+        assert np.array_equal(bits_of(y.out[:count]), ref_bits[first:first + count])
