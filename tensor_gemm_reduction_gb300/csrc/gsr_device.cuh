@@ -251,6 +251,7 @@ __device__ __forceinline__ void epilogue_bar_sync() {
 }
 
 // Named barrier over the epilogue threads that also ANDs a predicate.
+template <int kCount = kEpilogueThreads>
 __device__ __forceinline__ bool epilogue_bar_and(bool v) {
   uint32_t out;
   asm volatile(
@@ -259,7 +260,7 @@ __device__ __forceinline__ bool epilogue_bar_and(bool v) {
       "bar.red.and.pred po, 1, %2, pi;\n\t"
       "selp.u32 %0, 1, 0, po;\n\t}"
       : "=r"(out)
-      : "r"(static_cast<uint32_t>(v)), "n"(kEpilogueThreads)
+      : "r"(static_cast<uint32_t>(v)), "n"(kCount)
       : "memory");
   return out != 0;
 }

@@ -93,18 +93,21 @@ struct Params {  // 128-byte aligned through its CUtensorMap members
 // past the tile are stale shared memory whose TMEM lanes are never stored)
 // against all m_pad activation rows (the MMA's N). Its shared memory, from a 1024-aligned base:
 // the W ring, the X ring, the staging area that receives the peer CTA's
-// partial for the output rows this CTA finishes, four per-warp transpose
-// buffers (32 x 32 bf16), the mbarriers and a few words. Host and device share
+// partial for the output rows this CTA finishes (and, once read, the bf16
+// transposes of the finished rows), the mbarriers and a few words. Host and device share
 // this layout.
 constexpr int kSmallTileN = 128;
 constexpr int kSmallMaxM = 256;
+constexpr int kSmallEpiWarps = 8;            // two per TMEM lane quarter
+constexpr int kSmallEpiThreads = 32 * kSmallEpiWarps;
+constexpr int kSmallThreads = 64 + kSmallEpiThreads;  // warp 0 TMA, warp 1 MMA, the rest epilogue
 constexpr int kGranule = 16;                 // output rows per exchange granule
 constexpr int kSmallMaxStages = 16;
 constexpr uint32_t kSmallSmemLimit = 232448; // 227 KB per CTA
 
 struct SmallLayout {
   uint32_t w_bytes, x_bytes, stages;
-  uint32_t x_off, staging_off, transpose_off, bars_off, misc_off, total;  // total includes 1024 of alignment slack
+  uint32_t x_off, staging_off, bars_off, misc_off, total;  // total includes 1024 of alignment slack
   uint32_t tmem_cols, acc_stride;
 };
 
@@ -119,8 +122,7 @@ __host__ __device__ inline SmallLayout small_layout(int m_pad, int stages) {
   L.stages = static_cast<uint32_t>(stages);
   L.x_off = L.stages * L.w_bytes;
   L.staging_off = L.x_off + L.stages * L.x_bytes;
-  L.transpose_off = L.staging_off + small_owned_granules(m_pad) * kGranule * kSmallTileN * 4;
-  L.bars_off = L.transpose_off + 4 * 32 * 32 * 2;
+  L.bars_off = L.staging_off + small_owned_granules(m_pad) * kGranule * kSmallTileN * 4;
   L.misc_off = L.bars_off + (2 * L.stages + 7) * 8;
   L.total = 1024 + L.misc_off + 16;
   uint32_t cols = 32;

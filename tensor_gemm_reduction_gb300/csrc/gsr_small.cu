@@ -32,8 +32,11 @@
 // shard m / rps; the configuration depends only on the shape, so RS rows equal
 // AR rows bit for bit.
 //
-// Roles (192 threads): warp 0 TMA producer, warp 1 MMA issuer, warps 2..5
-// epilogue; every wait is bounded by %globaltimer like the main kernel's.
+// Roles (320 threads): warp 0 TMA producer, warp 1 MMA issuer, warps 2..9
+// epilogue, two per quarter of the TMEM lanes (a warp reads only the lanes of
+// its own quarter), taking alternate 32-row chunks of the output rows: the
+// epilogue is latency-bound inside each warp, so two warps per quarter halve
+// it. Every wait is bounded by %globaltimer like the main kernel's.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -236,7 +239,9 @@ __device__ void small_epilogue(const Params& p, const SmallLayout& L, uint32_t b
                                uint8_t* base_ptr, const SmallBars& b, uint32_t tmem_base,
                                uint32_t rank, const Ctl& ctl) {
   const int lane = static_cast<int>(threadIdx.x) & 31;
+  const int ew = (static_cast<int>(threadIdx.x) >> 5) - 2;     // epilogue warp 0..7
   const int quad = (static_cast<int>(threadIdx.x) >> 5) & 3;  // TMEM lanes this warp may read
+  const int first = 2 * (ew >> 2);   // this warp's first granule pair: chunks alternate
   const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
   const int granules = p.m_pad / kGranule;
   const int g_split = static_cast<int>(small_owned_granules(p.m_pad));  // rank 0 owns [0, g_split)
@@ -250,14 +255,15 @@ __device__ void small_epilogue(const Params& p, const SmallLayout& L, uint32_t b
   const uint32_t peer_drained = map_shared_to_rank(b.drained, peer);
   const int col_lane = quad * 32 + lane;   // this thread's TMEM lane = column in the tile
   const int reps = p.mode == kModeARRep ? p.R : 1;
-  // This warp's transpose buffer: 32 rows x 32 columns of bf16.
-  uint16_t* tb = reinterpret_cast<uint16_t*>(base_ptr + L.transpose_off) + quad * (2 * kGranule * 32);
+  // A quarter of TMEM lanes wholly past the tile (96-row tiles: lanes 96..127)
+  // holds no output: its warps only take part in the handshakes.
+  const bool live = quad * 32 < p.tile_rows;
   uint32_t local = 0;
   for (int tile = static_cast<int>(blockIdx.x) / 2; tile < p.n_tiles;
        tile += static_cast<int>(gridDim.x) / 2, ++local) {
     const uint32_t acc = local & 1u;
     bool ok = wait_bounded(b.tfull0 + 8 * acc, (local >> 1) & 1u, ctl, (kRoleEpilogue << 8) | 1);
-    if (!epilogue_bar_and(ok)) break;
+    if (!epilogue_bar_and<kSmallEpiThreads>(ok)) break;
     tc_fence_after_sync();
     const uint32_t taddr = tmem_base + lane_addr + acc * L.acc_stride;
     const int n0 = tile * p.tile_rows;
@@ -267,9 +273,9 @@ __device__ void small_epilogue(const Params& p, const SmallLayout& L, uint32_t b
     //    the peer has consumed what this CTA sent for the previous tile.
     if (local > 0) {
       ok = wait_bounded_cluster(b.drained, (local - 1) & 1u, ctl, (kRoleEpilogue << 8) | 2);
-      if (!epilogue_bar_and(ok)) break;
+      if (!epilogue_bar_and<kSmallEpiThreads>(ok)) break;
     }
-    for (int g = peer_lo; g < peer_hi; g += 2) {
+    for (int g = peer_lo + first; live && g < peer_hi; g += 4) {
       const int cnt = min(2, peer_hi - g);
       uint32_t v[32];
       load_granules(taddr + g * kGranule, cnt, v);
@@ -283,26 +289,35 @@ __device__ void small_epilogue(const Params& p, const SmallLayout& L, uint32_t b
     mbar_arrive_cluster(peer_staged);   // release at cluster scope: the stores above first
 
     // 2. This CTA's granules: its own half plus the peer's, rounded to bf16,
-    //    transposed and stored.
+    //    transposed and stored. The transpose goes back into the part of the
+    //    staging area this warp has just read (its 32 lanes of the granules'
+    //    column groups, 512 bytes each, 2048 bytes apart): 8 rows of 32 bf16
+    //    columns per block, so no separate buffer is needed.
     ok = wait_bounded_cluster(b.staged, local & 1u, ctl, (kRoleEpilogue << 8) | 3);
-    if (!epilogue_bar_and(ok)) break;
-    for (int g = own_lo; g < own_hi; g += 2) {
+    if (!epilogue_bar_and<kSmallEpiThreads>(ok)) break;
+    for (int g = own_lo + first; live && g < own_hi; g += 4) {
       const int cnt = min(2, own_hi - g);
       uint32_t v[32];
       load_granules(taddr + g * kGranule, cnt, v);
       const float4* src = my_staging + (g - own_lo) * 4 * kSmallTileN + col_lane;
+      uint8_t* const blocks = base_ptr + L.staging_off +
+                              static_cast<size_t>((g - own_lo) * 4 * kSmallTileN + quad * 32) * 16;
       float4 f[8];
 #pragma unroll
       for (int c4 = 0; c4 < 8; ++c4)
         if (c4 < 4 * cnt) f[c4] = src[c4 * kSmallTileN];
-      // rows 16g .. 16g + 16 cnt of this warp's 32 columns, transposed in tb[row][column]
+      __syncwarp();   // every lane has read its staging before the blocks are overwritten
+      // rows 16g .. 16g + 16 cnt of this warp's 32 columns: row r at block r / 8
 #pragma unroll
       for (int c4 = 0; c4 < 8; ++c4) {
         if (c4 >= 4 * cnt) break;
-        tb[(4 * c4 + 0) * 32 + lane] = bf16_bits(__uint_as_float(v[4 * c4 + 0]) + f[c4].x);
-        tb[(4 * c4 + 1) * 32 + lane] = bf16_bits(__uint_as_float(v[4 * c4 + 1]) + f[c4].y);
-        tb[(4 * c4 + 2) * 32 + lane] = bf16_bits(__uint_as_float(v[4 * c4 + 2]) + f[c4].z);
-        tb[(4 * c4 + 3) * 32 + lane] = bf16_bits(__uint_as_float(v[4 * c4 + 3]) + f[c4].w);
+        const float a[4] = {f[c4].x, f[c4].y, f[c4].z, f[c4].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int r = 4 * c4 + j;
+          reinterpret_cast<uint16_t*>(blocks + (r >> 3) * (kSmallTileN * 16) + (r & 7) * 64)[lane] =
+              bf16_bits(__uint_as_float(v[r]) + a[j]);
+        }
       }
       __syncwarp();
       // 16-byte vectors: 8 rows x 4 parts of 8 columns per instruction
@@ -313,7 +328,8 @@ __device__ void small_epilogue(const Params& p, const SmallLayout& L, uint32_t b
         const int m = g * kGranule + row;
         const int n = n0 + quad * 32 + part * 8;
         if (row < kGranule * cnt && m < p.M && n < n_end) {
-          const uint4 val = *reinterpret_cast<const uint4*>(tb + row * 32 + part * 8);
+          const uint4 val = *reinterpret_cast<const uint4*>(blocks + t * (kSmallTileN * 16) +
+                                                            (row & 7) * 64 + part * 16);
           for (int rep = 0; rep < reps; ++rep)
             *reinterpret_cast<uint4*>(out_row(p, m, rep) + n) = val;
         }
@@ -329,7 +345,7 @@ __device__ void small_epilogue(const Params& p, const SmallLayout& L, uint32_t b
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 1) gsr_small_kernel(const __grid_constant__ Params p) {
+__global__ void __launch_bounds__(kSmallThreads, 1) gsr_small_kernel(const __grid_constant__ Params p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -348,10 +364,10 @@ __global__ void __launch_bounds__(kThreads, 1) gsr_small_kernel(const __grid_con
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(b.tfull0 + 8 * i, 1);                  // MMA commit
-      mbar_init(b.tempty0 + 8 * i, 4);                 // one per epilogue warp
+      mbar_init(b.tempty0 + 8 * i, kSmallEpiWarps);    // one per epilogue warp
     }
-    mbar_init(b.staged, kEpilogueThreads);    // every epilogue thread of the peer
-    mbar_init(b.drained, kEpilogueThreads);
+    mbar_init(b.staged, kSmallEpiThreads);    // every epilogue thread of the peer
+    mbar_init(b.drained, kSmallEpiThreads);
     mbar_init(b.drain, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -414,7 +430,7 @@ cudaError_t launch_small(const Params& p, int ctas, cudaStream_t stream) {
   attr[1].val.clusterDim.y = 1;
   attr[1].val.clusterDim.z = 1;
   cfg.gridDim = dim3(ctas, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(kSmallThreads, 1, 1);
   cfg.dynamicSmemBytes = small_layout(p.m_pad, p.stages).total;
   cfg.stream = stream;
   cfg.attrs = attr;
