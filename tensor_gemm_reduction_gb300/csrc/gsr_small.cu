@@ -78,10 +78,10 @@ static_assert(kMaxShards + 1 <= 32, "the shard table must fit in the lanes of a 
 
 struct KCursor {
   int n0, n_step, kb, shard, shard_begin, next_begin;
-  __device__ KCursor(int begins, int kb_lo, int tile_rows)
-      : n0(static_cast<int>(blockIdx.x) / 2 * tile_rows),
-        n_step(static_cast<int>(gridDim.x) / 2 * tile_rows),
-        kb(kb_lo) {
+  __device__ void start(int begins, int kb_lo, int tile_rows) {
+    n0 = static_cast<int>(blockIdx.x) / 2 * tile_rows;
+    n_step = static_cast<int>(gridDim.x) / 2 * tile_rows;
+    kb = kb_lo;
     seek(begins, 0);
   }
   __device__ __forceinline__ void seek(int begins, int from) {
@@ -108,19 +108,38 @@ __device__ __forceinline__ int small_tiles_of_cluster(const Params& p) {
   return c < p.n_tiles ? (p.n_tiles - 1 - c) / step + 1 : 0;
 }
 
+// The producer's kernel-parameter reads and its walk's starting point. Taken
+// at kernel entry, before the CTA's own set-up, so that the first reads of the
+// parameters and of the first shard's descriptors (cold after a launch) overlap
+// that set-up instead of delaying the first copy.
+struct ProducerStart {
+  uint64_t pol_x, pol_w;
+  uint32_t stage_tx;
+  int kb_lo, kb_hi, total, begins;
+  KCursor kc;
+  // Called by the whole producer warp.
+  __device__ void init(const Params& p, const SmallLayout& L, uint32_t rank) {
+    pol_x = make_l2_policy(p.policy_a);
+    pol_w = make_l2_policy(p.policy_b);
+    // A slot's barrier counts both tiles: tile_rows rows of W and m_pad rows of X.
+    stage_tx = static_cast<uint32_t>(p.tile_rows) * BK * 2 + L.x_bytes;
+    // shard_kb_begin[0..kMaxShards] in lanes 0..16 (kMaxShards + 1 <= 32)
+    const int lane = static_cast<int>(threadIdx.x) & 31;
+    begins = p.shard_kb_begin[lane <= kMaxShards ? lane : kMaxShards];
+    kpair_range(p, rank, kb_lo, kb_hi);
+    total = (kb_hi - kb_lo) * small_tiles_of_cluster(p);
+    kc.start(begins, kb_lo, p.tile_rows);
+    prefetch_tensormap(&p.tmap_b[kc.shard]);
+    prefetch_tensormap(&p.tmap_a[kc.shard]);
+  }
+};
+
 __device__ void small_producer(const Params& p, const SmallLayout& L, uint32_t base,
-                               const SmallBars& b, uint32_t rank, const Ctl& ctl) {
-  const uint64_t pol_x = make_l2_policy(p.policy_a);
-  const uint64_t pol_w = make_l2_policy(p.policy_b);
-  // A slot's barrier counts both tiles: tile_rows rows of W and m_pad rows of X.
-  const uint32_t stage_tx = static_cast<uint32_t>(p.tile_rows) * BK * 2 + L.x_bytes;
-  int kb_lo, kb_hi;
-  kpair_range(p, rank, kb_lo, kb_hi);
-  const int total = (kb_hi - kb_lo) * small_tiles_of_cluster(p);
-  // shard_kb_begin[0..kMaxShards] in lanes 0..16 (kMaxShards + 1 <= 32)
-  const int lane = static_cast<int>(threadIdx.x) & 31;
-  const int begins = p.shard_kb_begin[lane <= kMaxShards ? lane : kMaxShards];
-  KCursor kc(begins, kb_lo, p.tile_rows);
+                               const SmallBars& b, ProducerStart& st, const Ctl& ctl) {
+  const uint64_t pol_x = st.pol_x, pol_w = st.pol_w;
+  const uint32_t stage_tx = st.stage_tx;
+  const int kb_lo = st.kb_lo, kb_hi = st.kb_hi, total = st.total, begins = st.begins;
+  KCursor& kc = st.kc;
   // This loop alone feeds the tensor pipe and shares its scheduler with a
   // waiting warp: its critical path is kept short (slot and parity advance
   // incrementally; no division or search per k-block). Each added operation
@@ -356,6 +375,9 @@ __global__ void __launch_bounds__(kSmallThreads, 1) gsr_small_kernel(const __gri
   volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + L.misc_off + 4);
   const int warp = static_cast<int>(threadIdx.x) >> 5;
   const uint32_t rank = cluster_rank();
+  // Warp 0's (the producer's) set-up first; see ProducerStart.
+  ProducerStart start;
+  if (warp == 0) start.init(p, L, rank);
 
   if (threadIdx.x == 0) {
     for (uint32_t i = 0; i < L.stages; ++i) {
@@ -393,7 +415,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) gsr_small_kernel(const __gri
 
   Ctl ctl{abort_flag, p.status, p.timeout_ns};
   if (warp == 0) {
-    small_producer(p, L, base, b, rank, ctl);
+    small_producer(p, L, base, b, start, ctl);
     __syncwarp();
     cluster_wait();
   } else if (warp == 1) {
