@@ -205,6 +205,16 @@ class Runner:
         self._call()
 
 
+def trimmed_mean(xs, cut: float = 0.25):
+    """Mean of the middle of the sorted samples (a `cut` fraction dropped at each
+    end): robust to the odd slow launch, and unlike the median it averages out
+    the clustering of single flushed launches at values about a microsecond apart."""
+    s = sorted(xs)
+    k = int(len(s) * cut)
+    mid = s[k:len(s) - k] or s
+    return sum(mid) / len(mid)
+
+
 def time_launches(fn, steps: int, warmup: int, flush=None):
     """Per-launch CUDA-event durations (ms) on the current stream, plus the
     elapsed time of the whole region (ms)."""
@@ -316,7 +326,8 @@ def run_reference(args, w):
 
 
 def sweep(plan, ws, dev, pk, names):
-    """Per-workload kernel time with an L2 flush before every launch."""
+    """Per-workload kernel time with an L2 flush before every launch: the
+    trimmed mean of 20 launches."""
     import torch
     from tensor_gemm_reduction_gb300 import inputs as gi
     flush_buf = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
@@ -328,8 +339,8 @@ def sweep(plan, ws, dev, pk, names):
             r = Runner(w, plan, ws, dev)
         except torch.OutOfMemoryError:
             continue
-        times, _ = time_launches(r, steps=10, warmup=3, flush=lambda: flush_buf.fill_(1))
-        t = statistics.median(times) * 1e-3
+        times, _ = time_launches(r, steps=20, warmup=3, flush=lambda: flush_buf.fill_(1))
+        t = trimmed_mean(times) * 1e-3
         t_roof = max(w.flops / (pk["bf16_burst"] * 1e12), w.bytes / (pk["hbm_gbs"] * 1e9))
         d = B_describe(plan, w)
         rows.append({"workload": w.name, "mode": w.mode, "M": w.M, "N": w.N, "K": w.K, "R": w.R,
@@ -346,7 +357,7 @@ def sweep(plan, ws, dev, pk, names):
 
 def sweep_pack(plan, ws, dev, pk):
     """The packed gather of per-shard states (HBM-bound copy), timed like the
-    GEMM rows: median of 10 launches, an L2 flush before each."""
+    GEMM rows: trimmed mean of 20 launches, an L2 flush before each."""
     import torch
     from tensor_gemm_reduction_gb300 import binding as B
     from tensor_gemm_reduction_gb300 import inputs as gi
@@ -355,9 +366,9 @@ def sweep_pack(plan, ws, dev, pk):
     S = gi.gaussian_states([w.M_r] * w.R, w.T, w.H, seed=w.seed, device=dev)
     P = torch.empty(w.rows_out, w.T * w.H, dtype=torch.bfloat16, device=dev)
     call = B.prepare_pack_gather(plan, S, w.rows_out, P, ws)
-    times, _ = time_launches(call, steps=10, warmup=3, flush=lambda: flush_buf.fill_(1))
+    times, _ = time_launches(call, steps=20, warmup=3, flush=lambda: flush_buf.fill_(1))
     B.gemm_shard_check_status(plan, ws)
-    t = statistics.median(times) * 1e-3
+    t = trimmed_mean(times) * 1e-3
     row = {"workload": w.name, "mode": "pack", "R": w.R, "M_r": w.M_r, "T": w.T, "H": w.H,
            "rows_out": w.rows_out, "us": round(t * 1e6, 2), "hbm_gbs": round(w.bytes / t / 1e9, 1),
            "roofline_frac": round(w.bytes / (pk["hbm_gbs"] * 1e9) / t, 3), "bound": "hbm",

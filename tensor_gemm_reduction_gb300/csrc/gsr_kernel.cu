@@ -211,9 +211,38 @@ struct Layout {
 
 // ------------------------------------------------------------ roles
 
+// The producer's L2 policies, schedule and first unit, taken at kernel entry
+// before the CTA's own set-up (barriers, TMEM, cluster sync): their kernel-
+// parameter reads and the prefetch of the first unit's descriptors, cold after
+// a launch, overlap that set-up instead of delaying the first copy. Called by
+// the whole producer warp.
+template <int BN, int CG>
+struct ProducerEntry {
+  uint64_t pol_a, pol_b;
+  Sched sch;
+  Unit t;
+  bool have;
+  __device__ void init(const Params& p, uint32_t rank) {
+    pol_a = make_l2_policy(p.policy_a);
+    pol_b = make_l2_policy(p.policy_b);
+    sch = sched_begin<CG>(p);
+    have = sched_next<BN, CG>(p, sch, t, rank);
+    if (!have) return;
+    if (p.mode == kModeAG) {
+      prefetch_tensormap(&p.tmap_a[t.shard >= 0 ? t.shard : p.ag_pad_shard]);
+      prefetch_tensormap(&p.tmap_b[0]);
+    } else {
+      int r = 0;
+      while (p.shard_kb_begin[r + 1] <= t.kb_begin) ++r;
+      prefetch_tensormap(&p.tmap_a[r]);
+      prefetch_tensormap(&p.tmap_b[r]);
+    }
+  }
+};
+
 template <int BN, int STAGES, int CG>
 __device__ void run_producer(const Params& p, uint32_t tiles_base, uint32_t bars, uint32_t rank,
-                             const Ctl& ctl) {
+                             ProducerEntry<BN, CG>& entry, const Ctl& ctl) {
   using L = Layout<BN, STAGES, CG>;
   const uint32_t full0 = bars, empty0 = bars + 8 * STAGES;
   // The descriptors of the other shards are prefetched once the first k-block
@@ -231,15 +260,15 @@ __device__ void run_producer(const Params& p, uint32_t tiles_base, uint32_t bars
       }
     }
   };
-  const uint64_t pol_a = make_l2_policy(p.policy_a);
-  const uint64_t pol_b = make_l2_policy(p.policy_b);
+  const uint64_t pol_a = entry.pol_a;
+  const uint64_t pol_b = entry.pol_b;
   uint32_t issued = 0;
   uint32_t slot = 0, slot_parity = 1;   // ring slot of the next load; its free-wait parity
   uint32_t arrived = 0;   // AG with arrival flags: shards seen ready (bit r)
   bool ok = true;
-  Sched sch = sched_begin<CG>(p);
-  Unit t;
-  while (ok && sched_next<BN, CG>(p, sch, t, rank)) {
+  Sched& sch = entry.sch;
+  Unit t = entry.t;
+  for (bool have = entry.have; ok && have; have = sched_next<BN, CG>(p, sch, t, rank)) {
     if (p.ready != nullptr && t.shard >= 0 && !(arrived & (1u << t.shard))) {
       const bool here = wait_flag(p.ready + t.shard, p.epoch, ctl, (kRoleProducer << 8) | 3);
       __syncwarp();
@@ -616,6 +645,8 @@ __global__ void __launch_bounds__(kThreads, 1) gsr_gemm_kernel(const __grid_cons
   const int warp = static_cast<int>(threadIdx.x) >> 5;
   const int lane = static_cast<int>(threadIdx.x) & 31;
   const uint32_t rank = (CG == 1) ? 0u : cluster_rank();
+  ProducerEntry<BN, CG> entry;
+  if (warp == 0) entry.init(p, rank);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
@@ -659,7 +690,7 @@ __global__ void __launch_bounds__(kThreads, 1) gsr_gemm_kernel(const __grid_cons
 
   Ctl ctl{abort_flag, p.status, p.timeout_ns};
   if (warp == 0) {
-    run_producer<BN, STAGES, CG>(p, tiles_base, bars, rank, ctl);   // whole warp, elected issue
+    run_producer<BN, STAGES, CG>(p, tiles_base, bars, rank, entry, ctl);   // whole warp, elected issue
     __syncwarp();
   } else if (warp == 1) {
     // The whole warp walks the MMA loop (its values stay warp-uniform); one
