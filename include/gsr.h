@@ -101,10 +101,13 @@ typedef enum {
                                the two CTAs of a cluster and summed in
                                distributed shared memory; it needs no workspace
                                beyond the status word                            */
-    GSR_OPT_SMALL_TILE_ROWS = 10 /* W rows per tile of the small-M kernel: 0 =
+    GSR_OPT_SMALL_TILE_ROWS = 10, /* W rows per tile of the small-M kernel: 0 =
                                heuristic (the fewest rows, in multiples of 8 up
                                to 128, that spread N over every SM pair in the
                                fewest waves), else a multiple of 8 in 8..128     */
+    GSR_OPT_RASTER_N = 11   /* main kernel: n-tiles per raster group, n running
+                               fastest inside a group (0 = off: GSR_OPT_RASTER_M
+                               applies), 1..64                                   */
 } gsr_option;
 
 /*

@@ -35,6 +35,7 @@ GSR_OPT_CTA_GROUP = 7
 GSR_OPT_SCHEDULE = 8
 GSR_OPT_SMALL_M = 9
 GSR_OPT_SMALL_TILE_ROWS = 10
+GSR_OPT_RASTER_N = 11
 
 MODE_AR, MODE_RS, MODE_AG = 0, 1, 2
 

@@ -33,6 +33,7 @@ struct gemm_shard_plan {
   int opt_block_n;     // 0 = heuristic
   int opt_max_ctas;    // 0 = one per SM
   int opt_raster_m;    // 0 = heuristic
+  int opt_raster_n;    // 0 = raster by m-tile groups
   int opt_l2_hints;    // 0 = heuristic
   int opt_cta_group;   // 0 = heuristic
   int opt_schedule;    // 0 = heuristic (stream-K hybrid), 1 = uniform, 2 = stream-K hybrid,
@@ -150,6 +151,7 @@ struct Config {
   int sk_last = 0;
   int ctas = 0;
   int group_m = 1;
+  int group_n = 0;
   int policy_a = gsr::kPolicyNormal;
   int policy_b = gsr::kPolicyNormal;
   size_t ws_bytes = 0;
@@ -330,6 +332,7 @@ Config choose_config(const gemm_shard_plan* P, int mode, int64_t M, int64_t N, i
   // per launch, against 3.3 GB at 16, 4.2 GB at 4, 5.6 GB at 32) and the most
   // throughput at the power limit.
   c.group_m = P->opt_raster_m ? P->opt_raster_m : 8;
+  c.group_n = P->opt_raster_n;
   switch (P->opt_l2_hints) {
     case 2:
       c.policy_a = gsr::kPolicyEvictLast;
@@ -392,6 +395,7 @@ void fill_common(gsr::Params& p, const gemm_shard_plan* P, const Config& c, int 
   p.sk_iters = c.sk_iters;
   p.sk_last = c.sk_last;
   p.group_m = c.group_m;
+  p.group_n = c.group_n;
   p.policy_a = c.policy_a;
   p.policy_b = c.policy_b;
   p.m_pad = c.m_pad;
@@ -533,6 +537,7 @@ static gemm_shard_plan* new_plan(int device, int sm_count, int64_t max_M, int64_
   P->opt_block_n = 0;
   P->opt_max_ctas = 0;
   P->opt_raster_m = 0;
+  P->opt_raster_n = 0;
   P->opt_l2_hints = 0;
   P->opt_cta_group = 0;
   P->opt_schedule = 0;
@@ -615,6 +620,10 @@ gsr_status gemm_shard_plan_set_option(gemm_shard_plan* plan, gsr_option option, 
     case GSR_OPT_RASTER_M:
       if (value < 0 || value > 64) return fail(GSR_ERR_INVALID_VALUE, "raster_m must be 0..64");
       plan->opt_raster_m = static_cast<int>(value);
+      return ok();
+    case GSR_OPT_RASTER_N:
+      if (value < 0 || value > 64) return fail(GSR_ERR_INVALID_VALUE, "raster_n must be 0..64");
+      plan->opt_raster_n = static_cast<int>(value);
       return ok();
     case GSR_OPT_L2_HINTS:
       if (value < 0 || value > 3) return fail(GSR_ERR_INVALID_VALUE, "l2_hints must be 0..3");

@@ -68,14 +68,27 @@ struct Unit {
 template <int BN, int CG>
 __device__ __forceinline__ void place_tile(const Params& p, Unit& t, uint32_t rank, int mt_begins) {
   // Raster: groups of group_m m-tiles; inside a group the m index runs fastest,
-  // so CTAs working at the same time share W (B) panels and A rows in L2.
-  const int span = p.group_m * p.n_tiles;
-  const int g = t.tile / span;
-  const int first_m = g * p.group_m;
-  const int gm = min(p.m_tiles - first_m, p.group_m);
-  const int in_g = t.tile - g * span;
-  const int mt = first_m + in_g % gm;
-  const int nt = in_g / gm;
+  // so CTAs working at the same time share W (B) panels and A rows in L2. With
+  // group_n > 0 the roles swap: groups of group_n n-tiles, n fastest inside, so
+  // a group's W panels serve every wave of the group.
+  int mt, nt;
+  if (p.group_n > 0) {
+    const int span = p.group_n * p.m_tiles;
+    const int g = t.tile / span;
+    const int first_n = g * p.group_n;
+    const int gn = min(p.n_tiles - first_n, p.group_n);
+    const int in_g = t.tile - g * span;
+    nt = first_n + in_g % gn;
+    mt = in_g / gn;
+  } else {
+    const int span = p.group_m * p.n_tiles;
+    const int g = t.tile / span;
+    const int first_m = g * p.group_m;
+    const int gm = min(p.m_tiles - first_m, p.group_m);
+    const int in_g = t.tile - g * span;
+    mt = first_m + in_g % gm;
+    nt = in_g / gm;
+  }
   t.n0 = nt * BN;
   // This CTA's 128 rows: half-tile h. AG half-tiles are numbered over all
   // shards, each inside one shard, so the two halves of a pair tile may come

@@ -70,6 +70,7 @@ struct Params {  // 128-byte aligned through its CUtensorMap members
   long long sk_iters;           // stream-K: k-blocks of tiles [dp_tiles, tiles)
   int sk_last;                  // stream-K: walk the whole tiles first, the range last
   int group_m;                  // raster group height, in m-tiles (1 = n fastest)
+  int group_n;                  // > 0: raster groups of group_n n-tiles instead, n fastest
   int policy_a;                 // L2 policy of A-operand loads (kPolicy*)
   int policy_b;                 // L2 policy of B-operand loads (kPolicy*)
   int rps;                      // RS: rows per shard = ceil(M/R)

@@ -11,9 +11,9 @@
 // a tile is tile_rows rows of W (output columns; the MMA's M) against all m_pad
 // activation rows (M rounded up to 16; the MMA's N), Y^T[n, m] accumulated in
 // TMEM with TMEM lane = output column and TMEM column = output row. The MMA is
-// always 128 rows tall; with tile_rows < 128 (a multiple of 8, chosen so that N spreads over
-// every pair of SMs) the rows past the tile read stale shared memory into TMEM
-// lanes that are never stored.
+// always 128 rows tall; with tile_rows < 128 (a multiple of 8, chosen so that
+// N spreads over every pair of SMs) the rows past the tile read stale shared
+// memory into TMEM lanes that are never stored.
 //
 // Each tile belongs to a cluster of two CTAs. CTA rank k accumulates the
 // k-blocks of its half of the K range (over every shard's k-blocks, in shard

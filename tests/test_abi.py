@@ -423,3 +423,18 @@ def test_stream_k_range_stays_in_32_bit(lib):
     # an ordinary K keeps its stream-K tail
     d = h.describe(B.MODE_AR, 32768, 7168, 0, [7168])
     assert d["sk_iters"] == 32 * 112 and (d["sk_iters"] + 1) * (74 + 1) < 2 ** 32
+
+
+def test_raster_options_are_validated_and_leave_the_configuration(host):
+    """Raster order (by m-tile groups or by n-tile groups) changes only the
+    order in which tiles are walked: tiles, pieces and grid stay the same."""
+    base = host.describe(B.MODE_AR, 32768, 7168, 0, [896] * 8)
+    for opt, v in ((B.GSR_OPT_RASTER_M, 4), (B.GSR_OPT_RASTER_N, 8), (B.GSR_OPT_RASTER_N, 64)):
+        h = Host(host.lib)
+        B.gemm_shard_plan_set_option(h.plan, opt, v)
+        assert h.describe(B.MODE_AR, 32768, 7168, 0, [896] * 8) == base
+    h = Host(host.lib)
+    for opt in (B.GSR_OPT_RASTER_M, B.GSR_OPT_RASTER_N):
+        for bad in (-1, 65):
+            with pytest.raises(B.GsrError):
+                B.gemm_shard_plan_set_option(h.plan, opt, bad)
