@@ -90,7 +90,12 @@ typedef enum {
                                over the last one or two waves, 3 = stream-K
                                over the partial last wave, each worker's
                                stream-K range before its whole tiles, 4 = as 3
-                               with the whole tiles first                        */
+                               with the whole tiles first, 5 = split tail: each
+                               tile of the partial last wave cut into the same
+                               k-pieces (2 or 3, one per worker, at most as many
+                               pieces as workers), walked before the whole
+                               tiles (the heuristic picks it when the partial
+                               wave is at most half a wave)                      */
     GSR_OPT_SMALL_M = 9,    /* the small-M kernel (AR/RS, M <= 256): 0 = heuristic
                                (used when M <= 256 and no other option above
                                forces a configuration), 1 = never, 2 = whenever
@@ -350,7 +355,8 @@ typedef struct {
     int cta_group;          /* 1: a CTA per 128-row tile; 2: a CTA pair per 256 rows */
     int schedule;           /* 1 = uniform pieces, 2 = stream-K hybrid, 3 = the
                                small-M kernel (block_n W rows per tile, split = 2
-                               halves of K per tile on a cluster of two CTAs)     */
+                               halves of K per tile on a cluster of two CTAs),
+                               4 = split tail (split = pieces per tail tile)      */
     int split;              /* uniform schedule: pieces per tile                    */
     int64_t tiles;          /* output tiles                                         */
     int64_t dp_tiles;       /* stream-K: tiles run whole                            */

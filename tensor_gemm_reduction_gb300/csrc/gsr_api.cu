@@ -311,6 +311,26 @@ Config choose_config(const gemm_shard_plan* P, int mode, int64_t M, int64_t N, i
     c.sched = gsr::kSchedStreamK;
     c.splits = 1;
     const int64_t full = c.tiles / workers, rem = c.tiles % workers;
+    // Split tail instead, when the partial last wave is at most half a wave:
+    // each of its tiles cut into the same 2 or 3 k-pieces, one per worker, so
+    // the workers holding the same piece of neighbouring tiles read the same
+    // k-blocks together (stream-K's ranges start anywhere, share little in L2,
+    // and leave some workers with two cut pieces). AR M = 1000, N = 7168: 36
+    // tail tiles x 2 pieces on 76 pairs.
+    const int64_t tail_split = rem ? std::min<int64_t>({3, workers / rem, c.kb_total}) : 0;
+    const bool split_tail =
+        rem != 0 && (P->opt_schedule == 5 ||
+                     (P->opt_schedule == 0 && tail_split >= 2 && rem * tail_split * 10 >= workers * 6));
+    if (split_tail) {
+      c.sched = gsr::kSchedSplitTail;
+      c.splits = static_cast<int>(std::max<int64_t>(tail_split, 1));
+      c.dp_tiles = full * workers;
+      c.sk_iters = 0;
+      c.sk_last = 0;
+      c.units = c.tiles;
+      c.slots = rem * c.splits;
+      c.ctas = static_cast<int>(c.cta_group * workers);
+    }
     int64_t dp = c.tiles;
     if (rem != 0) {
       if (P->opt_schedule == 2)
@@ -327,13 +347,15 @@ Config choose_config(const gemm_shard_plan* P, int mode, int64_t M, int64_t N, i
       dp = c.tiles;
       sk_iters = 0;
     }
-    c.dp_tiles = dp;
-    c.sk_iters = sk_iters;
-    c.sk_last = P->opt_schedule == 4 ? 1 : 0;
-    c.units = c.tiles;
-    c.slots = sk_iters > 0 ? (c.tiles - dp) + workers - 1 : 0;
-    c.ctas = static_cast<int>(c.cta_group *
-                              (sk_iters > 0 ? workers : std::min<int64_t>(c.tiles, workers)));
+    if (!split_tail) {
+      c.dp_tiles = dp;
+      c.sk_iters = sk_iters;
+      c.sk_last = P->opt_schedule == 4 ? 1 : 0;
+      c.units = c.tiles;
+      c.slots = sk_iters > 0 ? (c.tiles - dp) + workers - 1 : 0;
+      c.ctas = static_cast<int>(c.cta_group *
+                                (sk_iters > 0 ? workers : std::min<int64_t>(c.tiles, workers)));
+    }
   }
   c.ctas = std::max(c.ctas, c.cta_group);
 
@@ -647,7 +669,7 @@ gsr_status gemm_shard_plan_set_option(gemm_shard_plan* plan, gsr_option option, 
       plan->opt_cta_group = static_cast<int>(value);
       return ok();
     case GSR_OPT_SCHEDULE:
-      if (value < 0 || value > 4) return fail(GSR_ERR_INVALID_VALUE, "schedule must be 0..4");
+      if (value < 0 || value > 5) return fail(GSR_ERR_INVALID_VALUE, "schedule must be 0..5");
       plan->opt_schedule = static_cast<int>(value);
       return ok();
     case GSR_OPT_SMALL_M:
@@ -923,10 +945,13 @@ gsr_status gemm_shard_describe(const gemm_shard_plan* P, int mode, int64_t M, in
   const Config c = choose_config(P, mode, M, N, K, R, sizes);
   out->block_n = c.block_n;
   out->cta_group = c.cta_group;
-  out->schedule = c.small ? 3 : c.sched == gsr::kSchedStreamK ? 2 : 1;
+  out->schedule = c.small                               ? 3
+                  : c.sched == gsr::kSchedSplitTail ? 4
+                  : c.sched == gsr::kSchedStreamK   ? 2
+                                                    : 1;
   out->split = c.splits;
   out->tiles = c.tiles;
-  out->dp_tiles = c.sched == gsr::kSchedStreamK ? c.dp_tiles : c.tiles;
+  out->dp_tiles = (c.sched == gsr::kSchedStreamK || c.sched == gsr::kSchedSplitTail) ? c.dp_tiles : c.tiles;
   out->sk_iters = c.sk_iters;
   out->ctas = c.ctas;
   out->workspace_bytes = c.ws_bytes;

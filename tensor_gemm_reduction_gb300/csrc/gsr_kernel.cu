@@ -128,9 +128,16 @@ __device__ __forceinline__ Sched sched_begin(const Params& p) {
   s.w = static_cast<int>(blockIdx.x) / CG;
   s.G = static_cast<int>(gridDim.x) / CG;
   s.next = s.w;
-  const uint32_t I = static_cast<uint32_t>(p.sk_iters), G = static_cast<uint32_t>(s.G);
-  s.it = static_cast<uint32_t>(s.w) * I / G;
-  s.it_end = static_cast<uint32_t>(s.w + 1) * I / G;
+  if (p.sched == kSchedSplitTail) {
+    // One piece of the tail for each of the first (tail tiles x splits) workers.
+    const int pieces = (p.tiles - p.dp_tiles) * p.splits;
+    s.it = s.w < pieces ? static_cast<uint32_t>(s.w) : 0u;
+    s.it_end = s.w < pieces ? s.it + 1u : 0u;
+  } else {
+    const uint32_t I = static_cast<uint32_t>(p.sk_iters), G = static_cast<uint32_t>(s.G);
+    s.it = static_cast<uint32_t>(s.w) * I / G;
+    s.it_end = static_cast<uint32_t>(s.w + 1) * I / G;
+  }
   const int lane = static_cast<int>(threadIdx.x) & 31;
   s.mt_begins = p.shard_mt_begin[lane <= kMaxShards ? lane : kMaxShards];
   return s;
@@ -152,6 +159,23 @@ __device__ __forceinline__ bool sched_next(const Params& p, Sched& s, Unit& t, u
     t.piece = u - t.tile * p.splits;
     t.npieces = p.splits;
     t.slot0 = t.tile * p.splits;
+    t.kb_begin = t.piece * p.kb_total / p.splits;
+    t.kb_end = (t.piece + 1) * p.kb_total / p.splits;
+    place_tile<BN, CG>(p, t, rank, s.mt_begins);
+    return true;
+  }
+  if (p.sched == kSchedSplitTail && s.it < s.it_end) {
+    // This worker's piece of the tail, first: piece u / tail of tile
+    // dp + u % tail, so the workers holding piece j of the tail tiles run side
+    // by side over the same k-blocks and share those tiles' A rows and W
+    // columns in L2 (stream-K's ranges start anywhere and share little).
+    const int tail = p.tiles - p.dp_tiles, u = static_cast<int>(s.it);
+    s.it = s.it_end;
+    const int tt = u % tail;
+    t.tile = p.dp_tiles + tt;
+    t.piece = u / tail;
+    t.npieces = p.splits;
+    t.slot0 = tt * p.splits;
     t.kb_begin = t.piece * p.kb_total / p.splits;
     t.kb_end = (t.piece + 1) * p.kb_total / p.splits;
     place_tile<BN, CG>(p, t, rank, s.mt_begins);

@@ -24,7 +24,7 @@ enum Mode : int { kModeAR = 0, kModeRS = 1, kModeAG = 2, kModeARRep = 3 };
 // K-pair (small-M kernel): each output tile is computed by the two CTAs of a
 // cluster, each over half of the k-blocks, and the two halves are added in
 // distributed shared memory.
-enum Sched : int { kSchedUniform = 0, kSchedStreamK = 1, kSchedKPair = 2 };
+enum Sched : int { kSchedUniform = 0, kSchedStreamK = 1, kSchedKPair = 2, kSchedSplitTail = 3 };
 
 // L2 eviction priority requested for an operand's TMA loads.
 enum Policy : int { kPolicyNormal = 0, kPolicyEvictFirst = 1, kPolicyEvictLast = 2 };
@@ -65,7 +65,7 @@ struct Params {  // 128-byte aligned through its CUtensorMap members
   int kb_total;                 // k-blocks per tile (AR/RS: sum_r ceil(K_r/BK))
   int splits;                   // uniform schedule: pieces per tile (1 = none)
   int units;                    // uniform schedule: tiles * splits
-  int sched;                    // kSchedUniform or kSchedStreamK
+  int sched;                    // kSchedUniform, kSchedStreamK or kSchedSplitTail
   int dp_tiles;                 // stream-K: tiles [0, dp_tiles) run whole, round-robin
   long long sk_iters;           // stream-K: k-blocks of tiles [dp_tiles, tiles)
   int sk_last;                  // stream-K: walk the whole tiles first, the range last

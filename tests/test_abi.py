@@ -286,10 +286,16 @@ def test_uniform_schedule_splits_small_m(lib):
 
 def test_large_m_uses_cta_pairs_and_a_stream_k_tail(host):
     # 256 x 256 tiles per CTA pair: 128 x 28 = 3584 tiles on 74 pairs is 48.4
-    # waves; the partial last wave (32 tiles) is shared out k-block by k-block
+    # waves; the partial last wave (32 tiles, under half a wave) is cut into two
+    # k-pieces per tile, one per worker (split tail)
     d = host.describe(B.MODE_AR, 32768, 7168, 0, [896] * 8)
-    assert d["cta_group"] == 2 and d["schedule"] == 2 and d["ctas"] == 148
-    assert d["tiles"] == 3584 and d["dp_tiles"] == 48 * 74 and d["sk_iters"] == 32 * 112
+    assert d["cta_group"] == 2 and d["schedule"] == 4 and d["ctas"] == 148
+    assert d["tiles"] == 3584 and d["dp_tiles"] == 48 * 74 and d["split"] == 2 and d["sk_iters"] == 0
+    # or shared out k-block by k-block (stream-K over the partial last wave)
+    plan3 = B.gemm_shard_plan_create_host(148, 32768, 8192, 8192, 16)
+    B.gemm_shard_plan_set_option(plan3, B.GSR_OPT_SCHEDULE, 3)
+    d = B.gemm_shard_describe(plan3, B.MODE_AR, 32768, 7168, 0, [896] * 8)
+    assert d["schedule"] == 2 and d["dp_tiles"] == 48 * 74 and d["sk_iters"] == 32 * 112
     plan2 = B.gemm_shard_plan_create_host(148, 32768, 8192, 8192, 16)
     B.gemm_shard_plan_set_option(plan2, B.GSR_OPT_SCHEDULE, 2)   # the last 1.4 waves
     d = B.gemm_shard_describe(plan2, B.MODE_AR, 32768, 7168, 0, [896] * 8)
@@ -333,7 +339,7 @@ def test_forced_options(lib):
     d = h.describe(B.MODE_AR, 64, 256, 0, [64])
     assert d["split"] == 1
     for opt, bad in ((B.GSR_OPT_SPLIT_K, 17), (B.GSR_OPT_BLOCK_N, 64), (B.GSR_OPT_TIMEOUT_NS, -1),
-                     (B.GSR_OPT_MAX_CTAS, -5), (B.GSR_OPT_SCHEDULE, 5), (B.GSR_OPT_CTA_GROUP, 3),
+                     (B.GSR_OPT_MAX_CTAS, -5), (B.GSR_OPT_SCHEDULE, 6), (B.GSR_OPT_CTA_GROUP, 3),
                      (99, 1)):
         with pytest.raises(B.GsrError) as e:
             B.gemm_shard_plan_set_option(h.plan, opt, bad)
@@ -418,11 +424,17 @@ def test_stream_k_range_stays_in_32_bit(lib):
     (sk_iters + 1) * (workers + 1) >= 2^32 runs as whole tiles instead."""
     K = (1 << 31) - 128
     h = Host(lib, max_M=32768, max_N=8192, max_K=K, max_R=1)
+    B.gemm_shard_plan_set_option(h.plan, B.GSR_OPT_SCHEDULE, 3)   # stream-K tail
     d = h.describe(B.MODE_AR, 32768, 7168, 0, [K])
     assert d["cta_group"] == 2 and d["sk_iters"] == 0 and d["dp_tiles"] == d["tiles"]
     # an ordinary K keeps its stream-K tail
     d = h.describe(B.MODE_AR, 32768, 7168, 0, [7168])
     assert d["sk_iters"] == 32 * 112 and (d["sk_iters"] + 1) * (74 + 1) < 2 ** 32
+    # the split tail (the default here) cuts each tail tile into k-pieces with
+    # plain 32-bit products (at most 3 x 2^25 k-blocks)
+    h2 = Host(lib, max_M=32768, max_N=8192, max_K=K, max_R=1)
+    d = h2.describe(B.MODE_AR, 32768, 7168, 0, [K])
+    assert d["schedule"] == 4 and d["split"] == 2 and d["dp_tiles"] == 48 * 74
 
 
 def test_raster_options_are_validated_and_leave_the_configuration(host):
@@ -459,3 +471,17 @@ def test_192_column_tiles_only_where_they_fill_few_whole_waves(host):
     B.gemm_shard_plan_set_option(h2.plan, B.GSR_OPT_BLOCK_N, 256)
     assert h2.describe(B.MODE_AG, 0, 3648, 7168, [256] * 8)["block_n"] == 256
     assert host.describe(B.MODE_AG, 0, 3648, 7168, [256] * 8)["block_n"] == 256   # 148 SMs
+
+
+def test_split_tail_where_the_partial_wave_is_at_most_half(lib):
+    """On 152 SMs (76 pairs): AR M = 1000 (112 tiles: one wave plus 36) cuts
+    each of the 36 tail tiles into two k-pieces on 72 workers; the headline
+    shapes (partial waves of 8 and 12 tiles) keep the stream-K tail."""
+    h = Host(lib, sm=152, max_M=34816)
+    d = h.describe(B.MODE_AR, 1000, 7168, 0, [896] * 8)
+    assert (d["schedule"], d["split"], d["tiles"], d["dp_tiles"], d["ctas"]) == (4, 2, 112, 76, 152)
+    assert h.describe(B.MODE_RS, 1000, 7168, 0, [896] * 8) == d
+    assert h.describe(B.MODE_AG, 0, 6288, 7168, [4096] * 8)["schedule"] == 2
+    assert h.describe(B.MODE_AR, 32768, 7168, 0, [896] * 8)["schedule"] == 2
+    # whole waves need no tail at all
+    assert h.describe(B.MODE_AR, 2048, 4864, 0, [896] * 8)["sk_iters"] == 0

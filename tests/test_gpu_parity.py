@@ -31,6 +31,7 @@ VARIANTS = {
     "pairsk8last": dict(cta_group=2, schedule=4, max_ctas=8),
     "pairsplit": dict(max_M=4096, max_N=8192, max_K=8192, max_R=16, cta_group=2, split_k=3),
     "rastern": dict(raster_n=3),
+    "splittail": dict(cta_group=2, schedule=5, max_ctas=16),
 }
 
 
