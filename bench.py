@@ -32,6 +32,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "BF16 TFLOP/s per mode vs M on 1 GB300; % of dense BF16 peak; oracle time"
+ROW_PAUSE_S = 0.3   # idle pause before each per-workload row (see sweep)
 L2_BYTES = 126 * 1024 * 1024
 
 
@@ -327,7 +328,10 @@ def run_reference(args, w):
 
 def sweep(plan, ws, dev, pk, names):
     """Per-workload kernel time with an L2 flush before every launch: the
-    trimmed mean of 20 launches."""
+    trimmed mean of 20 launches. Each row starts after a short idle pause, so
+    that a short kernel is not timed while the GPU is still held at the power
+    limit by the previous row (after the M = 32768 rows the SM clock stays near
+    1.4 GHz for a while, which slowed the next mid-M rows by up to 25 %)."""
     import torch
     from tensor_gemm_reduction_gb300 import inputs as gi
     flush_buf = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
@@ -339,6 +343,8 @@ def sweep(plan, ws, dev, pk, names):
             r = Runner(w, plan, ws, dev)
         except torch.OutOfMemoryError:
             continue
+        torch.cuda.synchronize()
+        time.sleep(ROW_PAUSE_S)
         times, _ = time_launches(r, steps=20, warmup=3, flush=lambda: flush_buf.fill_(1))
         t = trimmed_mean(times) * 1e-3
         t_roof = max(w.flops / (pk["bf16_burst"] * 1e12), w.bytes / (pk["hbm_gbs"] * 1e9))
@@ -366,6 +372,8 @@ def sweep_pack(plan, ws, dev, pk):
     S = gi.gaussian_states([w.M_r] * w.R, w.T, w.H, seed=w.seed, device=dev)
     P = torch.empty(w.rows_out, w.T * w.H, dtype=torch.bfloat16, device=dev)
     call = B.prepare_pack_gather(plan, S, w.rows_out, P, ws)
+    torch.cuda.synchronize()
+    time.sleep(ROW_PAUSE_S)
     times, _ = time_launches(call, steps=20, warmup=3, flush=lambda: flush_buf.fill_(1))
     B.gemm_shard_check_status(plan, ws)
     t = trimmed_mean(times) * 1e-3
