@@ -339,10 +339,14 @@ Config choose_config(const gemm_shard_plan* P, int mode, int64_t M, int64_t N, i
         dp = full * workers;                          // only the partial last wave
     }
     int64_t sk_iters = (c.tiles - dp) * c.kb_total;
-    // Too little to share out, or too much for the kernel's 32-bit stream-K
-    // arithmetic ((sk_iters + 1) * (workers + 1) must stay below 2^32): whole
-    // tiles only.
-    if ((sk_iters > 0 && sk_iters < 4 * workers) ||
+    // Whole tiles only when: the partial last wave is nearly full (at least
+    // 85 % of the workers: sharing it out saves under 15 % of a tile, less
+    // than the cut tiles' pieces cost; measured at AR M = 4096 and AG KDA
+    // M = 3072, 2.5 % and 4 % faster; at 63 % stream-K still won by 2 %),
+    // there is too little to share out, or too much for the kernel's 32-bit
+    // stream-K arithmetic ((sk_iters + 1) * (workers + 1) must stay below 2^32).
+    const bool nearly_full = P->opt_schedule == 0 && rem * 20 >= workers * 17;
+    if (nearly_full || (sk_iters > 0 && sk_iters < 4 * workers) ||
         (sk_iters + 1) * (workers + 1) >= (int64_t(1) << 32)) {
       dp = c.tiles;
       sk_iters = 0;

@@ -485,3 +485,20 @@ def test_split_tail_where_the_partial_wave_is_at_most_half(lib):
     assert h.describe(B.MODE_AR, 32768, 7168, 0, [896] * 8)["schedule"] == 2
     # whole waves need no tail at all
     assert h.describe(B.MODE_AR, 2048, 4864, 0, [896] * 8)["sk_iters"] == 0
+
+
+def test_nearly_full_partial_wave_runs_whole_tiles(lib):
+    """On 152 SMs (76 pairs): a partial last wave of at least 85 % of the
+    workers runs as whole tiles (AR M = 4096: 448 tiles, 68 in the last wave;
+    AG KDA M = 3072: 300 tiles, 72), a fuller share-out stays stream-K (AG KDA
+    M = 2048: 48 of 76), and an explicit schedule still gets stream-K."""
+    h = Host(lib, sm=152, max_M=34816)
+    d = h.describe(B.MODE_AR, 4096, 7168, 0, [896] * 8)
+    assert (d["tiles"], d["dp_tiles"], d["sk_iters"], d["ctas"]) == (448, 448, 0, 152)
+    d = h.describe(B.MODE_AG, 0, 6288, 7168, [384] * 8)
+    assert (d["tiles"], d["dp_tiles"], d["sk_iters"]) == (300, 300, 0)
+    d = h.describe(B.MODE_AG, 0, 6288, 7168, [256] * 8)
+    assert d["schedule"] == 2 and d["sk_iters"] == 48 * 112
+    h3 = Host(lib, sm=152, max_M=34816)
+    B.gemm_shard_plan_set_option(h3.plan, B.GSR_OPT_SCHEDULE, 3)
+    assert h3.describe(B.MODE_AR, 4096, 7168, 0, [896] * 8)["sk_iters"] == 68 * 112

@@ -61,17 +61,17 @@ def test_noalloc_rejects_oversized_scratch(setup):
 
 
 def test_noalloc_falls_back_when_the_heuristic_needs_more_scratch(setup):
-    """M=2048, N=7168: the plan's stream-K configuration (224 pair tiles on 76
-    pairs, a 72-tile partial wave) needs more scratch than the built-in array
+    """M=2560, N=7168: the plan's stream-K configuration (280 pair tiles on 76
+    pairs, a 52-tile partial wave) needs more scratch than the built-in array
     holds, so the call runs the uniform schedule; results agree with gemm_ar
     within the test tolerance, on two calls in a row."""
     plan, ws = setup
-    d = B.gemm_shard_describe(plan, B.MODE_AR, 2048, 7168, 0, [896] * 8)
-    assert d["workspace_bytes"] > 24 << 20
+    d = B.gemm_shard_describe(plan, B.MODE_AR, 2560, 7168, 0, [896] * 8)
+    assert d["schedule"] == 2 and d["workspace_bytes"] > 24 << 20
     for seed in (31, 32):
-        X, W = _device_inputs(2048, 7168, [896] * 8, seed)
-        y_ref = torch.empty(2048, 7168, dtype=torch.bfloat16, device="cuda:0")
-        y_new = torch.full((2048, 7168), float("nan"), dtype=torch.bfloat16, device="cuda:0")
+        X, W = _device_inputs(2560, 7168, [896] * 8, seed)
+        y_ref = torch.empty(2560, 7168, dtype=torch.bfloat16, device="cuda:0")
+        y_new = torch.full((2560, 7168), float("nan"), dtype=torch.bfloat16, device="cuda:0")
         B.gemm_ar(plan, X, W, y_ref, ws)
         B.gemm_ar_noalloc(plan, X, W, y_new)
         torch.cuda.synchronize()
