@@ -6,6 +6,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 import torch
 
@@ -502,3 +503,33 @@ def test_nearly_full_partial_wave_runs_whole_tiles(lib):
     h3 = Host(lib, sm=152, max_M=34816)
     B.gemm_shard_plan_set_option(h3.plan, B.GSR_OPT_SCHEDULE, 3)
     assert h3.describe(B.MODE_AR, 4096, 7168, 0, [896] * 8)["sk_iters"] == 68 * 112
+
+
+@pytest.mark.parametrize("sm", [16, 148, 152])
+@pytest.mark.parametrize("schedule", [0, 2, 3, 4, 5])
+def test_workspace_and_schedule_invariants_over_shapes(lib, sm, schedule):
+    """Every configuration, heuristic or forced, fits the plan's workspace; a
+    split tail hands out at most one piece per worker, every piece at least
+    one k-block; whole-tile runs need no partial slots."""
+    h = Host(lib, sm=sm, max_M=34816)
+    if schedule:
+        B.gemm_shard_plan_set_option(h.plan, B.GSR_OPT_SCHEDULE, schedule)
+    rng = np.random.default_rng(100 * sm + schedule)
+    shapes = [(1000, 7168, [896] * 8), (4096, 7168, [896] * 8), (2048, 3648, [896] * 8),
+              (32768, 7168, [896] * 8), (3584, 6288, [7168])]
+    for _ in range(40):
+        M = int(rng.integers(1, 34817))
+        N = int(rng.integers(1, 1025)) * 8
+        R = int(rng.integers(1, 17))
+        shapes.append((M, N, [int(rng.integers(1, 129)) * 8 for _ in range(R)]))
+    for M, N, K_r in shapes:
+        d = h.describe(B.MODE_AR, M, N, 0, K_r)
+        assert d["workspace_bytes"] <= h.ws_bytes, (M, N, K_r)
+        assert 1 <= d["ctas"] <= sm
+        kb = sum((k + 63) // 64 for k in K_r)
+        workers = d["ctas"] // d["cta_group"]
+        if d["schedule"] == 4:
+            tail = d["tiles"] - d["dp_tiles"]
+            assert 0 < tail * d["split"] <= workers and 1 <= d["split"] <= min(3, kb), (M, N, K_r, d)
+        if d["schedule"] in (2, 4) and d["dp_tiles"] == d["tiles"]:
+            assert d["sk_iters"] == 0
