@@ -164,53 +164,136 @@ struct Config {
 // Kernel configuration: a function of the shape (rows, N, per-shard sizes, R)
 // and the device, never of the mode, so AR and RS on the same inputs run the
 // same tiles, the same pieces and the same summation order (bit-identical rows).
+// Three steps: the small-M kernel if it applies (small_m_config), else the main
+// kernel's tile shape (choose_config itself) and its work schedule
+// (uniform_schedule or tail_schedule).
+
+// Small M (AR/RS, a decode-like batch of at most 256 rows): streaming W is
+// the whole cost, so the small-M kernel runs every activation row against
+// tiles of W rows, each tile split over K between the two CTAs of a cluster.
+// The tile height is the smallest multiple of 8 (up to 128) that covers N
+// with every cluster in the fewest waves, so that all SMs stream W (N = 7168
+// on 76 clusters: 96 rows, 75 tiles). Returns false when the kernel does not
+// apply (or an option forces the main kernel).
+bool small_m_config(const gemm_shard_plan* P, int mode, int64_t M, int64_t N, int R,
+                    const int64_t* sizes, Config& c) {
+  if (mode == gsr::kModeAG || M < 1 || M > gsr::kSmallMaxM || P->opt_small == 1) return false;
+  int64_t kb = 0;
+  for (int r = 0; r < R; ++r) kb += cdiv(sizes[r], BK);
+  const bool forced = P->opt_split || P->opt_block_n || P->opt_cta_group || P->opt_schedule;
+  if (kb < 2 || (P->opt_small != 2 && forced)) return false;
+  c.small = 1;
+  c.m_pad = static_cast<int>(std::max<int64_t>(16, cdiv(M, 16) * 16));
+  c.stages = gsr::small_stages(c.m_pad);
+  const int cap = P->opt_max_ctas ? std::min(P->opt_max_ctas, P->sm_count) : P->sm_count;
+  const int64_t clusters = std::max(cap / 2, 1);
+  int64_t rows = P->opt_small_rows;
+  if (!rows) {
+    const int64_t waves = cdiv(N, gsr::kSmallTileN * clusters);
+    rows = std::min<int64_t>(gsr::kSmallTileN, cdiv(cdiv(N, waves * clusters), 8) * 8);
+  }
+  c.block_n = static_cast<int>(rows);
+  c.cta_group = 1;
+  c.sched = gsr::kSchedKPair;
+  c.splits = 2;
+  c.kb_total = kb;
+  c.m_tiles = 1;
+  c.n_tiles = cdiv(N, rows);
+  c.tiles = c.n_tiles;
+  c.units = 2 * c.tiles;
+  c.ctas = static_cast<int>(2 * std::min<int64_t>(c.tiles, clusters));
+  // Every cluster reads all of X and a disjoint slice of W.
+  const int hints = P->opt_l2_hints;
+  c.policy_a = (hints == 0 || hints == 2) ? gsr::kPolicyEvictLast
+               : hints == 3               ? gsr::kPolicyEvictFirst
+                                          : gsr::kPolicyNormal;
+  c.policy_b = (hints == 0 || hints == 2) ? gsr::kPolicyEvictFirst
+               : hints == 3               ? gsr::kPolicyEvictLast
+                                          : gsr::kPolicyNormal;
+  c.ws_bytes = gsr::kWsHeader + counters_bytes(P);
+  return true;
+}
+
+// Uniform schedule: every tile cut into the same number of pieces, dealt
+// round-robin (the default with fewer single-CTA tiles than SMs).
+void uniform_schedule(const gemm_shard_plan* P, int64_t workers, Config& c) {
+  c.sched = gsr::kSchedUniform;
+  if (P->opt_split) {
+    c.splits = static_cast<int>(std::min<int64_t>(P->opt_split, c.kb_total));
+  } else if (c.tiles >= workers) {
+    c.splits = 1;
+  } else {
+    int64_t sp = workers / std::max<int64_t>(c.tiles, 1);
+    sp = std::min<int64_t>(sp, std::max<int64_t>(c.kb_total / 4, 1));
+    c.splits = static_cast<int>(std::max<int64_t>(std::min<int64_t>(sp, 16), 1));
+  }
+  c.units = c.tiles * c.splits;
+  c.dp_tiles = 0;
+  c.sk_iters = 0;
+  c.slots = c.splits > 1 ? c.units : 0;
+  c.ctas = static_cast<int>(c.cta_group * std::min<int64_t>(c.units, workers));
+}
+
+// Whole tiles for every full wave, and for the partial last wave one of:
+//  - a split tail, when it is at most half a wave: each of its tiles cut into
+//    the same 2 or 3 k-pieces, one per worker, so the workers holding the same
+//    piece of neighbouring tiles read the same k-blocks together (stream-K's
+//    ranges start anywhere, share little in L2, and leave some workers with
+//    two cut pieces). AR M = 1000, N = 7168: 36 tail tiles x 2 pieces on 76
+//    pairs;
+//  - whole tiles, when it is nearly full (at least 85 % of the workers:
+//    sharing it out saves under 15 % of a tile, less than the cut tiles'
+//    pieces cost; measured at AR M = 4096 and AG KDA M = 3072, 2.5 % and 4 %
+//    faster; at 63 % stream-K still won by 2 %), when there is too little to
+//    share out, or too much for the kernel's 32-bit stream-K arithmetic
+//    ((sk_iters + 1) * (workers + 1) must stay below 2^32);
+//  - otherwise stream-K: its k-blocks cut evenly over every worker (schedule 2
+//    shares out the last one or two waves instead).
+void tail_schedule(const gemm_shard_plan* P, int64_t workers, Config& c) {
+  const int64_t full = c.tiles / workers, rem = c.tiles % workers;
+  c.splits = 1;
+  c.units = c.tiles;
+  c.sk_last = 0;
+  const int64_t tail_split = rem ? std::min<int64_t>({3, workers / rem, c.kb_total}) : 0;
+  const bool split_tail =
+      rem != 0 && (P->opt_schedule == 5 ||
+                   (P->opt_schedule == 0 && tail_split >= 2 && rem * tail_split * 10 >= workers * 6));
+  if (split_tail) {
+    c.sched = gsr::kSchedSplitTail;
+    c.splits = static_cast<int>(std::max<int64_t>(tail_split, 1));
+    c.dp_tiles = full * workers;
+    c.sk_iters = 0;
+    c.slots = rem * c.splits;
+    c.ctas = static_cast<int>(c.cta_group * workers);
+    return;
+  }
+  c.sched = gsr::kSchedStreamK;
+  int64_t dp = c.tiles;
+  if (rem != 0) {
+    if (P->opt_schedule == 2)
+      dp = full >= 2 ? (full - 1) * workers : 0;    // the last one or two waves
+    else                                            // 0, 3, 4
+      dp = full * workers;                          // only the partial last wave
+  }
+  int64_t sk_iters = (c.tiles - dp) * c.kb_total;
+  const bool nearly_full = P->opt_schedule == 0 && rem * 20 >= workers * 17;
+  if (nearly_full || (sk_iters > 0 && sk_iters < 4 * workers) ||
+      (sk_iters + 1) * (workers + 1) >= (int64_t(1) << 32)) {
+    dp = c.tiles;
+    sk_iters = 0;
+  }
+  c.dp_tiles = dp;
+  c.sk_iters = sk_iters;
+  c.sk_last = P->opt_schedule == 4 ? 1 : 0;
+  c.slots = sk_iters > 0 ? (c.tiles - dp) + workers - 1 : 0;
+  c.ctas = static_cast<int>(c.cta_group *
+                            (sk_iters > 0 ? workers : std::min<int64_t>(c.tiles, workers)));
+}
+
 Config choose_config(const gemm_shard_plan* P, int mode, int64_t M, int64_t N, int64_t K_ag, int R,
                      const int64_t* sizes) {
   Config c;
-  // Small M (AR/RS, a decode-like batch of at most 256 rows): streaming W is
-  // the whole cost, so the small-M kernel runs every activation row against
-  // tiles of W rows, each tile split over K between the two CTAs of a cluster.
-  // The tile height is the smallest multiple of 8 (up to 128) that covers N
-  // with every cluster in the fewest waves, so that all SMs stream W (N = 7168
-  // on 76 clusters: 96 rows, 75 tiles). Like every choice here it depends on
-  // the shape, not on the mode.
-  if (mode != gsr::kModeAG && M >= 1 && M <= gsr::kSmallMaxM && P->opt_small != 1) {
-    int64_t kb = 0;
-    for (int r = 0; r < R; ++r) kb += cdiv(sizes[r], BK);
-    const bool forced = P->opt_split || P->opt_block_n || P->opt_cta_group || P->opt_schedule;
-    if (kb >= 2 && (P->opt_small == 2 || !forced)) {
-      c.small = 1;
-      c.m_pad = static_cast<int>(std::max<int64_t>(16, cdiv(M, 16) * 16));
-      c.stages = gsr::small_stages(c.m_pad);
-      const int cap = P->opt_max_ctas ? std::min(P->opt_max_ctas, P->sm_count) : P->sm_count;
-      const int64_t clusters = std::max(cap / 2, 1);
-      int64_t rows = P->opt_small_rows;
-      if (!rows) {
-        const int64_t waves = cdiv(N, gsr::kSmallTileN * clusters);
-        rows = std::min<int64_t>(gsr::kSmallTileN, cdiv(cdiv(N, waves * clusters), 8) * 8);
-      }
-      c.block_n = static_cast<int>(rows);
-      c.cta_group = 1;
-      c.sched = gsr::kSchedKPair;
-      c.splits = 2;
-      c.kb_total = kb;
-      c.m_tiles = 1;
-      c.n_tiles = cdiv(N, rows);
-      c.tiles = c.n_tiles;
-      c.units = 2 * c.tiles;
-      c.ctas = static_cast<int>(2 * std::min<int64_t>(c.tiles, clusters));
-      // Every cluster reads all of X and a disjoint slice of W.
-      const int hints = P->opt_l2_hints;
-      c.policy_a = (hints == 0 || hints == 2) ? gsr::kPolicyEvictLast
-                   : hints == 3               ? gsr::kPolicyEvictFirst
-                                              : gsr::kPolicyNormal;
-      c.policy_b = (hints == 0 || hints == 2) ? gsr::kPolicyEvictFirst
-                   : hints == 3               ? gsr::kPolicyEvictLast
-                                              : gsr::kPolicyNormal;
-      c.ws_bytes = gsr::kWsHeader + counters_bytes(P);
-      return c;
-    }
-  }
+  if (small_m_config(P, mode, M, N, R, sizes, c)) return c;
   c.block_n = P->opt_block_n ? P->opt_block_n : (N <= 128 ? 128 : 256);
   // Tile rows: 128 per CTA; a CTA pair (cta_group 2) covers 256. AG tiles never
   // cross a shard.
@@ -286,81 +369,10 @@ Config choose_config(const gemm_shard_plan* P, int mode, int64_t M, int64_t N, i
     }
   }
 
-  if (P->opt_split || P->opt_schedule == 1 || (P->opt_schedule == 0 && small)) {
-    // Uniform schedule: every tile cut into the same number of pieces.
-    c.sched = gsr::kSchedUniform;
-    if (P->opt_split) {
-      c.splits = static_cast<int>(std::min<int64_t>(P->opt_split, c.kb_total));
-    } else if (c.tiles >= workers) {
-      c.splits = 1;
-    } else {
-      int64_t sp = workers / std::max<int64_t>(c.tiles, 1);
-      sp = std::min<int64_t>(sp, std::max<int64_t>(c.kb_total / 4, 1));
-      c.splits = static_cast<int>(std::max<int64_t>(std::min<int64_t>(sp, 16), 1));
-    }
-    c.units = c.tiles * c.splits;
-    c.dp_tiles = 0;
-    c.sk_iters = 0;
-    c.slots = c.splits > 1 ? c.units : 0;
-    c.ctas = static_cast<int>(c.cta_group * std::min<int64_t>(c.units, workers));
-  } else {
-    // Stream-K hybrid: whole tiles for every full wave, then the k-blocks of
-    // the partial last wave cut evenly over every worker (schedule 2 shares
-    // out the last one or two waves instead). Fewer cut tiles mean fewer
-    // partial tiles to publish and sum.
-    c.sched = gsr::kSchedStreamK;
-    c.splits = 1;
-    const int64_t full = c.tiles / workers, rem = c.tiles % workers;
-    // Split tail instead, when the partial last wave is at most half a wave:
-    // each of its tiles cut into the same 2 or 3 k-pieces, one per worker, so
-    // the workers holding the same piece of neighbouring tiles read the same
-    // k-blocks together (stream-K's ranges start anywhere, share little in L2,
-    // and leave some workers with two cut pieces). AR M = 1000, N = 7168: 36
-    // tail tiles x 2 pieces on 76 pairs.
-    const int64_t tail_split = rem ? std::min<int64_t>({3, workers / rem, c.kb_total}) : 0;
-    const bool split_tail =
-        rem != 0 && (P->opt_schedule == 5 ||
-                     (P->opt_schedule == 0 && tail_split >= 2 && rem * tail_split * 10 >= workers * 6));
-    if (split_tail) {
-      c.sched = gsr::kSchedSplitTail;
-      c.splits = static_cast<int>(std::max<int64_t>(tail_split, 1));
-      c.dp_tiles = full * workers;
-      c.sk_iters = 0;
-      c.sk_last = 0;
-      c.units = c.tiles;
-      c.slots = rem * c.splits;
-      c.ctas = static_cast<int>(c.cta_group * workers);
-    }
-    int64_t dp = c.tiles;
-    if (rem != 0) {
-      if (P->opt_schedule == 2)
-        dp = full >= 2 ? (full - 1) * workers : 0;    // the last one or two waves
-      else                                            // 0, 3, 4
-        dp = full * workers;                          // only the partial last wave
-    }
-    int64_t sk_iters = (c.tiles - dp) * c.kb_total;
-    // Whole tiles only when: the partial last wave is nearly full (at least
-    // 85 % of the workers: sharing it out saves under 15 % of a tile, less
-    // than the cut tiles' pieces cost; measured at AR M = 4096 and AG KDA
-    // M = 3072, 2.5 % and 4 % faster; at 63 % stream-K still won by 2 %),
-    // there is too little to share out, or too much for the kernel's 32-bit
-    // stream-K arithmetic ((sk_iters + 1) * (workers + 1) must stay below 2^32).
-    const bool nearly_full = P->opt_schedule == 0 && rem * 20 >= workers * 17;
-    if (nearly_full || (sk_iters > 0 && sk_iters < 4 * workers) ||
-        (sk_iters + 1) * (workers + 1) >= (int64_t(1) << 32)) {
-      dp = c.tiles;
-      sk_iters = 0;
-    }
-    if (!split_tail) {
-      c.dp_tiles = dp;
-      c.sk_iters = sk_iters;
-      c.sk_last = P->opt_schedule == 4 ? 1 : 0;
-      c.units = c.tiles;
-      c.slots = sk_iters > 0 ? (c.tiles - dp) + workers - 1 : 0;
-      c.ctas = static_cast<int>(c.cta_group *
-                                (sk_iters > 0 ? workers : std::min<int64_t>(c.tiles, workers)));
-    }
-  }
+  if (P->opt_split || P->opt_schedule == 1 || (P->opt_schedule == 0 && small))
+    uniform_schedule(P, workers, c);
+  else
+    tail_schedule(P, workers, c);
   c.ctas = std::max(c.ctas, c.cta_group);
 
   // Raster: groups of group_m m-tiles, m fastest inside a group, so a wave of
