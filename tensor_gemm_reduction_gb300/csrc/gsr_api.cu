@@ -168,6 +168,20 @@ struct Config {
 // kernel's tile shape (choose_config itself) and its work schedule
 // (uniform_schedule or tail_schedule).
 
+// AG row granule: 128 rows (one per CTA tile), or 64 rows (two per CTA tile,
+// possibly from neighbouring shards) when that needs fewer CTA tiles, i.e.
+// when shards are multiples of 64 but not of 128 rows (448-row shards: 28
+// CTA tiles of rows for 8 shards instead of 32). A function of the shard
+// sizes only.
+int ag_granule(int R, const int64_t* M_r) {
+  int64_t g128 = 0, g64 = 0;
+  for (int r = 0; r < R; ++r) {
+    g128 += cdiv(M_r[r], 128);
+    g64 += cdiv(M_r[r], 64);
+  }
+  return cdiv(g64, 2) < g128 ? 64 : 128;
+}
+
 // Small M (AR/RS, a decode-like batch of at most 256 rows): streaming W is
 // the whole cost, so the small-M kernel runs every activation row against
 // tiles of W rows, each tile split over K between the two CTAs of a cluster.
@@ -302,7 +316,9 @@ Config choose_config(const gemm_shard_plan* P, int mode, int64_t M, int64_t N, i
   auto count_m_tiles = [&](int64_t cg) {
     int64_t halves = 0;
     if (mode == gsr::kModeAG) {
-      for (int r = 0; r < R; ++r) halves += cdiv(sizes[r], BM);
+      const int gran = ag_granule(R, sizes);
+      for (int r = 0; r < R; ++r) halves += cdiv(sizes[r], gran);
+      halves = cdiv(halves, BM / gran);
     } else {
       halves = cdiv(M, BM);
     }
@@ -452,6 +468,7 @@ void fill_common(gsr::Params& p, const gemm_shard_plan* P, const Config& c, int 
   p.m_pad = c.m_pad;
   p.stages = c.stages;
   p.tile_rows = c.small ? c.block_n : 0;
+  p.ag_gran = BM;   // AG sets its own
   p.timeout_ns = P->timeout_ns;
   uint8_t* w = static_cast<uint8_t*>(ws);
   p.status = reinterpret_cast<uint32_t*>(w);
@@ -805,15 +822,16 @@ static gsr_status run_ag(const gemm_shard_plan* P, int64_t N, int64_t K, int R, 
   fill_common(p, P, c, gsr::kModeAG, R, M, N, ws);
   int mt = 0, row = 0;
   p.ag_pad_shard = -1;
+  p.ag_gran = ag_granule(R, M_r);
   for (int r = 0; r < R; ++r) {
-    p.shard_mt_begin[r] = mt;        // in 128-row half-tiles, each inside one shard
+    p.shard_mt_begin[r] = mt;        // in row granules, each inside one shard
     p.shard_row_begin[r] = row;
     p.shard_rows[r] = static_cast<int>(M_r[r]);
-    mt += static_cast<int>(cdiv(M_r[r], BM));
+    mt += static_cast<int>(cdiv(M_r[r], p.ag_gran));
     row += static_cast<int>(M_r[r]);
     if (M_r[r] > 0 && p.ag_pad_shard < 0) p.ag_pad_shard = r;
     if (M_r[r] > 0) {
-      CUresult cr = encode_kmajor(&p.tmap_a[r], A_r[r], M_r[r], K, BM);
+      CUresult cr = encode_kmajor(&p.tmap_a[r], A_r[r], M_r[r], K, p.ag_gran);
       if (cr != CUDA_SUCCESS) return fail(GSR_ERR_CUDA, "encoding A_r[%d] descriptor failed (%d)", r, (int)cr);
     }
   }

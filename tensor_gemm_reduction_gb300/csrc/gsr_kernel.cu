@@ -39,6 +39,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "gsr_device.cuh"
 #include "gsr_params.h"
 
@@ -56,10 +58,41 @@ struct Unit {
   int m0;         // first row of THIS CTA's 128 rows in its A operand: AR/RS
                   // global, AG local to the CTA's shard
   int shard;      // AG: M-shard of this CTA's rows (-1: the idle half of an odd
-                  // last pair tile, which reads zeros and stores nothing)
+                  // last pair tile, which reads zeros and stores nothing); with
+                  // 64-row granules, of its first 64 rows (see next_granule)
   int kb_begin;   // k-blocks [kb_begin, kb_end) of this piece
   int kb_end;
 };
+
+// AG: the shard and first shard row of row granule g (granules are numbered
+// over all shards, each inside one shard); shard -1 past the last row. Called
+// by whole warps (`mt_begins` holds shard_mt_begin[lane]).
+__device__ __forceinline__ void locate_granule(const Params& p, int mt_begins, int g, int& shard,
+                                               int& m0) {
+  if (g >= p.ag_halves) {
+    shard = -1;
+    m0 = 0;
+    return;
+  }
+  int r = 0;
+  while (r + 1 < p.R && __shfl_sync(0xffffffffu, mt_begins, r + 1) <= g) ++r;
+  shard = r;
+  m0 = (g - __shfl_sync(0xffffffffu, mt_begins, r)) * p.ag_gran;
+}
+
+// AG with 64-row granules: the granule after (shard, m0), i.e. the second half
+// of a CTA's 128 rows, derived where it is used rather than carried in every
+// unit (registers). Called by whole warps.
+__device__ __forceinline__ void next_granule(const Params& p, int mt_begins, int shard, int m0,
+                                             int& shard_b, int& m0b) {
+  if (shard < 0) {
+    shard_b = -1;
+    m0b = 0;
+    return;
+  }
+  const int g = __shfl_sync(0xffffffffu, mt_begins, shard) + m0 / p.ag_gran + 1;
+  locate_granule(p, mt_begins, g, shard_b, m0b);
+}
 
 // Position of the tile in the output (raster order) and its shard. Called by
 // whole warps: `mt_begins` holds shard_mt_begin[lane] in each lane (AG), read
@@ -90,20 +123,14 @@ __device__ __forceinline__ void place_tile(const Params& p, Unit& t, uint32_t ra
     nt = in_g / gm;
   }
   t.n0 = nt * BN;
-  // This CTA's 128 rows: half-tile h. AG half-tiles are numbered over all
-  // shards, each inside one shard, so the two halves of a pair tile may come
-  // from neighbouring shards and no rows are wasted on shard boundaries.
+  // This CTA's 128 rows: half-tile h. AG rows come in granules numbered over
+  // all shards, each inside one shard: one 128-row granule per CTA tile, or
+  // two 64-row granules (where shards are multiples of 64 but not of 128 rows,
+  // e.g. 448) that may come from neighbouring shards. Either way the halves of
+  // a pair tile may too, and no rows are wasted on shard boundaries.
   const int h = mt * CG + static_cast<int>(rank);
   if (p.mode == kModeAG) {
-    if (h >= p.ag_halves) {
-      t.shard = -1;
-      t.m0 = 0;
-    } else {
-      int r = 0;
-      while (r + 1 < p.R && __shfl_sync(0xffffffffu, mt_begins, r + 1) <= h) ++r;
-      t.shard = r;
-      t.m0 = (h - __shfl_sync(0xffffffffu, mt_begins, r)) * BM;
-    }
+    locate_granule(p, mt_begins, p.ag_gran == BM ? h : 2 * h, t.shard, t.m0);
   } else {
     t.shard = 0;
     t.m0 = h * BM;
@@ -306,67 +333,92 @@ __device__ void run_producer(const Params& p, uint32_t tiles_base, uint32_t bars
   Sched& sch = entry.sch;
   Unit t = entry.t;
   for (bool have = entry.have; ok && have; have = sched_next<BN, CG>(p, sch, t, rank)) {
-    if (p.ready != nullptr && t.shard >= 0 && !(arrived & (1u << t.shard))) {
-      const bool here = wait_flag(p.ready + t.shard, p.epoch, ctl, (kRoleProducer << 8) | 3);
-      __syncwarp();
-      if (!here) {
-        ok = false;
-        break;
+    const bool a_two = p.mode == kModeAG && p.ag_gran != BM;   // two 64-row boxes
+    int shard_b = t.shard, m0b = t.m0;
+    if (a_two) next_granule(p, sch.mt_begins, t.shard, t.m0, shard_b, m0b);
+    // AG with arrival flags: every shard this CTA's rows come from must be in.
+    for (int j = 0; ok && j < 2; ++j) {
+      const int sh = j ? shard_b : t.shard;
+      if (p.ready != nullptr && sh >= 0 && !(arrived & (1u << sh))) {
+        const bool here = wait_flag(p.ready + sh, p.epoch, ctl, (kRoleProducer << 8) | 3);
+        __syncwarp();
+        if (!here) ok = false;
+        else arrived |= 1u << sh;
       }
-      arrived |= 1u << t.shard;
     }
+    if (!ok) break;
     // This CTA's rows of A, and its columns of B: with a CTA pair the MMA's N
     // columns are split in halves between the two CTAs.
     // The idle half of an odd last pair tile reads rows past the end of a
     // non-empty shard: the TMA unit fills them with zeros.
     const int a_shard = t.shard >= 0 ? t.shard : p.ag_pad_shard;
     const int a_row = t.shard >= 0 ? t.m0 : p.shard_rows[p.ag_pad_shard];
+    const int a_shard_b = shard_b >= 0 ? shard_b : p.ag_pad_shard;
+    const int a_row_b = shard_b >= 0 ? m0b : p.shard_rows[p.ag_pad_shard];
     const int b_row = t.n0 + static_cast<int>(rank * (tile_mma_n<BN>(p, t) / CG));
     int r = 0;
     if (p.mode != kModeAG)
       while (p.shard_kb_begin[r + 1] <= t.kb_begin) ++r;
-    for (int kb = t.kb_begin; kb < t.kb_end; ++kb) {
-      const uint32_t stage = slot;
-      const bool free_slot = wait_bounded(empty0 + 8 * stage, slot_parity, ctl, (kRoleProducer << 8) | 1);
-      __syncwarp();
-      if (!free_slot) {
-        ok = false;
-        break;
+    // The k-block loop, in two compiled forms so that the usual one (one box of
+    // A rows) carries no test for the second box: this loop alone feeds the
+    // tensor pipe, and every instruction added to it per k-block costs.
+    auto stream_kblocks = [&](auto two_boxes) {
+      constexpr bool kTwo = decltype(two_boxes)::value;
+      for (int kb = t.kb_begin; kb < t.kb_end; ++kb) {
+        const uint32_t stage = slot;
+        const bool free_slot = wait_bounded(empty0 + 8 * stage, slot_parity, ctl, (kRoleProducer << 8) | 1);
+        __syncwarp();
+        if (!free_slot) {
+          ok = false;
+          break;
+        }
+        const uint32_t full = full0 + 8 * stage;
+        const uint32_t sa = tiles_base + stage * L::kABytes;
+        const uint32_t sb = tiles_base + STAGES * L::kABytes + stage * L::kBBytes;
+        const CUtensorMap* ma;
+        const CUtensorMap* ma_b = nullptr;   // the second 64-row box's shard
+        const CUtensorMap* mb;
+        int kx;
+        if (p.mode == kModeAG) {
+          ma = &p.tmap_a[a_shard];
+          if constexpr (kTwo) ma_b = &p.tmap_a[a_shard_b];
+          mb = &p.tmap_b[0];
+          kx = kb * BK;
+        } else {
+          while (p.shard_kb_begin[r + 1] <= kb) ++r;
+          ma = &p.tmap_a[r];
+          mb = &p.tmap_b[r];
+          kx = (kb - p.shard_kb_begin[r]) * BK;
+        }
+        // With 64-row AG granules the A tile is two boxes of 64 rows (8 KB each,
+        // a whole number of 128-byte swizzle atoms, so the layout is that of one
+        // 128-row box).
+        constexpr uint32_t kHalfA = L::kABytes / 2;
+        if constexpr (CG == 1) {
+          mbar_arrive_expect_tx(full, L::kStageBytes);
+          tma_load_2d_hint(sa, ma, full, kx, a_row, pol_a);
+          if constexpr (kTwo) tma_load_2d_hint(sa + kHalfA, ma_b, full, kx, a_row_b, pol_a);
+          tma_load_2d_hint(sb, mb, full, kx, b_row, pol_b);
+        } else {
+          // Both CTAs' bytes are counted on the leader's full barrier, which the
+          // leader alone arms (for the pair's bytes).
+          if (rank == 0) mbar_arrive_expect_tx(full, CG * L::kStageBytes);
+          const uint32_t lead_full = map_shared_to_rank(full, 0);
+          tma_load_2d_pair(sa, ma, lead_full, kx, a_row, pol_a);
+          if constexpr (kTwo) tma_load_2d_pair(sa + kHalfA, ma_b, lead_full, kx, a_row_b, pol_a);
+          tma_load_2d_pair(sb, mb, lead_full, kx, b_row, pol_b);
+        }
+        if (++issued == 1) prefetch_descriptors();
+        if (++slot == STAGES) {
+          slot = 0;
+          slot_parity ^= 1u;
+        }
       }
-      const uint32_t full = full0 + 8 * stage;
-      const uint32_t sa = tiles_base + stage * L::kABytes;
-      const uint32_t sb = tiles_base + STAGES * L::kABytes + stage * L::kBBytes;
-      const CUtensorMap* ma;
-      const CUtensorMap* mb;
-      int kx;
-      if (p.mode == kModeAG) {
-        ma = &p.tmap_a[a_shard];
-        mb = &p.tmap_b[0];
-        kx = kb * BK;
-      } else {
-        while (p.shard_kb_begin[r + 1] <= kb) ++r;
-        ma = &p.tmap_a[r];
-        mb = &p.tmap_b[r];
-        kx = (kb - p.shard_kb_begin[r]) * BK;
-      }
-      if constexpr (CG == 1) {
-        mbar_arrive_expect_tx(full, L::kStageBytes);
-        tma_load_2d_hint(sa, ma, full, kx, a_row, pol_a);
-        tma_load_2d_hint(sb, mb, full, kx, b_row, pol_b);
-      } else {
-        // Both CTAs' bytes are counted on the leader's full barrier, which the
-        // leader alone arms (for the pair's bytes).
-        if (rank == 0) mbar_arrive_expect_tx(full, CG * L::kStageBytes);
-        const uint32_t lead_full = map_shared_to_rank(full, 0);
-        tma_load_2d_pair(sa, ma, lead_full, kx, a_row, pol_a);
-        tma_load_2d_pair(sb, mb, lead_full, kx, b_row, pol_b);
-      }
-      if (++issued == 1) prefetch_descriptors();
-      if (++slot == STAGES) {
-        slot = 0;
-        slot_parity ^= 1u;
-      }
-    }
+    };
+    if (a_two)
+      stream_kblocks(std::true_type{});
+    else
+      stream_kblocks(std::false_type{});
   }
   if (!ok && (CG == 1 || rank == 0)) {
     // Let every copy already issued land before the CTA's shared memory goes
@@ -511,9 +563,14 @@ __device__ void run_epilogue(const Params& p, uint32_t bars, uint32_t tmem_base,
     uint16_t* row_ptr;
     size_t rep_off = 0;
     if (p.mode == kModeAG) {
-      const int sh = t.shard >= 0 ? t.shard : 0;
-      const int lr = m0 + row_in_tile;
-      row_ok = t.shard >= 0 && lr < p.shard_rows[sh];
+      // With 64-row granules, rows 64..127 of the tile are the second granule's.
+      int shard_b = t.shard, m0b = t.m0;
+      if (p.ag_gran != BM) next_granule(p, sch.mt_begins, t.shard, t.m0, shard_b, m0b);
+      const bool second = p.ag_gran != BM && row_in_tile >= 64;
+      const int shard = second ? shard_b : t.shard;
+      const int sh = shard >= 0 ? shard : 0;
+      const int lr = second ? m0b + (row_in_tile - 64) : m0 + row_in_tile;
+      row_ok = shard >= 0 && lr < p.shard_rows[sh];
       row_ptr = p.y + (static_cast<size_t>(p.shard_row_begin[sh]) + lr) * p.N + t.n0;
     } else {
       const int gr = m0 + row_in_tile;

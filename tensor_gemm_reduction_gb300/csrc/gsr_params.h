@@ -75,8 +75,10 @@ struct Params {  // 128-byte aligned through its CUtensorMap members
   int policy_b;                 // L2 policy of B-operand loads (kPolicy*)
   int rps;                      // RS: rows per shard = ceil(M/R)
   int shard_kb_begin[kMaxShards + 1];  // AR/RS: first k-block of shard r
-  int shard_mt_begin[kMaxShards + 1];  // AG: first 128-row half-tile of shard r
-  int ag_halves;                // AG: 128-row half-tiles over all shards
+  int shard_mt_begin[kMaxShards + 1];  // AG: first row granule of shard r
+  int ag_halves;                // AG: row granules over all shards
+  int ag_gran;                  // AG: rows per granule, 128 (one per CTA tile) or 64
+                                // (two per CTA tile, possibly from two shards)
   int ag_pad_shard;             // AG: a non-empty shard, read out of range (zeros)
                                 // by the idle half of an odd last pair tile
   int shard_row_begin[kMaxShards + 1]; // AG: first output row of shard r

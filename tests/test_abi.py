@@ -303,9 +303,10 @@ def test_large_m_uses_cta_pairs_and_a_stream_k_tail(host):
     assert d["dp_tiles"] == 47 * 74 and d["sk_iters"] == 106 * 112
     d = host.describe(B.MODE_AG, 0, 6288, 7168, [4096] * 8)
     assert d["cta_group"] == 2 and d["tiles"] == 8 * 16 * 25
-    # 448-row shards: two pair tiles each, 87.5 % of rows used, as with 128-row tiles
+    # 448-row shards: 64-row granules, two per CTA and possibly from two
+    # shards, so no rows are wasted: 3584 rows in 14 pair tiles (not 16)
     d = host.describe(B.MODE_AG, 0, 3648, 7168, [448] * 8)
-    assert d["cta_group"] == 2 and d["tiles"] == 8 * 2 * 15
+    assert d["cta_group"] == 2 and d["tiles"] == 14 * 15
     # 384-row shards: 24 half-tiles of 128 rows, paired across shard boundaries
     d = host.describe(B.MODE_AG, 0, 3648, 7168, [384] * 8)
     assert d["cta_group"] == 2 and d["tiles"] == 12 * 15

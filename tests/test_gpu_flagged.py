@@ -46,13 +46,17 @@ def test_flags_already_set_match_plain_ag(cfg):
     assert np.array_equal(bits_of(Y1), bits_of(Y0))
 
 
+@pytest.mark.parametrize("M_r", [[2048, 2048, 1024, 2048], [448, 448, 1088, 448]],
+                         ids=["128-row granules", "64-row granules"])
 @pytest.mark.parametrize("cfg", ["auto", "cta1"])
-def test_kernel_waits_for_shards_copied_while_it_runs(cfg):
+def test_kernel_waits_for_shards_copied_while_it_runs(cfg, M_r):
     """The GEMM is launched before its shards exist on the device; a second
     stream copies them in from pinned host memory, one shard at a time, and
-    signals each one. The result must equal the plain AG on resident shards."""
+    signals each one. The result must equal the plain AG on resident shards.
+    With 64-row granules a CTA's rows may come from two shards, and it waits
+    for both."""
     p, ws = plan(**CONFIGS[cfg])
-    inp = gi.gaussian_ag([2048, 2048, 1024, 2048], 3648, 2048, seed=22)
+    inp = gi.gaussian_ag(M_r, 3648, 2048, seed=22)
     dev = device()
     host = [a.pin_memory() for a in inp.A_r]
     A = [torch.empty_like(a, device=dev) for a in inp.A_r]
@@ -75,7 +79,8 @@ def test_kernel_waits_for_shards_copied_while_it_runs(cfg):
     B.gemm_ag(p, A, W, Y_ref, ws)
     B.gemm_shard_check_status(p, ws)
     assert np.array_equal(bits_of(Y), bits_of(Y_ref))
-    rows = np.array([0, 1, 2047, 2048, 4095, 4096, 5119, 5120, inp.M - 1])
+    bounds = np.cumsum(M_r)[:-1]
+    rows = np.unique(np.concatenate([[0, 1, inp.M - 1], bounds - 1, bounds]))
     r = np.repeat(rows, inp.N)
     c = np.tile(np.arange(inp.N), len(rows))
     ref = oracle.ag_at(inp.A_r, inp.W, r, c).reshape(len(rows), inp.N)

@@ -214,6 +214,11 @@ AG_SHAPES = [
     ([384, 384, 384], 264, 128),        # pair tiles across shard boundaries
     ([384, 0, 200, 0], 520, 136),       # odd half-tile count, empty shards
     ([0, 0, 130], 136, 64),             # leading empty shards, idle last half
+    # 64-row granules (shards multiples of 64 but not 128): a CTA's 128 rows
+    # may come from two shards
+    ([448] * 4, 520, 256),
+    ([64, 448, 192, 0, 320], 264, 128),   # empty shard in between
+    ([448, 448, 64], 3648, 256),          # odd granule count: last tile half empty
 ]
 
 
