@@ -255,10 +255,11 @@ void uniform_schedule(const gemm_shard_plan* P, int64_t workers, Config& c) {
 //    ranges start anywhere, share little in L2, and leave some workers with
 //    two cut pieces). AR M = 1000, N = 7168: 36 tail tiles x 2 pieces on 76
 //    pairs;
-//  - whole tiles, when it is nearly full (at least 85 % of the workers:
-//    sharing it out saves under 15 % of a tile, less than the cut tiles'
-//    pieces cost; measured at AR M = 4096 and AG KDA M = 3072, 2.5 % and 4 %
-//    faster; at 63 % stream-K still won by 2 %), when there is too little to
+//  - whole tiles, when it is mostly full (at least 70 % of the workers:
+//    sharing it out saves under 30 % of a tile, less than the cut tiles'
+//    pieces cost; measured at 76, 89 and 95 % (AG MLA M = 3584, AR M = 4096,
+//    AG KDA M = 3072) 2.3, 2.5 and 4 % faster; at 63 % stream-K still won by
+//    1-2 %, at 53 % by 0.7 %), when there is too little to
 //    share out, or too much for the kernel's 32-bit stream-K arithmetic
 //    ((sk_iters + 1) * (workers + 1) must stay below 2^32);
 //  - otherwise stream-K: its k-blocks cut evenly over every worker (schedule 2
@@ -290,7 +291,7 @@ void tail_schedule(const gemm_shard_plan* P, int64_t workers, Config& c) {
       dp = full * workers;                          // only the partial last wave
   }
   int64_t sk_iters = (c.tiles - dp) * c.kb_total;
-  const bool nearly_full = P->opt_schedule == 0 && rem * 20 >= workers * 17;
+  const bool nearly_full = P->opt_schedule == 0 && rem * 10 >= workers * 7;
   if (nearly_full || (sk_iters > 0 && sk_iters < 4 * workers) ||
       (sk_iters + 1) * (workers + 1) >= (int64_t(1) << 32)) {
     dp = c.tiles;

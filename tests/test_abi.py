@@ -490,15 +490,18 @@ def test_split_tail_where_the_partial_wave_is_at_most_half(lib):
 
 
 def test_nearly_full_partial_wave_runs_whole_tiles(lib):
-    """On 152 SMs (76 pairs): a partial last wave of at least 85 % of the
+    """On 152 SMs (76 pairs): a partial last wave of at least 70 % of the
     workers runs as whole tiles (AR M = 4096: 448 tiles, 68 in the last wave;
-    AG KDA M = 3072: 300 tiles, 72), a fuller share-out stays stream-K (AG KDA
-    M = 2048: 48 of 76), and an explicit schedule still gets stream-K."""
+    AG KDA M = 3072: 300 tiles, 72; AG MLA M = 3584 in 448-row shards: 210
+    tiles, 58), a fuller share-out stays stream-K (AG KDA M = 2048: 48 of 76),
+    and an explicit schedule still gets stream-K."""
     h = Host(lib, sm=152, max_M=34816)
     d = h.describe(B.MODE_AR, 4096, 7168, 0, [896] * 8)
     assert (d["tiles"], d["dp_tiles"], d["sk_iters"], d["ctas"]) == (448, 448, 0, 152)
     d = h.describe(B.MODE_AG, 0, 6288, 7168, [384] * 8)
     assert (d["tiles"], d["dp_tiles"], d["sk_iters"]) == (300, 300, 0)
+    d = h.describe(B.MODE_AG, 0, 3648, 7168, [448] * 8)
+    assert (d["tiles"], d["dp_tiles"], d["sk_iters"]) == (210, 210, 0)
     d = h.describe(B.MODE_AG, 0, 6288, 7168, [256] * 8)
     assert d["schedule"] == 2 and d["sk_iters"] == 48 * 112
     h3 = Host(lib, sm=152, max_M=34816)
