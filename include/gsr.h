@@ -84,8 +84,14 @@ typedef enum {
                                3 = A evict-first / B evict-last                     */
     GSR_OPT_CTA_GROUP = 7,  /* CTAs per MMA tile: 0 = heuristic, 1 = one CTA per
                                128-row tile, 2 = a CTA pair per 256-row tile        */
-    GSR_OPT_SCHEDULE = 8,   /* work schedule: 0 = heuristic (stream-K over the
-                               partial last wave), 1 = uniform (every tile cut
+    GSR_OPT_SCHEDULE = 8,   /* work schedule: 0 = heuristic (uniform while there
+                               are fewer single-CTA tiles than SMs; else whole
+                               tiles for the full waves and, for a partial last
+                               wave, a split tail (5) when it is at most half a
+                               wave and its pieces keep at least 60 % of the
+                               workers busy, whole tiles when at least 70 % of
+                               the workers have one, stream-K (3) otherwise),
+                               1 = uniform (every tile cut
                                into the same number of pieces), 2 = stream-K
                                over the last one or two waves, 3 = stream-K
                                over the partial last wave, each worker's
@@ -94,14 +100,14 @@ typedef enum {
                                tile of the partial last wave cut into the same
                                k-pieces (2 or 3, one per worker, at most as many
                                pieces as workers), walked before the whole
-                               tiles (the heuristic picks it when the partial
-                               wave is at most half a wave)                      */
+                               tiles                                             */
     GSR_OPT_SMALL_M = 9,    /* the small-M kernel (AR/RS, M <= 256): 0 = heuristic
                                (used when M <= 256 and no other option above
                                forces a configuration), 1 = never, 2 = whenever
                                M <= 256 and the K range has at least two
-                               k-blocks of 64. It streams W in 128-row tiles
-                               against all M rows at once (the activation rows
+                               k-blocks of 64. It streams W in tiles of rows
+                               (GSR_OPT_SMALL_TILE_ROWS, at most 128) against
+                               all M rows at once (the activation rows
                                are the MMA's N), each tile split over K between
                                the two CTAs of a cluster and summed in
                                distributed shared memory; it needs no workspace

@@ -36,8 +36,9 @@ struct gemm_shard_plan {
   int opt_raster_n;    // 0 = raster by m-tile groups
   int opt_l2_hints;    // 0 = heuristic
   int opt_cta_group;   // 0 = heuristic
-  int opt_schedule;    // 0 = heuristic (stream-K hybrid), 1 = uniform, 2 = stream-K hybrid,
-                       // 3 = stream-K only for a partial last wave
+  int opt_schedule;    // 0 = heuristic, 1 = uniform, 2 = stream-K over the last one or two
+                       // waves, 3/4 = stream-K over a partial last wave (its range first /
+                       // last), 5 = split tail (GSR_OPT_SCHEDULE in gsr.h)
   int opt_small;       // 0 = heuristic, 1 = never use the small-M kernel, 2 = always when it applies
   int opt_small_rows;  // small-M kernel: W rows per tile (0 = heuristic)
   int pair_clusters;   // CTA pairs that can be resident at once
@@ -249,8 +250,9 @@ void uniform_schedule(const gemm_shard_plan* P, int64_t workers, Config& c) {
 }
 
 // Whole tiles for every full wave, and for the partial last wave one of:
-//  - a split tail, when it is at most half a wave: each of its tiles cut into
-//    the same 2 or 3 k-pieces, one per worker, so the workers holding the same
+//  - a split tail, when it is at most half a wave and its pieces keep at least
+//    60 % of the workers busy: each of its tiles cut into the same 2 or 3
+//    k-pieces, one per worker, so the workers holding the same
 //    piece of neighbouring tiles read the same k-blocks together (stream-K's
 //    ranges start anywhere, share little in L2, and leave some workers with
 //    two cut pieces). AR M = 1000, N = 7168: 36 tail tiles x 2 pieces on 76
