@@ -372,10 +372,13 @@ typedef struct {
 } gsr_config;
 
 /* The kernel configuration the plan chooses for a call, for logging and tests:
- * mode 0 = AR, 1 = RS, 2 = AG. AR/RS use M and sizes = K_r (K is ignored); AG
- * uses K and sizes = M_r (M is ignored). The configuration depends on the
- * shape, the device and the plan's options, never on the mode, except that AG
- * counts tiles per shard. */
+ * mode 0 = AR, 1 = RS, 2 = AG. AR/RS use M (>= 0) and sizes = K_r (positive
+ * multiples of 8; K is ignored); AG uses K (a positive multiple of 8) and
+ * sizes = M_r (>= 0; M is ignored). The plan's maxima are not checked. The
+ * configuration depends on the shape, the device and the plan's options, never
+ * on the mode, except that AG counts tiles per shard. GSR_ERR_INVALID_VALUE
+ * for a NULL plan, out or sizes, a mode outside 0..2, R outside 1..16 or a
+ * size that breaks the rules above. */
 gsr_status gemm_shard_describe(const gemm_shard_plan *plan, int mode, int64_t M,
                                int64_t N, int64_t K, int R, const int64_t *sizes,
                                gsr_config *out);

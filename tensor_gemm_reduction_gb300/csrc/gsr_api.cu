@@ -979,6 +979,16 @@ gsr_status gemm_shard_describe(const gemm_shard_plan* P, int mode, int64_t M, in
   if (mode < 0 || mode > 2) return fail(GSR_ERR_INVALID_VALUE, "mode must be 0, 1 or 2");
   if (R < 1 || R > kMaxShards || !sizes) return fail(GSR_ERR_INVALID_VALUE, "bad R or sizes");
   if (N < 8 || N % 8) return fail(GSR_ERR_INVALID_VALUE, "N must be a positive multiple of 8");
+  if (mode == gsr::kModeAG) {
+    if (K < 8 || K % 8) return fail(GSR_ERR_INVALID_VALUE, "K must be a positive multiple of 8");
+    for (int r = 0; r < R; ++r)
+      if (sizes[r] < 0) return fail(GSR_ERR_INVALID_VALUE, "M_r[%d] must be >= 0", r);
+  } else {
+    if (M < 0) return fail(GSR_ERR_INVALID_VALUE, "M must be >= 0");
+    for (int r = 0; r < R; ++r)
+      if (sizes[r] < 8 || sizes[r] % 8)
+        return fail(GSR_ERR_INVALID_VALUE, "K_r[%d] must be a positive multiple of 8", r);
+  }
   const Config c = choose_config(P, mode, M, N, K, R, sizes);
   out->block_n = c.block_n;
   out->cta_group = c.cta_group;

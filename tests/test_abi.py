@@ -170,6 +170,24 @@ def test_ag_argument_validation(host, kw, frag):
     assert frag in B.gsr_last_error_string()
 
 
+@pytest.mark.parametrize("args,frag", [
+    ((B.MODE_AR, -1, 256, 0, [128]), "M must"),
+    ((B.MODE_AR, 16, 256, 0, [128, 20]), "K_r[1]"),
+    ((B.MODE_RS, 16, 256, 0, [0]), "K_r[0]"),
+    ((B.MODE_AG, 0, 256, 0, [16]), "K must"),
+    ((B.MODE_AG, 0, 256, 100, [16]), "K must"),
+    ((B.MODE_AG, 0, 256, 128, [16, -1]), "M_r[1]"),
+    ((B.MODE_AR, 16, 250, 0, [128]), "N must"),
+    ((3, 16, 256, 0, [128]), "mode"),
+    ((B.MODE_AR, 16, 256, 0, []), "bad R"),
+])
+def test_describe_argument_validation(host, args, frag):
+    with pytest.raises(B.GsrError) as e:
+        host.describe(*args)
+    assert e.value.status == B.GSR_ERR_INVALID_VALUE
+    assert frag in str(e.value)
+
+
 def test_ag_null_pointer_allowed_for_empty_shard(host):
     assert host.ag(256, 128, [16, 0, 8], a=[0x100000, 0, 0x300000]) == B.GSR_ERR_UNSUPPORTED
 
