@@ -1,0 +1,117 @@
+"""Host-side logic of the benchmark, checked without a GPU: the workload table
+(shapes and algorithmic work), the robust mean of the sweep, the clock-record
+summary that decides the peak, and the guard that drops stale ncu traffic."""
+import json
+import os
+
+import pytest
+
+import bench
+from tensor_gemm_reduction_gb300 import inputs as gi
+
+
+def test_workload_table_has_the_pages_projection_shapes():
+    names = {w.name: w for w in gi.ALL_WORKLOADS}
+    # AG-GEMM page, microbenchmark tables: KDA (N = 6288) and MLA (N = 3648)
+    # projections at K = 7168 on TP8, global M = 8 x local M.
+    for local in (256, 384, 448, 512, 1024, 2048, 4096):
+        for kind, n in (("kda", 6288), ("mla", 3648)):
+            w = names[f"ag_{kind}_m{8 * local}"]
+            assert (w.mode, w.N, w.K, w.R, w.M) == ("ag", n, 7168, 8, 8 * local)
+            assert w.shard_sizes() == [local] * 8
+    # GEMM-RS/AR page, o_proj: N = K = 7168, K split over 8 ranks.
+    for m in (128, 129, 1000, 4096, 32768):
+        w = names[f"ar_oproj_m{m}"]
+        assert (w.mode, w.N, w.K, w.R, w.M) == ("ar", 7168, 7168, 8, m)
+        assert w.shard_sizes() == [896] * 8
+    for r in (2, 4, 8, 16):
+        w = names[f"rs_r{r}"]
+        assert w.shard_sizes() == [7168 // r] * r and w.M == 32768
+        # RS shares its inputs with AR o_proj M = 32768.
+        assert w.seed == gi.default_seed(32768, 7168)
+    assert names["ar_tiny"].seed == 0
+
+
+def test_algorithmic_work_closed_forms():
+    w = bench.workload_by_name("ag_kda_m32768")
+    assert w.flops == 2 * 32768 * 6288 * 7168            # 2.95 TFLOP
+    assert round(w.flops / 1e12, 2) == 2.95
+    assert w.bytes == 2 * (32768 * 7168 + 6288 * 7168 + 32768 * 6288)
+    ar = bench.workload_by_name("ar_oproj_m32768")
+    assert round(ar.flops / 1e12, 2) == 3.37
+    # W alone at N = K = 7168 is 102.8 MB: the whole cost of a decode step.
+    small = bench.workload_by_name("ar_oproj_m128")
+    assert small.bytes - 2 * (128 * 7168 * 2) == 2 * 7168 * 7168
+    assert round(2 * 7168 * 7168 / 1e6, 1) == 102.8
+    # Packed gather: the kept rows of every state read once, P written once.
+    p = gi.PACK_SP
+    assert p.bytes == 2 * 2 * (8 * 4096 - 5) * 4 * 7168
+
+
+def test_unknown_workload_is_rejected():
+    with pytest.raises(SystemExit):
+        bench.workload_by_name("no_such_workload")
+
+
+def test_describe_workload_names_the_shard_sizes():
+    d = bench.describe_workload(bench.workload_by_name("ag_mla_m3584"))
+    assert d == {"workload": "ag_mla_m3584", "mode": "ag", "R": 8, "M": 3584, "N": 3648,
+                 "K": 7168, "M_r": 448}
+    d = bench.describe_workload(bench.workload_by_name("rs_r16"))
+    assert d["K_r"] == 448 and "M_r" not in d
+
+
+def test_trimmed_mean_drops_both_tails():
+    xs = [10.0] * 8 + [1000.0, 0.001, 10.5, 9.5]
+    assert bench.trimmed_mean(xs) == pytest.approx(10.0)
+    assert bench.trimmed_mean([3.0]) == 3.0
+    assert bench.trimmed_mean([1.0, 2.0]) == 1.5
+
+
+def _clock_rows(path, rows):
+    with open(path, "w") as f:
+        for sm, mx, pw, flags in rows:
+            f.write(f"0, {sm}, {mx}, {pw}, 0x0, " + ", ".join(flags) + "\n")
+
+
+def test_clock_summary_uses_loaded_samples_and_collects_reasons(tmp_path):
+    s = bench.ClockSampler(0)
+    s.path = str(tmp_path / "clocks.csv")
+    s.proc = object()              # as if nvidia-smi had run
+    idle = ("Not Active",) * 4
+    capped = ("Not Active", "Not Active", "Not Active", "Active")
+    _clock_rows(s.path, [(2070, 2070, 200.0, idle)] * 5 +
+                        [(1400, 2070, 1390.0, capped)] * 3 + [(1450, 2070, 1300.0, idle)] * 2)
+    out = s.summary()
+    assert out["sm_mhz"] == 1400                 # median of the five loaded samples
+    assert out["sm_max_mhz"] == 2070
+    assert out["samples"] == 5
+    assert out["reasons"] == ["sw_power_cap"]
+    assert not os.path.exists(s.path)
+
+
+def test_clock_summary_without_nvidia_smi():
+    s = bench.ClockSampler(0)
+    assert s.summary()["reasons"] == ["nvidia-smi unavailable"]
+
+
+def test_peaks_fall_back_without_the_measured_file(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.peaks()["source"] == "fallback"
+    (tmp_path / "MEASURED_PEAKS.json").write_text(
+        json.dumps({"hbm_gbs": 7000.0, "bf16_tflops": 1800.0}))
+    pk = bench.peaks()
+    assert pk["source"] == "measured"
+    assert pk["bf16_sustained"] == pk["bf16_burst"] == 1800.0
+
+
+def test_ncu_traffic_is_dropped_once_the_kernel_changes(tmp_path, monkeypatch):
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(
+        {"ag_kda_m32768": {"kernel_hash": "aaaa", "dram_bytes_per_launch": 123}}))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "aaaa")
+    assert bench.ncu_traffic("ag_kda_m32768") == 123
+    assert bench.ncu_traffic("ag_mla_m2048") is None
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "bbbb")
+    assert bench.ncu_traffic("ag_kda_m32768") is None
