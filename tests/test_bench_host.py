@@ -1,6 +1,7 @@
 """Host-side logic of the benchmark, checked without a GPU: the workload table
 (shapes and algorithmic work), the robust mean of the sweep, the clock-record
-summary that decides the peak, and the guard that drops stale ncu traffic."""
+summary that decides the peak, the guard that drops stale ncu traffic, and the
+reference arm (the oracle on host cores) and its JSON line."""
 import json
 import os
 
@@ -115,3 +116,37 @@ def test_ncu_traffic_is_dropped_once_the_kernel_changes(tmp_path, monkeypatch):
     assert bench.ncu_traffic("ag_mla_m2048") is None
     monkeypatch.setattr(bench, "kernel_source_hash", lambda: "bbbb")
     assert bench.ncu_traffic("ag_kda_m32768") is None
+
+
+def _bench(args, env_extra=None):
+    import subprocess
+    import sys
+    env = dict(os.environ, **(env_extra or {}))
+    return subprocess.run([sys.executable, os.path.join(os.path.dirname(bench.__file__), "bench.py")]
+                          + args, capture_output=True, text=True, timeout=300, env=env)
+
+
+def test_reference_arm_prints_one_contract_line():
+    r = _bench(["--impl", "reference", "--workload", "ar_tiny", "--steps", "3", "--warmup", "3"])
+    assert r.returncode == 0, r.stderr
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == "TFLOP/s"
+    assert d["steps"] == 3 and d["warmup"] == 3 and d["higher_is_better"] is True
+    assert d["value"] > 0 and d["cpu_baseline"]["value"] == d["value"]
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"] == {"value": d["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+    assert d["config"]["workload"] == "ar_tiny"
+
+
+def test_reference_arm_other_ranks_exit_quietly():
+    r = _bench(["--impl", "reference", "--workload", "ar_tiny", "--steps", "3", "--warmup", "3"],
+               {"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
+    assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_bench_rejects_fewer_than_three_warmup_steps():
+    r = _bench(["--impl", "reference", "--workload", "ar_tiny", "--steps", "3", "--warmup", "2"])
+    assert r.returncode != 0 and "--warmup" in r.stderr
