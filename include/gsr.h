@@ -131,7 +131,10 @@ typedef enum {
  * Returns GSR_ERR_UNSUPPORTED (and no plan) on anything but a compute
  * capability 10.3 device or when no CUDA driver is present;
  * GSR_ERR_INVALID_VALUE when out is NULL, a maximum is < 1, max_N or max_K is
- * not a multiple of 8, or max_R is outside 1..GSR_MAX_SHARDS.
+ * not a multiple of 8, max_R is outside 1..GSR_MAX_SHARDS, or the maxima give
+ * 2^27 or more output tiles of 128 x 128 (an output of about 2.2e12 elements,
+ * far past any device's memory; the kernels count tiles and their pieces in
+ * 32-bit integers).
  */
 gsr_status gemm_shard_plan_create(gemm_shard_plan **out, int device, int64_t max_M,
                                   int64_t max_N, int64_t max_K, int max_R);

@@ -592,6 +592,12 @@ static gsr_status check_maxima(gemm_shard_plan** out, int64_t max_M, int64_t max
     return fail(GSR_ERR_INVALID_VALUE, "maxima must stay below 2^31");
   if (max_R < 1 || max_R > kMaxShards)
     return fail(GSR_ERR_INVALID_VALUE, "max_R=%d outside 1..%d", max_R, kMaxShards);
+  // The kernels count tiles and pieces (up to 16 per tile) in 32-bit integers.
+  const int64_t tiles = (cdiv(max_M, BM) + 2 * max_R) * cdiv(max_N, 128);
+  if (tiles > INT32_MAX / 16)
+    return fail(GSR_ERR_INVALID_VALUE,
+                "max_M x max_N gives %lld output tiles of 128 x 128; at most %d are supported",
+                (long long)tiles, INT32_MAX / 16);
   return ok();
 }
 

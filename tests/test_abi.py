@@ -66,11 +66,23 @@ def test_null_plan_is_rejected(lib):
     (148, 128, 256, 12, 2),     # max_K not a multiple of 8
     (148, 128, 256, 256, 0),    # max_R
     (148, 128, 256, 256, 17),   # max_R > 16
+    (148, 1 << 24, 1 << 20, 256, 2),   # 2^30 output tiles: past 32-bit piece counts
 ])
 def test_host_plan_rejects_bad_maxima(lib, args):
     h = ctypes.c_void_p()
     assert lib.gemm_shard_plan_create_host(ctypes.byref(h), *args) == B.GSR_ERR_INVALID_VALUE
     assert h.value is None
+
+
+def test_host_plan_accepts_the_largest_tile_count(lib):
+    # (2^20 / 128 + 2 R) x (2^16 / 128) tiles = (8192 + 4) x 512, well inside 2^27;
+    # one more factor of 32 in N crosses it.
+    h = ctypes.c_void_p()
+    assert lib.gemm_shard_plan_create_host(ctypes.byref(h), 148, 1 << 20, 1 << 16, 256, 2) == B.GSR_OK
+    lib.gemm_shard_plan_destroy(h)
+    assert lib.gemm_shard_plan_create_host(ctypes.byref(h), 148, 1 << 20, 1 << 21, 256, 2) \
+        == B.GSR_ERR_INVALID_VALUE
+    assert "output tiles" in B.gsr_last_error_string()
 
 
 def _arr(ctype, vals):
