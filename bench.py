@@ -175,9 +175,7 @@ class Runner:
         self.w, self.plan, self.ws, self.B = w, plan, ws, B
         inp = gi.make_inputs(w, device=dev)     # seeded on the device: fast at full size
         self.inp = inp
-        if w.mode == "ag":
-            self.Y = torch.empty(w.M, w.N, dtype=torch.bfloat16, device=dev)
-        elif w.mode == "ar":
+        if w.mode in ("ag", "ar"):
             self.Y = torch.empty(w.M, w.N, dtype=torch.bfloat16, device=dev)
         else:
             rps = -(-w.M // w.R)
@@ -346,6 +344,7 @@ def sweep(plan, ws, dev, pk, names):
         torch.cuda.synchronize()
         time.sleep(ROW_PAUSE_S)
         times, _ = time_launches(r, steps=20, warmup=3, flush=lambda: flush_buf.fill_(1))
+        r.B.gemm_shard_check_status(plan, ws)    # raises if an in-kernel wait ran out
         t = trimmed_mean(times) * 1e-3
         t_roof = max(w.flops / (pk["bf16_burst"] * 1e12), w.bytes / (pk["hbm_gbs"] * 1e9))
         d = B_describe(plan, w)
