@@ -25,6 +25,7 @@ Every function's pin (brute force, invariants, special cases) is in
 from __future__ import annotations
 
 import ctypes
+import fcntl
 import os
 import subprocess
 from typing import List, Sequence, Tuple
@@ -39,20 +40,33 @@ _LIB = os.path.join(_OUT_DIR, "libgsr_oracle.so")
 _lib = None
 
 
+def _fresh() -> bool:
+    return os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)
+
+
 def build(force: bool = False) -> str:
-    """Compile the oracle with gcc (OpenMP when available). Returns the .so path."""
-    os.makedirs(_OUT_DIR, exist_ok=True)
-    if (not force and os.path.exists(_LIB)
-            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+    """Compile the oracle with gcc (OpenMP when available). Returns the .so path.
+    Processes that build at the same time take turns (a lock file), and the
+    library is replaced atomically."""
+    if not force and _fresh():
         return _LIB
-    base = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared",
-            _SRC, "-o", _LIB + ".tmp"]
-    try:
-        subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True,
-                       capture_output=True, text=True)
-    except subprocess.CalledProcessError:
-        subprocess.run(base, check=True, capture_output=True, text=True)
-    os.replace(_LIB + ".tmp", _LIB)
+    os.makedirs(_OUT_DIR, exist_ok=True)
+    with open(os.path.join(_OUT_DIR, ".build.lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        try:
+            if not force and _fresh():
+                return _LIB
+            tmp = f"{_LIB}.{os.getpid()}.tmp"
+            base = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared",
+                    _SRC, "-o", tmp]
+            try:
+                subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True,
+                               capture_output=True, text=True)
+            except subprocess.CalledProcessError:
+                subprocess.run(base, check=True, capture_output=True, text=True)
+            os.replace(tmp, _LIB)
+        finally:
+            fcntl.flock(lock, fcntl.LOCK_UN)
     return _LIB
 
 

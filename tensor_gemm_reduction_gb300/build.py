@@ -10,6 +10,8 @@ the driver on a GPU machine.
 from __future__ import annotations
 
 import argparse
+import contextlib
+import fcntl
 import os
 import shutil
 import subprocess
@@ -43,10 +45,30 @@ def _stale() -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
+@contextlib.contextmanager
+def _build_lock():
+    """One build at a time per tree: processes that start together (one per
+    rank) would otherwise write the same object files."""
+    os.makedirs(OUT_DIR, exist_ok=True)
+    with open(os.path.join(OUT_DIR, ".build.lock"), "w") as fh:
+        fcntl.flock(fh, fcntl.LOCK_EX)
+        try:
+            yield
+        finally:
+            fcntl.flock(fh, fcntl.LOCK_UN)
+
+
 def build(force: bool = False, verbose_ptxas: bool = False) -> str:
     if not force and not _stale():
         return LIB
-    os.makedirs(OUT_DIR, exist_ok=True)
+    with _build_lock():
+        # Another process may have finished the same build while this one waited.
+        if not force and not _stale():
+            return LIB
+        return _build(verbose_ptxas)
+
+
+def _build(verbose_ptxas: bool) -> str:
     nvcc = _nvcc()
     common = [nvcc, *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
               "-I", INCLUDE, "-I", CSRC]
@@ -65,7 +87,7 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
 
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + ".tmp"
+    tmp = f"{LIB}.{os.getpid()}.tmp"
     cmd = [nvcc, *ARCH, "-shared", "-Xcompiler", "-fPIC", "-cudart", "static", *objs, "-o", tmp]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:

@@ -567,3 +567,36 @@ def test_workspace_and_schedule_invariants_over_shapes(lib, sm, schedule):
             assert 0 < tail * d["split"] <= workers and 1 <= d["split"] <= min(3, kb), (M, N, K_r, d)
         if d["schedule"] in (2, 4) and d["dp_tiles"] == d["tiles"]:
             assert d["sk_iters"] == 0
+
+
+def _build_in_child(q):
+    from tensor_gemm_reduction_gb300 import build as b
+    import oracle as o
+    q.put((b.build(), o.build()))
+
+
+def test_concurrent_builds_take_turns(lib):
+    """Ranks that start together all call build(): with the library stale, they
+    must take turns and leave one loadable library, not interleaved objects."""
+    import multiprocessing as mp
+    import oracle
+    for src, built in ((os.path.join(ROOT, "include", "gsr.h"), B.library_path()),
+                       (os.path.join(ROOT, "oracle", "gsr_oracle.c"), oracle.build())):
+        st = os.stat(src)
+        os.utime(src, (st.st_atime, max(st.st_mtime, os.path.getmtime(built)) + 1))
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_build_in_child, args=(q,)) for _ in range(3)]
+    for p in procs:
+        p.start()
+    paths = [q.get(timeout=600) for _ in procs]
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert len(set(paths)) == 1
+    assert not gbuild._stale() and oracle._fresh()
+    again = ctypes.CDLL(paths[0][0])
+    for n in header_functions():
+        assert hasattr(again, n)
+    for built in paths[0]:
+        assert [f for f in os.listdir(os.path.dirname(built)) if f.endswith(".tmp")] == []
