@@ -165,6 +165,18 @@ def describe_workload(w) -> dict:
     return d
 
 
+def bench_config(w, world: int) -> dict:
+    """The `config` object of the JSON line (the same for both arms; the seed of
+    the workload's generator, 2000 + M + K unless the workload fixes another)."""
+    from tensor_gemm_reduction_gb300 import inputs as gi
+    read = w.bytes - 2 * w.M * w.N
+    l2 = ("inputs larger than L2: %.0f MB read per step" % (read / 1e6) if read > L2_BYTES else
+          "inputs fit in L2 (%.1f MB per step): timed back to back without a flush" % (read / 1e6))
+    return dict(describe_workload(w), l2=l2,
+                parallelism="replicas" if world > 1 else "single",
+                seed=w.seed if w.seed is not None else gi.default_seed(w.M, w.K))
+
+
 class Runner:
     """Device-resident inputs and outputs of one workload plus its call."""
 
@@ -316,7 +328,7 @@ def run_reference(args, w):
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws_, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": describe_workload(w), "impl": "reference",
+        "config": bench_config(w, ws_), "impl": "reference",
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.threads(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -501,9 +513,7 @@ def main():
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": region_s / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": dict(describe_workload(w), l2="inputs larger than L2: %.0f MB read per step" %
-                       ((w.bytes - 2 * w.M * w.N) / 1e6), parallelism="replicas" if world > 1 else "single",
-                       seed="2000+M+K, torch CUDA generator"),
+        "config": bench_config(w, world),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": ncu_traffic(w.name),
                      "peak_kind": ("sustained" if sustained else "burst") + " bf16, " + pk["source"] +

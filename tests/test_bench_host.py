@@ -150,3 +150,19 @@ def test_reference_arm_other_ranks_exit_quietly():
 def test_bench_rejects_fewer_than_three_warmup_steps():
     r = _bench(["--impl", "reference", "--workload", "ar_tiny", "--steps", "3", "--warmup", "2"])
     assert r.returncode != 0 and "--warmup" in r.stderr
+
+
+def test_both_arms_share_the_config_object():
+    w = bench.workload_by_name("ag_kda_m32768")
+    c = bench.bench_config(w, 1)
+    assert c["workload"] == "ag_kda_m32768" and c["seed"] == 2000 + 32768 + 7168
+    assert c["parallelism"] == "single" and bench.bench_config(w, 8)["parallelism"] == "replicas"
+    assert bench.bench_config(bench.workload_by_name("ar_tiny"), 1)["seed"] == 0
+    r = _bench(["--impl", "reference", "--workload", "ar_tiny", "--steps", "3", "--warmup", "3"])
+    assert json.loads(r.stdout)["config"] == bench.bench_config(bench.workload_by_name("ar_tiny"), 1)
+
+
+def test_config_states_whether_the_inputs_exceed_l2():
+    assert bench.bench_config(bench.workload_by_name("ag_kda_m32768"), 1)["l2"].startswith(
+        "inputs larger than L2: 560 MB")
+    assert "fit in L2" in bench.bench_config(bench.workload_by_name("ar_tiny"), 1)["l2"]
