@@ -600,3 +600,48 @@ def test_concurrent_builds_take_turns(lib):
         assert hasattr(again, n)
     for built in paths[0]:
         assert [f for f in os.listdir(os.path.dirname(built)) if f.endswith(".tmp")] == []
+
+
+C_CLIENT = r"""
+#include <stdio.h>
+#include <string.h>
+#include "gsr.h"
+int main(void) {
+  gemm_shard_plan *p = NULL;
+  if (gemm_shard_plan_create_host(&p, 152, 4096, 7168, 7168, 8) != GSR_OK) return 1;
+  int64_t K_r[8] = {896, 896, 896, 896, 896, 896, 896, 896};
+  gsr_config c;
+  if (gemm_shard_describe(p, 0, 1000, 7168, 0, 8, K_r, &c) != GSR_OK) return 2;
+  if (c.block_n != 256 || c.cta_group != 2 || c.tiles != 112) return 3;
+  if (gemm_shard_workspace_size(p) < c.workspace_bytes) return 4;
+  if (gemm_ar(p, 1000, 7168, 8, K_r, NULL, NULL, NULL, NULL, 0, NULL) != GSR_ERR_INVALID_VALUE)
+    return 5;
+  if (strstr(gsr_last_error_string(), "NULL") == NULL) return 6;
+  if (gemm_shard_plan_destroy(p) != GSR_OK) return 7;
+  return 0;
+}
+"""
+
+
+@pytest.mark.parametrize("lang", ["c", "c++"])
+def test_header_is_plain_c_and_cxx(lang):
+    import subprocess
+    std = "-std=c99" if lang == "c" else "-std=c++17"
+    r = subprocess.run(["gcc" if lang == "c" else "g++", std, "-Wall", "-Wextra", "-pedantic",
+                        "-Werror", "-fsyntax-only", "-x", lang,
+                        os.path.join(ROOT, "include", "gsr.h")], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+
+
+def test_a_plain_c_program_links_and_calls_the_library(lib, tmp_path):
+    import subprocess
+    src = tmp_path / "client.c"
+    src.write_text(C_CLIENT)
+    exe = tmp_path / "client"
+    libdir = os.path.dirname(B.library_path())
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                        str(src), "-L", libdir, "-lgsr", f"-Wl,-rpath,{libdir}", "-o", str(exe)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    run = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert run.returncode == 0, (run.returncode, run.stdout, run.stderr)
