@@ -136,6 +136,52 @@ def test_ar_identity_weight_returns_x_bitwise():
     assert np.array_equal(bits_of(Y.out), bits_of(torch.cat(inp.X_r, dim=1)))
 
 
+def _one_hot(M: int, K: int, seed: int):
+    g = torch.Generator().manual_seed(seed)
+    cols = torch.randint(0, K, (M,), generator=g)
+    X = torch.zeros(M, K, dtype=torch.bfloat16)
+    X[torch.arange(M), cols] = 1.0
+    return X, cols
+
+
+@pytest.mark.parametrize("variant", ["auto", "sk8", "pairsk8", "splittail", "pairsplit"])
+@pytest.mark.parametrize("M", [100, 300])
+def test_ar_one_hot_rows_select_weight_columns_bitwise(M, variant):
+    """Row m of X is one-hot at column k_m (anywhere in any shard): every
+    product but one is zero, so Y[m, n] = W[n, k_m] exactly, whatever the
+    split, the schedule or the kernel (M = 100 runs the small-M kernel)."""
+    K_r = [128, 64, 192]
+    inp = gi.gaussian_ar(M, 264, K_r, seed=21)
+    X, cols = _one_hot(M, sum(K_r), seed=M)
+    inp.X_r = [X[:, a:a + k].contiguous() for a, k in zip((0, 128, 192), K_r)]
+    Y, _, _ = run_ar(inp, p=vplan(variant))
+    W = torch.cat(inp.W_r, dim=1)
+    assert np.array_equal(bits_of(Y.out), bits_of(W[:, cols].t().contiguous()))
+
+
+@pytest.mark.parametrize("variant", ["auto", "sk8", "pairsk8"])
+def test_ag_one_hot_rows_select_weight_columns_bitwise(variant):
+    M_r = [100, 0, 257, 64]
+    inp = gi.gaussian_ag(M_r, 200, 320, seed=22)
+    X, cols = _one_hot(sum(M_r), 320, seed=5)
+    inp.A_r, r0 = [], 0
+    for m in M_r:
+        inp.A_r.append(X[r0:r0 + m].contiguous())
+        r0 += m
+    Y = run_ag(inp, p=vplan(variant))
+    assert np.array_equal(bits_of(Y.out), bits_of(inp.W[:, cols].t().contiguous()))
+    assert Y.guards_intact()
+
+
+@pytest.mark.parametrize("M", [64, 1000])
+def test_zero_activations_give_zero_output(M):
+    inp = gi.gaussian_ar(M, 520, [256, 256], seed=23)
+    inp.X_r = [torch.zeros_like(x) for x in inp.X_r]
+    Y, _, _ = run_ar(inp)
+    assert not to_f64(Y.out).any()
+    assert Y.guards_intact()
+
+
 def test_ar_negated_input_negates_output_and_keeps_first_result():
     """After the page's lifetime test (M=257, K=768, seed 2500): a second call with
     -X gives exactly -Y, and the first result, in its own buffer, is untouched."""
