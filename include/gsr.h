@@ -41,6 +41,11 @@
  *     status word, the kernel returns cleanly, and gemm_shard_check_status
  *     reports it. The library never aborts the process and never traps.
  *     gsr_last_error_string() describes the last failure on this thread.
+ *   - Logging: with the environment variable GSR_LOG_CONFIG set (to anything
+ *     but "0") when the library is first used, every GEMM call that passes
+ *     validation and has rows to compute writes one line to stderr before its
+ *     launch: the mode, the shape and the kernel configuration it chose (the
+ *     fields of gsr_config). Nothing is logged otherwise.
  */
 #ifndef GSR_H
 #define GSR_H

@@ -13,6 +13,7 @@
 #include <algorithm>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -433,6 +434,30 @@ CUresult encode_kmajor(CUtensorMap* m, const void* ptr, int64_t rows, int64_t co
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
+// GSR_LOG_CONFIG (set and not "0"): every call that passes validation writes
+// its configuration to stderr, one line, before the launch. Read once.
+bool log_config_enabled() {
+  static const bool on = [] {
+    const char* v = std::getenv("GSR_LOG_CONFIG");
+    return v != nullptr && v[0] != '\0' && std::strcmp(v, "0") != 0;
+  }();
+  return on;
+}
+
+void log_config(const char* mode, int64_t M, int64_t N, int R, const Config& c) {
+  if (!log_config_enabled()) return;
+  const char* sched = c.small                            ? "small_m"
+                      : c.sched == gsr::kSchedSplitTail ? "split_tail"
+                      : c.sched == gsr::kSchedStreamK   ? "stream_k"
+                                                        : "uniform";
+  std::fprintf(stderr,
+               "gsr: %s M=%lld N=%lld R=%d kernel=%s block_n=%d cta_group=%d schedule=%s "
+               "split=%d tiles=%lld dp_tiles=%lld sk_iters=%lld ctas=%d workspace=%zu\n",
+               mode, (long long)M, (long long)N, R, c.small ? "small" : "main", c.block_n,
+               c.cta_group, sched, c.splits, (long long)c.tiles, (long long)c.dp_tiles,
+               (long long)c.sk_iters, c.ctas, c.ws_bytes);
+}
+
 gsr_status check_plan(const gemm_shard_plan* P) {
   if (!P) return fail(GSR_ERR_INVALID_VALUE, "plan is NULL");
   return ok();
@@ -548,6 +573,7 @@ gsr_status run_ksharded(const gemm_shard_plan* P, int mode, int64_t M, int64_t N
   s = check_ws(c, ws, ws_bytes);
   if (s) return s;
   if (M == 0) return ok();
+  log_config(mode == gsr::kModeAR ? "ar" : mode == gsr::kModeRS ? "rs" : "ar_replicated", M, N, R, c);
   if (P->device < 0) return fail(GSR_ERR_UNSUPPORTED, "host plan: arguments are valid, nothing launched");
   if (!encode_fn()) return fail(GSR_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled is unavailable");
 
@@ -823,6 +849,7 @@ static gsr_status run_ag(const gemm_shard_plan* P, int64_t N, int64_t K, int R, 
   s = check_ws(c, ws, ws_bytes);
   if (s) return s;
   if (M == 0) return ok();
+  log_config(ready ? "ag_flagged" : "ag", M, N, R, c);
   if (P->device < 0) return fail(GSR_ERR_UNSUPPORTED, "host plan: arguments are valid, nothing launched");
   if (!encode_fn()) return fail(GSR_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled is unavailable");
 

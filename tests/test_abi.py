@@ -645,3 +645,43 @@ def test_a_plain_c_program_links_and_calls_the_library(lib, tmp_path):
     assert r.returncode == 0, r.stderr
     run = subprocess.run([str(exe)], capture_output=True, text=True)
     assert run.returncode == 0, (run.returncode, run.stdout, run.stderr)
+
+
+LOG_CLIENT = r"""
+import ctypes, sys
+sys.path.insert(0, sys.argv[1])
+from tensor_gemm_reduction_gb300 import binding as B
+lib = B.load_library()
+p = B.gemm_shard_plan_create_host(152, 32768, 8192, 8192, 16)
+ws = B.gemm_shard_workspace_size(p)
+k = (ctypes.c_int64 * 8)(*([896] * 8))
+ptr = lambda n, base: (ctypes.c_void_p * n)(*[base + 0x100000 * i for i in range(n)])
+lib.gemm_ar(p.handle, 1000, 7168, 8, k, ptr(8, 0x1000000), ptr(8, 0x9000000), ctypes.c_void_p(0x10000),
+            ctypes.c_void_p(0x20000000), ws, None)
+lib.gemm_ar(p.handle, 128, 7168, 8, k, ptr(8, 0x1000000), ptr(8, 0x9000000), ctypes.c_void_p(0x10000),
+            ctypes.c_void_p(0x20000000), ws, None)
+m = (ctypes.c_int64 * 8)(*([4096] * 8))
+lib.gemm_ag(p.handle, 6288, 7168, 8, m, ptr(8, 0x1000000), ctypes.c_void_p(0x9000000),
+            ctypes.c_void_p(0x10000), ctypes.c_void_p(0x20000000), ws, None)
+lib.gemm_ar(p.handle, 0, 7168, 8, k, ptr(8, 0x1000000), ptr(8, 0x9000000), ctypes.c_void_p(0x10000),
+            ctypes.c_void_p(0x20000000), ws, None)
+"""
+
+
+@pytest.mark.parametrize("value,expect", [("1", 3), ("0", 0), (None, 0)])
+def test_config_logging_env(lib, value, expect):
+    import subprocess
+    import sys
+    env = {k: v for k, v in os.environ.items() if k != "GSR_LOG_CONFIG"}
+    if value is not None:
+        env["GSR_LOG_CONFIG"] = value
+    r = subprocess.run([sys.executable, "-c", LOG_CLIENT, ROOT], capture_output=True, text=True,
+                       env=env, timeout=120)
+    assert r.returncode == 0, r.stderr
+    lines = [l for l in r.stderr.splitlines() if l.startswith("gsr: ")]
+    assert len(lines) == expect, r.stderr
+    if expect:
+        assert lines[0].startswith("gsr: ar M=1000 N=7168 R=8 kernel=main block_n=256 cta_group=2 "
+                                   "schedule=split_tail split=2 tiles=112")
+        assert "kernel=small" in lines[1] and "schedule=small_m" in lines[1]
+        assert lines[2].startswith("gsr: ag M=32768 N=6288 R=8 kernel=main") and "stream_k" in lines[2]
