@@ -165,16 +165,39 @@ def describe_workload(w) -> dict:
     return d
 
 
-def bench_config(w, world: int) -> dict:
+def parse_options(items) -> dict:
+    """--option NAME=VALUE pairs -> {GSR_OPT_* constant name: int}. NAME is the
+    option's name in gsr.h without the prefix, in any case (split_k, block_n,
+    schedule, raster_m, small_m, ...)."""
+    from tensor_gemm_reduction_gb300 import binding as B
+    out = {}
+    for item in items or ():
+        name, sep, value = item.partition("=")
+        key = "GSR_OPT_" + name.strip().upper()
+        if not sep or not hasattr(B, key):
+            known = sorted(k[8:].lower() for k in dir(B) if k.startswith("GSR_OPT_"))
+            raise SystemExit(f"--option {item!r}: expected NAME=VALUE with NAME one of {known}")
+        try:
+            out[key] = int(value, 0)
+        except ValueError:
+            raise SystemExit(f"--option {item!r}: the value must be an integer") from None
+    return out
+
+
+def bench_config(w, world: int, options: dict | None = None) -> dict:
     """The `config` object of the JSON line (the same for both arms; the seed of
-    the workload's generator, 2000 + M + K unless the workload fixes another)."""
+    the workload's generator, 2000 + M + K unless the workload fixes another;
+    plan options only when some were given)."""
     from tensor_gemm_reduction_gb300 import inputs as gi
     read = w.bytes - 2 * w.M * w.N
     l2 = ("inputs larger than L2: %.0f MB read per step" % (read / 1e6) if read > L2_BYTES else
           "inputs fit in L2 (%.1f MB per step): timed back to back without a flush" % (read / 1e6))
-    return dict(describe_workload(w), l2=l2,
-                parallelism="replicas" if world > 1 else "single",
-                seed=w.seed if w.seed is not None else gi.default_seed(w.M, w.K))
+    cfg = dict(describe_workload(w), l2=l2,
+               parallelism="replicas" if world > 1 else "single",
+               seed=w.seed if w.seed is not None else gi.default_seed(w.M, w.K))
+    if options:
+        cfg["options"] = {k[len("GSR_OPT_"):].lower(): v for k, v in options.items()}
+    return cfg
 
 
 class Runner:
@@ -328,7 +351,7 @@ def run_reference(args, w):
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws_, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": bench_config(w, ws_), "impl": "reference",
+        "config": bench_config(w, ws_, parse_options(args.option)), "impl": "reference",
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.threads(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -452,12 +475,16 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--context", choices=("torch_mm",), default=None,
                     help="time torch.mm (cuBLAS) on the concatenated operands instead (context only)")
+    ap.add_argument("--option", action="append", default=[], metavar="NAME=VALUE",
+                    help="plan option of gsr.h without its GSR_OPT_ prefix (repeatable), e.g. "
+                         "schedule=5 or block_n=192; recorded in config.options")
     ap.add_argument("--profile-window", action="store_true",
                     help="with --context: bracket one warm launch with cudaProfilerStart/Stop")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
     w = workload_by_name(args.workload)
+    options = parse_options(args.option)
 
     if args.context is not None:
         run_context_mm(args, w)
@@ -481,6 +508,8 @@ def main():
     pk = peaks()
 
     plan = B.gemm_shard_plan_create(local, 34816, 8192, 8192, 16)
+    for key, value in options.items():
+        B.gemm_shard_plan_set_option(plan, getattr(B, key), value)
     ws = B.gemm_shard_workspace_alloc(plan)
     B.gemm_shard_workspace_init(plan, ws)
     run = Runner(w, plan, ws, dev)
@@ -513,7 +542,7 @@ def main():
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": region_s / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": bench_config(w, world),
+        "config": bench_config(w, world, options),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": ncu_traffic(w.name),
                      "peak_kind": ("sustained" if sustained else "burst") + " bf16, " + pk["source"] +

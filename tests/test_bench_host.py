@@ -166,3 +166,19 @@ def test_config_states_whether_the_inputs_exceed_l2():
     assert bench.bench_config(bench.workload_by_name("ag_kda_m32768"), 1)["l2"].startswith(
         "inputs larger than L2: 560 MB")
     assert "fit in L2" in bench.bench_config(bench.workload_by_name("ar_tiny"), 1)["l2"]
+
+
+def test_plan_options_parse_and_are_recorded():
+    from tensor_gemm_reduction_gb300 import binding as B
+    opts = bench.parse_options(["schedule=5", "BLOCK_N=192", "raster_n=0x4"])
+    assert opts == {"GSR_OPT_SCHEDULE": 5, "GSR_OPT_BLOCK_N": 192, "GSR_OPT_RASTER_N": 4}
+    assert all(hasattr(B, k) for k in opts)
+    w = bench.workload_by_name("ag_mla_m2048")
+    assert bench.bench_config(w, 1, opts)["options"] == {"schedule": 5, "block_n": 192, "raster_n": 4}
+    assert "options" not in bench.bench_config(w, 1, {})
+    for bad in (["nosuch=1"], ["schedule"], ["schedule=fast"]):
+        with pytest.raises(SystemExit):
+            bench.parse_options(bad)
+    r = _bench(["--impl", "reference", "--workload", "ar_tiny", "--steps", "3", "--warmup", "3",
+                "--option", "split_k=2"])
+    assert json.loads(r.stdout)["config"]["options"] == {"split_k": 2}
