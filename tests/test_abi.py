@@ -685,3 +685,22 @@ def test_config_logging_env(lib, value, expect):
                                    "schedule=split_tail split=2 tiles=112")
         assert "kernel=small" in lines[1] and "schedule=small_m" in lines[1]
         assert lines[2].startswith("gsr: ag M=32768 N=6288 R=8 kernel=main") and "stream_k" in lines[2]
+
+
+def test_last_error_string_is_per_thread(lib, host):
+    """gsr_last_error_string is thread-local: another thread's failure in between
+    does not replace this thread's message."""
+    import threading
+    barrier = threading.Barrier(2)
+    seen = {}
+
+    def worker(name, call):
+        assert call() == B.GSR_ERR_INVALID_VALUE
+        barrier.wait()           # both threads have failed, each its own way
+        barrier.wait()
+        seen[name] = B.gsr_last_error_string()
+
+    t1 = threading.Thread(target=worker, args=("m", lambda: host.ar(-1, 256, [128])))
+    t2 = threading.Thread(target=worker, args=("r", lambda: host.ar(16, 256, [8] * 17)))
+    t1.start(); t2.start(); t1.join(); t2.join()
+    assert "M must be" in seen["m"] and "R=17" in seen["r"]
