@@ -704,3 +704,30 @@ def test_last_error_string_is_per_thread(lib, host):
     t2 = threading.Thread(target=worker, args=("r", lambda: host.ar(16, 256, [8] * 17)))
     t1.start(); t2.start(); t1.join(); t2.join()
     assert "M must be" in seen["m"] and "R=17" in seen["r"]
+
+
+@pytest.mark.parametrize("name,good,bad", [
+    ("SPLIT_K", [0, 1, 16], [-1, 17]),
+    ("BLOCK_N", [0, 128, 192, 256], [64, 200, 512]),
+    ("TIMEOUT_NS", [0, 1, 10**12], [-1]),
+    ("MAX_CTAS", [0, 1, 2**31 - 1], [-1, 2**31]),
+    ("RASTER_M", [0, 1, 64], [-1, 65]),
+    ("RASTER_N", [0, 1, 64], [-1, 65]),
+    ("L2_HINTS", [0, 3], [-1, 4]),
+    ("CTA_GROUP", [0, 1, 2], [-1, 3]),
+    ("SCHEDULE", [0, 5], [-1, 6]),
+    ("SMALL_M", [0, 2], [-1, 3]),
+    ("SMALL_TILE_ROWS", [0, 8, 128], [-8, 4, 136]),
+])
+def test_every_option_checks_its_range(host, name, good, bad):
+    opt = getattr(B, "GSR_OPT_" + name)
+    for v in good:
+        assert host.lib.gemm_shard_plan_set_option(host.plan.handle, opt, v) == B.GSR_OK, (name, v)
+    for v in bad:
+        assert host.lib.gemm_shard_plan_set_option(host.plan.handle, opt, v) == \
+            B.GSR_ERR_INVALID_VALUE, (name, v)
+
+
+def test_unknown_option_is_rejected(host):
+    assert host.lib.gemm_shard_plan_set_option(host.plan.handle, 99, 1) == B.GSR_ERR_INVALID_VALUE
+    assert "unknown option" in B.gsr_last_error_string()
