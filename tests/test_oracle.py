@@ -377,3 +377,14 @@ def test_pins_catch_mutant(oracle_mod, tmp_path, monkeypatch, name):
     assert _pins_pass(oracle_mod), "pins must pass on the real oracle"
     monkeypatch.setattr(oracle_mod, "_lib", lib)
     assert not _pins_pass(oracle_mod), f"mutant {name} survived every pin"
+
+
+def test_oracle_source_compiles_warning_free():
+    """The oracle's C builds without warnings, with OpenMP and without it."""
+    import subprocess
+    src = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "oracle",
+                       "gsr_oracle.c")
+    for extra in (["-fopenmp"], ["-Wno-unknown-pragmas"]):
+        r = subprocess.run(["gcc", "-std=c11", "-O2", "-Wall", "-Wextra", "-Werror", "-fsyntax-only",
+                            *extra, src], capture_output=True, text=True)
+        assert r.returncode == 0, r.stderr
