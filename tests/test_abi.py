@@ -731,3 +731,27 @@ def test_every_option_checks_its_range(host, name, good, bad):
 def test_unknown_option_is_rejected(host):
     assert host.lib.gemm_shard_plan_set_option(host.plan.handle, 99, 1) == B.GSR_ERR_INVALID_VALUE
     assert "unknown option" in B.gsr_last_error_string()
+
+
+def _noalloc(h, M, N, K_r):
+    R = len(K_r)
+    return h.lib.gemm_ar_noalloc(h.plan.handle, M, N, R, _arr(ctypes.c_int64, K_r),
+                                 _arr(ctypes.c_void_p, [0x100000 * (r + 1) for r in range(R)]),
+                                 _arr(ctypes.c_void_p, [0x8000000 + 0x100000 * r for r in range(R)]),
+                                 ctypes.c_void_p(0x10000), None)
+
+
+def test_noalloc_fits_the_builtin_scratch_or_says_why(lib):
+    h = Host(lib, sm=152)
+    # Every heuristic shape fits (the uniform schedule where the plan's own
+    # configuration would need more than 24 MiB): valid up to the launch point.
+    for M in (0, 1, 128, 1000, 4096, 32768):
+        assert _noalloc(h, M, 7168, [896] * 8) == (B.GSR_OK if M == 0 else B.GSR_ERR_UNSUPPORTED)
+        if M:
+            assert "arguments are valid" in B.gsr_last_error_string()
+    # A forced 16-way split on 3584 tiles needs far more: rejected before any launch.
+    B.gemm_shard_plan_set_option(h.plan, B.GSR_OPT_SPLIT_K, 16)
+    assert _noalloc(h, 32768, 7168, [896] * 8) == B.GSR_ERR_WORKSPACE
+    assert "built-in scratch" in B.gsr_last_error_string()
+    # Argument errors come first, as for gemm_ar.
+    assert _noalloc(h, 16, 252, [128]) == B.GSR_ERR_INVALID_VALUE
