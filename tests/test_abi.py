@@ -755,3 +755,37 @@ def test_noalloc_fits_the_builtin_scratch_or_says_why(lib):
     assert "built-in scratch" in B.gsr_last_error_string()
     # Argument errors come first, as for gemm_ar.
     assert _noalloc(h, 16, 252, [128]) == B.GSR_ERR_INVALID_VALUE
+
+
+def test_replicated_ar_validation(host):
+    lib = host.lib
+
+    def call(y, M=16):
+        K = _arr(ctypes.c_int64, [128, 128])
+        X = _arr(ctypes.c_void_p, [0x100000, 0x200000])
+        W = _arr(ctypes.c_void_p, [0x300000, 0x400000])
+        Y = None if y is None else _arr(ctypes.c_void_p, y)
+        return lib.gemm_ar_replicated(host.plan.handle, M, 256, 2, K, X, W, Y,
+                                      ctypes.c_void_p(0x20000000), host.ws_bytes, None)
+
+    assert call([0x10000, 0x20000]) == B.GSR_ERR_UNSUPPORTED           # valid: stops at the launch
+    assert call(None) == B.GSR_ERR_INVALID_VALUE
+    assert call([0x10000, 0]) == B.GSR_ERR_INVALID_VALUE
+    assert call([0x10000, 0x20008]) == B.GSR_ERR_INVALID_VALUE
+    assert "16-byte" in B.gsr_last_error_string()
+    assert call([0, 0], M=0) == B.GSR_OK                                # nothing to write
+
+
+def test_workspace_init_checks(host):
+    lib = host.lib
+    need = host.ws_bytes
+    assert lib.gemm_shard_workspace_init(host.plan.handle, None, need, None) == B.GSR_ERR_WORKSPACE
+    assert lib.gemm_shard_workspace_init(host.plan.handle, ctypes.c_void_p(0x20000010), need,
+                                         None) == B.GSR_ERR_WORKSPACE
+    assert lib.gemm_shard_workspace_init(host.plan.handle, ctypes.c_void_p(0x20000000), 64,
+                                         None) == B.GSR_ERR_WORKSPACE
+    assert "too small" in B.gsr_last_error_string()
+    assert lib.gemm_shard_workspace_init(host.plan.handle, ctypes.c_void_p(0x20000000), need,
+                                         None) == B.GSR_ERR_UNSUPPORTED
+    assert lib.gemm_shard_workspace_init(None, ctypes.c_void_p(0x20000000), need, None) == \
+        B.GSR_ERR_INVALID_VALUE
