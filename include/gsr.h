@@ -294,27 +294,44 @@ gsr_status gemm_shard_signal(const gemm_shard_plan *plan, uint32_t *flag, uint32
  *   - When the plan's configuration for a shape needs more than 24 MiB of
  *     scratch, the call runs the uniform schedule instead (the same results
  *     within rounding; split pieces then need at most one 128 KiB slot per
- *     SM). A shape that needs more even then (for example a forced split-K on
- *     many tiles) is rejected with GSR_ERR_WORKSPACE before anything is
+ *     SM), unless the plan forces a split (GSR_OPT_SPLIT_K) or a schedule
+ *     (GSR_OPT_SCHEDULE): a forced configuration is never replaced, and one
+ *     that does not fit is rejected with GSR_ERR_WORKSPACE before anything is
  *     launched; use gemm_ar with a workspace for it. The uniform schedule
  *     always fits when 4 bytes x (ceil(max_M/128) + 2 max_R) x ceil(max_N/128)
  *     counters plus 128 KiB per SM stay under 24 MiB (on a 152-SM GB300:
- *     plans of up to about a million output tiles).
+ *     plans of up to about a million output tiles). Where the configuration
+ *     is the plan's own (gemm_shard_describe reports it), the result is
+ *     bit-identical to gemm_ar's.
  *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress), once per device; make that first call before
- *     any stream capture begins.
+ *     (cudaGetSymbolAddress) and keeps it for that device's context; make
+ *     that first call before any stream capture begins. The lookup is
+ *     repeated only when the device's context has changed (after a
+ *     cudaDeviceReset, the library image and its array are loaded again) or
+ *     on a thread where no context is current yet.
  *   - Every call on a device shares the one array and starts by clearing its
  *     status word and counters (a stream-ordered memset). Calls that may
  *     overlap on the GPU (different streams, or different host threads without
  *     ordering) race on it and must not be issued.
- *   - A bounded in-kernel wait that runs out is not reported back (there is
- *     no workspace to pass to gemm_shard_check_status); use gemm_ar where that
- *     report is needed.
+ *   - A bounded in-kernel wait that runs out leaves its code in the array's
+ *     status word: gemm_ar_noalloc_check_status reads it. The next call
+ *     clears it, so read it before the next call.
  * Arguments, validation and results are those of gemm_ar.
  */
 gsr_status gemm_ar_noalloc(const gemm_shard_plan *plan, int64_t M, int64_t N, int R,
                            const int64_t *K_r, const void *const *X_r,
                            const void *const *W_r, void *Y, gsr_stream_t stream);
+
+/*
+ * gemm_shard_check_status for gemm_ar_noalloc: synchronise `stream`, read the
+ * built-in scratch's status word on the plan's device, clear it and return
+ * GSR_OK or GSR_ERR_TIMEOUT (the code of the first wait that ran out is in
+ * gsr_last_error_string). It reports on the last gemm_ar_noalloc call on that
+ * device, whichever plan made it. (The pages have no counterpart.)
+ * GSR_ERR_INVALID_VALUE for a NULL plan, GSR_ERR_UNSUPPORTED on a host plan,
+ * GSR_ERR_CUDA if the copy fails.
+ */
+gsr_status gemm_ar_noalloc_check_status(const gemm_shard_plan *plan, gsr_stream_t stream);
 
 /*
  * Packed gather of per-shard states (the pages' "Kimi K3 SP: pack the per-layer

@@ -53,7 +53,7 @@ EXPORTED = (
     "gemm_shard_workspace_size", "gemm_shard_workspace_init", "gemm_ar", "gemm_rs",
     "gemm_ag", "gemm_shard_check_status", "gsr_last_error_string", "gemm_shard_describe",
     "gemm_ar_noalloc", "gemm_ag_flagged", "gemm_shard_signal", "gemm_ar_replicated",
-    "gemm_shard_pack_gather",
+    "gemm_shard_pack_gather", "gemm_ar_noalloc_check_status",
 )
 
 
@@ -109,6 +109,7 @@ def load_library() -> ctypes.CDLL:
     lib.gemm_shard_signal.argtypes = [vp, vp, ctypes.c_uint32, vp]
     lib.gemm_shard_pack_gather.argtypes = [vp, i32, i64_arr, i32, i64, ptr_arr, i64, vp, vp, sz, vp]
     lib.gemm_shard_check_status.argtypes = [vp, vp, vp]
+    lib.gemm_ar_noalloc_check_status.argtypes = [vp, vp]
     lib.gsr_last_error_string.restype = ctypes.c_char_p
     lib.gemm_shard_describe.argtypes = [vp, i32, i64, i64, i64, i32, i64_arr,
                                         ctypes.POINTER(GsrConfig)]
@@ -311,6 +312,12 @@ def gemm_ar_noalloc(plan: Plan, X_r: Sequence[torch.Tensor], W_r: Sequence[torch
     _check(load_library().gemm_ar_noalloc(plan.handle, M, N, R, k, xp, wp,
                                           ctypes.c_void_p(Y.data_ptr()), _stream(stream)))
     return Y
+
+
+def gemm_ar_noalloc_check_status(plan: Plan, stream=None) -> None:
+    """Synchronise, then raise GsrError(GSR_ERR_TIMEOUT) if the last
+    gemm_ar_noalloc call on the plan's device had an in-kernel wait run out."""
+    _check(load_library().gemm_ar_noalloc_check_status(plan.handle, _stream(stream)))
 
 
 def _rs_args(plan, X_r, W_r, Y_r, ws, M=None):

@@ -984,24 +984,35 @@ gsr_status gemm_shard_pack_gather(const gemm_shard_plan* P, int R, const int64_t
   return ok();
 }
 
+}  // extern "C"
+
+namespace {
+// Reads the status word at `word_addr` after synchronising the stream, clears
+// it if it is set, and turns it into GSR_OK or GSR_ERR_TIMEOUT.
+gsr_status read_and_clear_status(int device, void* word_addr, cudaStream_t st) {
+  DeviceScope scope(device);
+  if (scope.err != cudaSuccess) return cuda_fail(scope.err, "selecting the plan's device");
+  uint32_t word = 0;
+  cudaError_t e = cudaMemcpyAsync(&word, word_addr, sizeof word, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the status word");
+  if (word == 0) return ok();
+  e = cudaMemsetAsync(word_addr, 0, sizeof word, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "clearing the status word");
+  return fail(GSR_ERR_TIMEOUT, "in-kernel wait ran out (code 0x%08x: role %u, site %u)", word,
+              (word >> 8) & 0xFFu, word & 0xFFu);
+}
+}  // namespace
+
+extern "C" {
+
 gsr_status gemm_shard_check_status(const gemm_shard_plan* P, void* ws, gsr_stream_t stream) {
   gsr_status s = check_plan(P);
   if (s) return s;
   if (!ws) return fail(GSR_ERR_WORKSPACE, "workspace is NULL");
   if (P->device < 0) return fail(GSR_ERR_UNSUPPORTED, "host plan: no device status to read");
-  DeviceScope scope(P->device);
-  if (scope.err != cudaSuccess) return cuda_fail(scope.err, "selecting the plan's device");
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  uint32_t word = 0;
-  cudaError_t e = cudaMemcpyAsync(&word, ws, sizeof word, cudaMemcpyDeviceToHost, st);
-  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
-  if (e != cudaSuccess) return cuda_fail(e, "reading the workspace status word");
-  if (word == 0) return ok();
-  e = cudaMemsetAsync(ws, 0, sizeof word, st);
-  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
-  if (e != cudaSuccess) return cuda_fail(e, "clearing the workspace status word");
-  return fail(GSR_ERR_TIMEOUT, "in-kernel wait ran out (code 0x%08x: role %u, site %u)", word,
-              (word >> 8) & 0xFFu, word & 0xFFu);
+  return read_and_clear_status(P->device, ws, reinterpret_cast<cudaStream_t>(stream));
 }
 
 gsr_status gemm_shard_describe(const gemm_shard_plan* P, int mode, int64_t M, int64_t N, int64_t K,
@@ -1059,23 +1070,61 @@ constexpr int kScratchDevices = 64;
 static __device__ __align__(256) unsigned char gsr_builtin_scratch[kBuiltinScratchBytes];
 
 namespace {
-std::mutex g_scratch_mutex;
-void* g_scratch_addr[kScratchDevices] = {};
+// The context a cached address belongs to, through the driver's entry points
+// (the library links no driver library). A cudaDeviceReset, or any other end
+// of the device's primary context, unloads the library image; the next context
+// loads it again, possibly at another address.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+CtxGetCurrentFn g_ctx_current = nullptr;
+CtxGetIdFn g_ctx_id = nullptr;
+std::once_flag g_ctx_fns_once;
 
-// Device address of the scratch array on `device`, looked up once per device
-// (the device must be current). Host code cannot use the array's name as an
-// address: on the host it names a shadow object, not device memory.
+// The current context's unique id; false if there is none on this thread or
+// the driver does not offer the query.
+bool current_context_id(unsigned long long* id) {
+  std::call_once(g_ctx_fns_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      g_ctx_current = reinterpret_cast<CtxGetCurrentFn>(fn);
+    fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      g_ctx_id = reinterpret_cast<CtxGetIdFn>(fn);
+  });
+  CUcontext ctx = nullptr;
+  if (!g_ctx_current || !g_ctx_id || g_ctx_current(&ctx) != CUDA_SUCCESS || !ctx) return false;
+  return g_ctx_id(ctx, id) == CUDA_SUCCESS;
+}
+
+struct ScratchSlot {
+  void* addr = nullptr;
+  unsigned long long ctx_id = 0;
+};
+std::mutex g_scratch_mutex;
+ScratchSlot g_scratch[kScratchDevices];
+
+// Device address of the scratch array on `device` (which must be current),
+// looked up once per device and context. Host code cannot use the array's
+// name as an address: on the host it names a shadow object, not device memory.
 gsr_status builtin_scratch_address(int device, void** out) {
   if (device < 0 || device >= kScratchDevices)
     return fail(GSR_ERR_UNSUPPORTED, "device ordinal %d has no built-in scratch slot", device);
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  if (!g_scratch_addr[device]) {
+  ScratchSlot& slot = g_scratch[device];
+  unsigned long long id = 0;
+  const bool have_id = current_context_id(&id);
+  if (!slot.addr || !have_id || id != slot.ctx_id) {
     void* p = nullptr;
     cudaError_t e = cudaGetSymbolAddress(&p, gsr_builtin_scratch);
     if (e != cudaSuccess) return cuda_fail(e, "looking up the built-in scratch address");
-    g_scratch_addr[device] = p;
+    slot.addr = p;
+    // The lookup makes the device's primary context current on this thread.
+    slot.ctx_id = current_context_id(&id) ? id : 0;
   }
-  *out = g_scratch_addr[device];
+  *out = slot.addr;
   return ok();
 }
 }  // namespace
@@ -1089,9 +1138,12 @@ extern "C" gsr_status gemm_ar_noalloc(const gemm_shard_plan* P, int64_t M, int64
   if (s) return s;
   // The plan's own configuration when its scratch fits; otherwise the uniform
   // schedule, whose split pieces need at most one 128 KiB slot per SM.
+  // A schedule or split the caller forced through a plan option is kept (the
+  // call is then rejected if it does not fit), since another schedule would
+  // change the summation order.
   gemm_shard_plan fitted = *P;
   if (choose_config(P, gsr::kModeAR, M, N, 0, R, K_r).ws_bytes > kBuiltinScratchBytes &&
-      P->opt_split == 0)
+      P->opt_split == 0 && P->opt_schedule == 0)
     fitted.opt_schedule = 1;
   const Config c = choose_config(&fitted, gsr::kModeAR, M, N, 0, R, K_r);
   if (c.ws_bytes > kBuiltinScratchBytes)
@@ -1116,3 +1168,14 @@ extern "C" gsr_status gemm_ar_noalloc(const gemm_shard_plan* P, int64_t M, int64
                       kBuiltinScratchBytes, stream);
 }
 
+extern "C" gsr_status gemm_ar_noalloc_check_status(const gemm_shard_plan* P, gsr_stream_t stream) {
+  gsr_status s = check_plan(P);
+  if (s) return s;
+  if (P->device < 0) return fail(GSR_ERR_UNSUPPORTED, "host plan: no device status to read");
+  DeviceScope scope(P->device);
+  if (scope.err != cudaSuccess) return cuda_fail(scope.err, "selecting the plan's device");
+  void* scratch = nullptr;
+  s = builtin_scratch_address(P->device, &scratch);
+  if (s) return s;
+  return read_and_clear_status(P->device, scratch, reinterpret_cast<cudaStream_t>(stream));
+}

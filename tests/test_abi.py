@@ -757,6 +757,31 @@ def test_noalloc_fits_the_builtin_scratch_or_says_why(lib):
     assert _noalloc(h, 16, 252, [128]) == B.GSR_ERR_INVALID_VALUE
 
 
+def test_noalloc_keeps_a_forced_schedule(lib):
+    """M=2560, N=7168: the heuristic's stream-K tail needs more than the
+    built-in 24 MiB, so an unforced plan falls back to the uniform schedule,
+    but a plan that forces stream-K (schedule 2, or 4: stream-K with the
+    whole tiles first) is rejected instead of silently summing in another
+    order."""
+    h = Host(lib, sm=152)
+    d = B.gemm_shard_describe(h.plan, B.MODE_AR, 2560, 7168, 0, [896] * 8)
+    assert d["schedule"] == 2 and d["workspace_bytes"] > 24 << 20
+    assert _noalloc(h, 2560, 7168, [896] * 8) == B.GSR_ERR_UNSUPPORTED   # valid: falls back
+    for sched in (2, 4):
+        f = Host(lib, sm=152)
+        B.gemm_shard_plan_set_option(f.plan, B.GSR_OPT_SCHEDULE, sched)
+        d = B.gemm_shard_describe(f.plan, B.MODE_AR, 2560, 7168, 0, [896] * 8)
+        assert d["workspace_bytes"] > 24 << 20
+        assert _noalloc(f, 2560, 7168, [896] * 8) == B.GSR_ERR_WORKSPACE, sched
+        assert "built-in scratch" in B.gsr_last_error_string()
+
+
+def test_noalloc_status_query_on_a_host_plan(lib):
+    h = Host(lib, sm=152)
+    assert lib.gemm_ar_noalloc_check_status(h.plan.handle, None) == B.GSR_ERR_UNSUPPORTED
+    assert lib.gemm_ar_noalloc_check_status(None, None) == B.GSR_ERR_INVALID_VALUE
+
+
 def test_replicated_ar_validation(host):
     lib = host.lib
 
