@@ -13,6 +13,16 @@ def pytest_configure(config):
         "markers", "gpu: needs a GB300 (sm_103a) GPU and the built CUDA library")
 
 
+def pytest_terminal_summary(terminalreporter):
+    """Print the full-size element-wise parity lines, if any test recorded one."""
+    util = sys.modules.get("gpu_util")
+    lines = getattr(util, "PARITY_LOG", None) if util else None
+    if lines:
+        terminalreporter.section("element-wise parity against the oracle")
+        for line in lines:
+            terminalreporter.write_line(line)
+
+
 @pytest.fixture(scope="session")
 def oracle_mod():
     import oracle

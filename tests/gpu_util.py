@@ -89,3 +89,54 @@ def shards_to(dev, tensors, reverse_order=False):
 
 def bits_of(t: torch.Tensor) -> np.ndarray:
     return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+# One line per element-wise comparison at full size, printed in the run's
+# terminal summary (conftest.py).
+PARITY_LOG: list = []
+
+
+class ParityStats:
+    """Running element-wise comparison of a GPU output with the oracle, block by
+    block: the count of elements over |y - ref| <= RTOL*|ref| + ATOL, the max
+    abs error, the max relative error over |ref| >= ATOL, and how much of the
+    bound the worst element used."""
+
+    def __init__(self, what: str):
+        self.what = what
+        self.n = 0
+        self.bad = 0
+        self.nonfinite = 0
+        self.max_abs = 0.0
+        self.max_rel = 0.0
+        self.max_bound_use = 0.0
+
+    def add(self, y: np.ndarray, ref: np.ndarray) -> None:
+        assert y.shape == ref.shape, (y.shape, ref.shape)
+        self.n += y.size
+        fin = np.isfinite(y)
+        self.nonfinite += int(y.size - np.count_nonzero(fin))
+        err = np.abs(y - ref)
+        aref = np.abs(ref)
+        bound = RTOL * aref + ATOL
+        self.bad += int(np.count_nonzero(~(err <= bound)))
+        if y.size:
+            self.max_abs = max(self.max_abs, float(np.nanmax(np.where(fin, err, 0.0))))
+            self.max_bound_use = max(self.max_bound_use,
+                                     float(np.nanmax(np.where(fin, err / bound, np.inf))))
+            big = aref >= ATOL
+            if big.any():
+                self.max_rel = max(self.max_rel,
+                                   float(np.nanmax(np.where(fin & big, err, 0.0)[big] / aref[big])))
+
+    def line(self) -> str:
+        return (f"{self.what}: {self.n} elements, {self.bad} over the bound, "
+                f"{self.nonfinite} non-finite; max abs err {self.max_abs:.3g}, "
+                f"max rel err {self.max_rel:.3g} (|ref| >= {ATOL:g}), "
+                f"worst element at {self.max_bound_use:.3f} of its bound")
+
+    def finish(self, expect_elements: int | None = None) -> None:
+        PARITY_LOG.append(self.line())
+        if expect_elements is not None:
+            assert self.n == expect_elements, f"{self.what}: compared {self.n} of {expect_elements}"
+        assert self.nonfinite == 0 and self.bad == 0, self.line()
