@@ -19,6 +19,7 @@ ranks over the slowest rank's time.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import math
@@ -34,6 +35,11 @@ sys.path.insert(0, ROOT)
 METRIC = "BF16 TFLOP/s per mode vs M on 1 GB300; % of dense BF16 peak; oracle time"
 ROW_PAUSE_S = 0.3   # idle pause before each per-workload row (see sweep)
 L2_BYTES = 126 * 1024 * 1024
+# GB300 datasheet figures (dense bf16 tensor throughput, HBM3e bandwidth). The
+# roofline's `peak` is the measured one (a cuBLAS GEMM and a device copy on
+# this machine); these give the second fraction, against the nominal part.
+NOMINAL_BF16_TFLOPS = 2250.0
+NOMINAL_HBM_GBS = 7900.0
 
 
 def log(*a):
@@ -80,6 +86,121 @@ def ncu_traffic(workload: str):
     if not e or e.get("kernel_hash") != kernel_source_hash():
         return None
     return e.get("dram_bytes_per_launch")
+
+
+class NvmlField(ctypes.Structure):
+    """nvmlFieldValue_t: one field query and its 8-byte value."""
+    _fields_ = [("fieldId", ctypes.c_uint), ("scopeId", ctypes.c_uint),
+                ("timestamp", ctypes.c_longlong), ("latencyUsec", ctypes.c_longlong),
+                ("valueType", ctypes.c_int), ("nvmlReturn", ctypes.c_int),
+                ("value", ctypes.c_ulonglong)]
+
+
+class NvmlClockSampler:
+    """SM clock, power and clock-event reasons read in-process through NVML
+    (read-only queries; no setting is touched) every ~1 ms on a background
+    thread, so that a timed region of a few tens of milliseconds still holds
+    tens of samples. Only samples taken between mark_start() and mark_end()
+    enter the summary. NVML is loaded with ctypes from the driver's own
+    library; where it is missing, start() returns False."""
+    SM = 1                      # NVML_CLOCK_SM
+    POWER_INSTANT = 186         # NVML_FI_DEV_POWER_INSTANT
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown"}
+
+    def __init__(self, cuda_index: int, interval_s: float = 0.001):
+        self.cuda_index = cuda_index
+        self.interval = interval_s
+        self.samples = []          # (t, sm_mhz, power_w, reasons_mask)
+        self.t0 = self.t1 = None
+        self._stop = False
+        self._thread = None
+        self.nvml = None
+        self.handle = None
+        self.max_mhz = None
+
+    def _open(self) -> bool:
+        import torch
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+        except OSError:
+            return False
+        if nv.nvmlInit_v2() != 0:
+            return False
+        self.nvml = nv
+        h = ctypes.c_void_p()
+        pr = torch.cuda.get_device_properties(self.cuda_index)
+        bus = f"{pr.pci_domain_id:08x}:{pr.pci_bus_id:02x}:{pr.pci_device_id:02x}.0".encode()
+        if nv.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(bus), ctypes.byref(h)) != 0 and \
+                nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.cuda_index), ctypes.byref(h)) != 0:
+            return False
+        self.handle = h
+        mx = ctypes.c_uint()
+        if nv.nvmlDeviceGetMaxClockInfo(h, self.SM, ctypes.byref(mx)) == 0:
+            self.max_mhz = float(mx.value)
+        self._reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        return True
+
+    def _read(self):
+        nv, h = self.nvml, self.handle
+        mhz, mw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        f = NvmlField(fieldId=self.POWER_INSTANT)
+        sm = float(mhz.value) if nv.nvmlDeviceGetClockInfo(h, self.SM, ctypes.byref(mhz)) == 0 else None
+        if nv.nvmlDeviceGetFieldValues(h, 1, ctypes.byref(f)) == 0 and f.nvmlReturn == 0:
+            watts = f.value / 1000.0
+        elif nv.nvmlDeviceGetPowerUsage(h, ctypes.byref(mw)) == 0:
+            watts = mw.value / 1000.0
+        else:
+            watts = None
+        mask = int(rs.value) if self._reasons(h, ctypes.byref(rs)) == 0 else 0
+        return sm, watts, mask
+
+    def _loop(self):
+        while not self._stop:
+            t = time.perf_counter()
+            self.samples.append((t,) + self._read())
+            time.sleep(self.interval)
+
+    def start(self) -> bool:
+        import threading
+        if not self._open():
+            return False
+        self._thread = threading.Thread(target=self._loop, daemon=True)
+        self._thread.start()
+        time.sleep(0.02)
+        return True
+
+    def mark_start(self):
+        self.t0 = time.perf_counter()
+
+    def mark_end(self):
+        self.t1 = time.perf_counter()
+
+    def stop(self):
+        if self._thread is not None:
+            time.sleep(0.005)
+            self._stop = True
+            self._thread.join(timeout=5)
+        if self.nvml is not None:
+            self.nvml.nvmlShutdown()
+
+    def summary(self):
+        inside = [x for x in self.samples if self.t0 is not None and self.t0 <= x[0] <= self.t1]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["no samples"],
+                    "source": "nvml"}
+        sm = [x[1] for x in inside if x[1] is not None]
+        pw = [x[2] for x in inside if x[2] is not None]
+        reasons = sorted({name for x in inside for bit, name in self.REASONS.items() if x[3] & bit})
+        span = (self.t1 - self.t0) * 1e3
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_mhz_min": min(sm) if sm else None, "sm_max_mhz": self.max_mhz,
+                "power_w_median": statistics.median(pw) if pw else None,
+                "power_w_max": max(pw) if pw else None, "samples": len(inside),
+                "region_ms_host": span, "reasons": reasons,
+                "source": "nvml, in-process, ~%g ms apart, samples inside the timed region only"
+                          % (self.interval * 1e3)}
 
 
 class ClockSampler:
@@ -249,9 +370,10 @@ def trimmed_mean(xs, cut: float = 0.25):
     return sum(mid) / len(mid)
 
 
-def time_launches(fn, steps: int, warmup: int, flush=None):
+def time_launches(fn, steps: int, warmup: int, flush=None, marks=None):
     """Per-launch CUDA-event durations (ms) on the current stream, plus the
-    elapsed time of the whole region (ms)."""
+    elapsed time of the whole region (ms). `marks` (a clock sampler) is told
+    when the region starts and when the synchronise after it returns."""
     import torch
     for _ in range(warmup):
         if flush is not None:
@@ -262,6 +384,8 @@ def time_launches(fn, steps: int, warmup: int, flush=None):
           for _ in range(steps)]
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    if marks is not None:
+        marks.mark_start()
     t0.record()
     for s, e in ev:
         if flush is not None:
@@ -271,6 +395,8 @@ def time_launches(fn, steps: int, warmup: int, flush=None):
         e.record()
     t1.record()
     torch.cuda.synchronize()
+    if marks is not None:
+        marks.mark_end()
     return [s.elapsed_time(e) for s, e in ev], t0.elapsed_time(t1)
 
 
@@ -387,6 +513,9 @@ def sweep(plan, ws, dev, pk, names):
                      "us": round(t * 1e6, 2), "tflops": round(w.flops / t / 1e12, 1),
                      "hbm_gbs": round(w.bytes / t / 1e9, 1),
                      "roofline_frac": round(t_roof / t, 3),
+                     "roofline_frac_nominal": round(
+                         max(w.flops / (NOMINAL_BF16_TFLOPS * 1e12),
+                             w.bytes / (NOMINAL_HBM_GBS * 1e9)) / t, 3),
                      "bound": "tensor" if w.flops / (pk["bf16_burst"] * 1e12) >= w.bytes / (pk["hbm_gbs"] * 1e9) else "hbm",
                      "split": d["split"], "block_n": d["block_n"],
                      "kernel": "small_m" if d["schedule"] == 3 else "main"})
@@ -413,7 +542,8 @@ def sweep_pack(plan, ws, dev, pk):
     t = trimmed_mean(times) * 1e-3
     row = {"workload": w.name, "mode": "pack", "R": w.R, "M_r": w.M_r, "T": w.T, "H": w.H,
            "rows_out": w.rows_out, "us": round(t * 1e6, 2), "hbm_gbs": round(w.bytes / t / 1e9, 1),
-           "roofline_frac": round(w.bytes / (pk["hbm_gbs"] * 1e9) / t, 3), "bound": "hbm",
+           "roofline_frac": round(w.bytes / (pk["hbm_gbs"] * 1e9) / t, 3),
+           "roofline_frac_nominal": round(w.bytes / (NOMINAL_HBM_GBS * 1e9) / t, 3), "bound": "hbm",
            "kernel": "pack"}
     del S, P, flush_buf
     torch.cuda.empty_cache()
@@ -520,17 +650,21 @@ def main():
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    with ClockSampler(local) as clk:
-        t_wall = time.perf_counter()
-        times, region_ms = time_launches(run, steps=args.steps, warmup=0)
-        t_wall = time.perf_counter() - t_wall
+    nvml = NvmlClockSampler(local)
+    if nvml.start():
+        times, region_ms = time_launches(run, steps=args.steps, warmup=0, marks=nvml)
+        nvml.stop()
+        clocks = nvml.summary()
+    else:
+        with ClockSampler(local) as clk:
+            times, region_ms = time_launches(run, steps=args.steps, warmup=0)
+        clocks = clk.summary()
     if world > 1:
         dist.barrier()
     B.gemm_shard_check_status(plan, ws)
     value, region_s = replica_value(region_ms * 1e-3, w.flops * args.steps, world)
     avg_launch_s = statistics.mean(times) * 1e-3
     achieved = w.flops / avg_launch_s / 1e12
-    clocks = clk.summary()
     # The sustained peak is a seconds-long back-to-back loop held at the power
     # limit; it is the matching denominator whenever this loop ran into the
     # same limit (or lasted as long), the burst peak otherwise.
@@ -548,6 +682,10 @@ def main():
                      "peak_kind": ("sustained" if sustained else "burst") + " bf16, " + pk["source"] +
                                   (" (the loop ran at the power limit: sw_power_cap)" if capped else ""),
                      "frac_of_burst": achieved / pk["bf16_burst"],
+                     "nominal_peak": NOMINAL_BF16_TFLOPS,
+                     "frac_of_nominal": achieved / NOMINAL_BF16_TFLOPS,
+                     "peak_note": "peak and frac: of measured (cuBLAS bf16 GEMM on this pool's "
+                                  "GB300s); frac_of_nominal: of the datasheet dense bf16 peak",
                      "algorithmic_flops_per_launch": w.flops, "avg_launch_us": avg_launch_s * 1e6},
         "gpu_launches": args.steps,
         "clocks": clocks,

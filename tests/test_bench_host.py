@@ -4,6 +4,7 @@ summary that decides the peak, the guard that drops stale ncu traffic, and the
 reference arm (the oracle on host cores) and its JSON line."""
 import json
 import os
+import statistics
 
 import pytest
 
@@ -182,3 +183,23 @@ def test_plan_options_parse_and_are_recorded():
     r = _bench(["--impl", "reference", "--workload", "ar_tiny", "--steps", "3", "--warmup", "3",
                 "--option", "split_k=2"])
     assert json.loads(r.stdout)["config"]["options"] == {"split_k": 2}
+
+
+def test_nvml_sampler_summary_keeps_only_the_timed_region():
+    """The in-process clock sampler's summary: samples outside the marked
+    region are dropped, the median SM clock and the power come from the
+    samples inside it, and the event-reason bits decode to their names."""
+    s = bench.NvmlClockSampler(0)
+    s.max_mhz = 2070.0
+    s.t0, s.t1 = 10.0, 10.05
+    s.samples = [(9.99, 700.0, 150.0, 0x1)] + \
+        [(10.0 + 0.001 * i, 1900.0 + i, 900.0 + i, 0x4 if i == 7 else 0) for i in range(40)] + \
+        [(10.2, 600.0, 140.0, 0x8)]
+    c = s.summary()
+    assert c["samples"] == 40
+    assert c["sm_mhz"] == statistics.median(1900.0 + i for i in range(40))
+    assert c["sm_mhz_min"] == 1900.0 and c["sm_max_mhz"] == 2070.0
+    assert c["power_w_max"] == 939.0
+    assert c["reasons"] == ["sw_power_cap"]          # hw_slowdown fell outside the region
+    e = bench.NvmlClockSampler(0)
+    assert e.summary()["reasons"] == ["no samples"]
