@@ -259,6 +259,42 @@ class ClockSampler:
                 "power_w_max": maxp, "samples": len(loaded), "reasons": reasons}
 
 
+def init_replicas():
+    """World size, rank and local rank from the launcher's environment; with
+    more than one rank, a gloo process group for the barriers and the max over
+    ranks (nothing on the data path)."""
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group(backend="gloo")
+    return world, rank, local
+
+
+def replica_region(step, steps: int, warmup: int, world: int, sync, time_fn):
+    """One rank's timed region: `warmup` untimed steps, a synchronise and a
+    barrier, `steps` steps timed by time_fn(step, steps) -> (per-step ms,
+    region ms), then a barrier, so every rank's region spans the same moment."""
+    for _ in range(warmup):
+        step()
+    sync()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    times, region_ms = time_fn(step, steps)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    return times, region_ms
+
+
+def finish_replicas(world: int) -> None:
+    """Every rank waits for rank 0's output, then the process group ends."""
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
 def replica_value(local_seconds: float, flops_per_rank: float, world: int):
     """Whole-job TFLOP/s of `world` independent replicas: all ranks' flops over
     the slowest rank's timed region (max over ranks through the process group)."""
@@ -625,13 +661,10 @@ def main():
         return
 
     import torch
-    import torch.distributed as dist
     from tensor_gemm_reduction_gb300 import binding as B
     from tensor_gemm_reduction_gb300 import build as gbuild
 
-    world, rank, local = dist_env()
-    if world > 1:
-        dist.init_process_group(backend="gloo")
+    world, rank, local = init_replicas()
     torch.cuda.set_device(local)
     dev = torch.device(f"cuda:{local}")
     gbuild.build()
@@ -645,22 +678,19 @@ def main():
     run = Runner(w, plan, ws, dev)
 
     # ---- timed region: K back-to-back steps, inputs resident in HBM
-    for _ in range(args.warmup):
-        run()
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
     nvml = NvmlClockSampler(local)
     if nvml.start():
-        times, region_ms = time_launches(run, steps=args.steps, warmup=0, marks=nvml)
+        times, region_ms = replica_region(
+            run, args.steps, args.warmup, world, torch.cuda.synchronize,
+            lambda step, n: time_launches(step, steps=n, warmup=0, marks=nvml))
         nvml.stop()
         clocks = nvml.summary()
     else:
         with ClockSampler(local) as clk:
-            times, region_ms = time_launches(run, steps=args.steps, warmup=0)
+            times, region_ms = replica_region(
+                run, args.steps, args.warmup, world, torch.cuda.synchronize,
+                lambda step, n: time_launches(step, steps=n, warmup=0))
         clocks = clk.summary()
-    if world > 1:
-        dist.barrier()
     B.gemm_shard_check_status(plan, ws)
     value, region_s = replica_value(region_ms * 1e-3, w.flops * args.steps, world)
     avg_launch_s = statistics.mean(times) * 1e-3
@@ -710,9 +740,7 @@ def main():
             result["per_config"].append(sweep_pack(plan, ws, dev, pk))
     if rank == 0:
         print(json.dumps(result), flush=True)
-    if world > 1:
-        dist.barrier()
-        dist.destroy_process_group()
+    finish_replicas(world)
 
 
 def e2e(run, w, steps, world):
