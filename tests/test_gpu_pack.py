@@ -109,3 +109,35 @@ def test_pack_gather_full_size():
     ref = oracle.pack_gather([[x.cpu() for x in st] for st in S], w.rows_out)
     assert np.array_equal(bits_of(P.out), ref)
     assert P.guards_intact()
+
+
+def test_packed_states_feed_the_ag_projection():
+    """The packed gather feeding AG: the gathered rows P (rows_out x T*H: each
+    rank's hidden and auxiliary states side by side, the ranks stacked) are the
+    activation of a projection over the concatenated states, W: N x T*H (the
+    fused input of an EAGLE-style drafter's first layer). AG reads P in place,
+    either as one shard or as the ranks' row ranges of P (contiguous sub-buffers,
+    no copy); both match the oracle's AG over the oracle's pack within the
+    test tolerance."""
+    from gpu_util import assert_close, to_f64
+    M_r, T, H, rows_out, N = [96, 64, 130], 3, 256, 285, 264
+    S = gi.gaussian_states(M_r, T, H, seed=11)
+    dev = device()
+    S_dev = [shards_to(dev, states)[0] for states in S]
+    P = run_pack(S_dev, rows_out, T, H).out
+    W = (torch.randn(N, T * H, generator=torch.Generator().manual_seed(12)) / (T * H) ** 0.5
+         ).to(torch.bfloat16)
+    ref = oracle.ag([oracle.pack_gather(S, rows_out)], gi.bf16_bits(W))
+    p, ws = plan()
+    W_dev = W.to(dev)
+    Y1 = Guarded(rows_out, N)
+    B.gemm_ag(p, [P], W_dev, Y1.out, ws)
+    # the ranks' kept rows as separate shards pointing into P
+    bounds = np.minimum(np.cumsum([0] + M_r), rows_out)
+    views = [P[a:b] for a, b in zip(bounds[:-1], bounds[1:])]
+    Y2 = Guarded(rows_out, N)
+    B.gemm_ag(p, views, W_dev, Y2.out, ws)
+    B.gemm_shard_check_status(p, ws)
+    assert_close(to_f64(Y1.out), ref, "pack -> AG (one shard)")
+    assert Y1.guards_intact() and Y2.guards_intact()
+    assert_close(to_f64(Y2.out), ref, "pack -> AG (rank row ranges)")
