@@ -560,6 +560,24 @@ def sweep(plan, ws, dev, pk, names):
     return rows
 
 
+def sweep_floor(dev):
+    """The event-to-event time of a one-element kernel after the same L2 flush
+    as the sweep's rows: the floor under every row's time (launch and
+    completion of a kernel that follows a flush). A row's roofline time plus
+    this floor bounds what any kernel can score in this sweep."""
+    import torch
+    flush_buf = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    x = torch.zeros(1, device=dev)
+    torch.cuda.synchronize()
+    time.sleep(ROW_PAUSE_S)
+    times, _ = time_launches(lambda: x.add_(1), steps=20, warmup=3, flush=lambda: flush_buf.fill_(1))
+    del flush_buf
+    torch.cuda.empty_cache()
+    return {"workload": "launch_floor", "us": round(trimmed_mean(times) * 1e3, 2),
+            "kernel": "torch one-element add (not this library's)",
+            "note": "event to event after the same L2 flush as every row"}
+
+
 def sweep_pack(plan, ws, dev, pk):
     """The packed gather of per-shard states (HBM-bound copy), timed like the
     GEMM rows: trimmed mean of 20 launches, an L2 flush before each."""
@@ -735,7 +753,7 @@ def main():
         del run
         torch.cuda.empty_cache()
         names = [s for s in args.sweep_only.split(",") if s]
-        result["per_config"] = sweep(plan, ws, dev, pk, names)
+        result["per_config"] = [sweep_floor(dev)] + sweep(plan, ws, dev, pk, names)
         if not names or "pack_sp_t4" in names:
             result["per_config"].append(sweep_pack(plan, ws, dev, pk))
     if rank == 0:

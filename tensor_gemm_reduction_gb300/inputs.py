@@ -231,10 +231,13 @@ AG_MLA = [Workload(f"ag_mla_m{8 * m}", "ag", N=3648, K=7168, R=8, M=8 * m)
           for m in AG_LOCAL_M]
 AR_OPROJ = [Workload(f"ar_oproj_m{m}", "ar", N=7168, K=7168, R=8, M=m)
             for m in (128, 129, 1000, 4096, 32768)]
+# Decode batches below 128 rows, where the pages' fused AR was slower than the
+# unfused path (GEMM-RS/AR page, risks and impact): the same projection.
+AR_DECODE = [Workload(f"ar_oproj_m{m}", "ar", N=7168, K=7168, R=8, M=m) for m in (1, 16, 64)]
 # RS shares its seed with AR o_proj M=32768, so one set of inputs serves both.
 RS_ALL = [Workload(f"rs_r{r}", "rs", N=7168, K=7168, R=r, M=32768,
                    seed=default_seed(32768, 7168)) for r in (2, 4, 8, 16)]
-ALL_WORKLOADS = [AR_TINY] + AG_KDA + AG_MLA + AR_OPROJ + RS_ALL
+ALL_WORKLOADS = [AR_TINY] + AG_KDA + AG_MLA + AR_DECODE + AR_OPROJ + RS_ALL
 
 
 def make_inputs(w: Workload, device: str | torch.device = "cpu"):

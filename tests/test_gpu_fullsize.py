@@ -5,7 +5,7 @@ benchmark times (same plan maxima, heuristic configuration).
 The workloads are the pages' projections: AG KDA-like (N=6288) and MLA-like
 (N=3648) with R=8 shards of 256..4096 rows and K=7168 (AG-GEMM page,
 microbenchmark tables); AR o_proj-like (R=8 K-shards of 896, N=7168, M in
-{128, 129, 1000, 4096, 32768}); RS with R in {2, 4, 8, 16} at M=32768 (the
+{1, 16, 64, 128, 129, 1000, 4096, 32768}); RS with R in {2, 4, 8, 16} at M=32768 (the
 GEMM-RS/AR page, test `_reference`: rank s keeps rows [s*M/R, (s+1)*M/R) of
 the all-reduced product).
 
@@ -80,7 +80,8 @@ def test_ag_full_size_every_element(w):
     st.finish(expect_elements=w.M * w.N)
 
 
-@pytest.mark.parametrize("w", [x for x in gi.AR_OPROJ if x.M != 32768], ids=lambda w: w.name)
+@pytest.mark.parametrize("w", [x for x in gi.AR_DECODE + gi.AR_OPROJ if x.M != 32768],
+                         ids=lambda w: w.name)
 def test_ar_full_size_every_element(w):
     p, ws = plan()
     dev = device()
