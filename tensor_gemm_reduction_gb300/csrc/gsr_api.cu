@@ -377,12 +377,13 @@ Config choose_config(const gemm_shard_plan* P, int mode, int64_t M, int64_t N, i
       c.cta_group == 2 ? std::min<int64_t>(cap / 2, P->pair_clusters) : static_cast<int64_t>(cap);
   // 192-column pair tiles where 256 leaves a narrow last column of tiles (N a
   // multiple of 192 but not of 256, like N = 3648 = 19 x 192) and 192 fills at
-  // most three whole waves, so no tile is cut. Measured at AG N = 3648:
-  // M = 2048 (two waves) 4 % and M = 3072 (three) 2 % faster; from four waves
-  // on no gain, and at large M 192-column tiles are slower.
+  // most four whole waves, so no tile is cut. Measured at AG N = 3648 against
+  // 256-column tiles: M = 2048 (two waves) 4 %, M = 3072 (three) 2 % and
+  // M = 4096 (four) 4 % faster; at eight waves (M = 8192) within 1 %, and at
+  // large M 192-column tiles are slower.
   if (!P->opt_block_n && c.cta_group == 2 && c.block_n == 256 && N % 256 != 0 && N % 192 == 0) {
     const int64_t t192 = c.m_tiles * (N / 192);
-    if (workers > 0 && t192 % workers == 0 && t192 / workers <= 3) {
+    if (workers > 0 && t192 % workers == 0 && t192 / workers <= 4) {
       c.block_n = 192;
       c.n_tiles = N / 192;
       c.tiles = t192;

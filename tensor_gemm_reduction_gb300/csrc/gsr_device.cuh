@@ -319,6 +319,28 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
+// A pair's stage of copies under one elected lane: the leader's expect_tx
+// (`arm`), then this CTA's A and B boxes completing on the leader's barrier.
+__device__ __forceinline__ void stage_copies_pair(uint32_t arm, uint32_t full, uint32_t bytes,
+                                                  uint32_t lead_full, uint32_t sa,
+                                                  const CUtensorMap* ma, int a_row, uint32_t sb,
+                                                  const CUtensorMap* mb, int b_row, int kx,
+                                                  uint64_t pol_a, uint64_t pol_b) {
+  asm volatile(
+      "{\n\t.reg .pred e, q;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.and.b32 q, %0, 0, e;\n\t"
+      "@q mbarrier.arrive.expect_tx.shared::cta.b64 _, [%1], %2;\n\t"
+      "@e cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%4], [%5, {%6, %7}], [%3], %8;\n\t"
+      "@e cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%9], [%10, {%6, %11}], [%3], %12;\n\t}" ::"r"(arm),
+      "r"(full), "r"(bytes), "r"(lead_full), "r"(sa), "l"(reinterpret_cast<uint64_t>(ma)),
+      "r"(kx), "r"(a_row), "l"(pol_a), "r"(sb), "l"(reinterpret_cast<uint64_t>(mb)), "r"(b_row),
+      "l"(pol_b)
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t slot_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem),
                "r"(ncols)
@@ -342,6 +364,27 @@ __device__ __forceinline__ void mma_bf16_ss_pair(uint32_t d_tmem, uint64_t a_des
       "elect.sync _|e, 0xffffffff;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// The four K=16 steps of one k-block (descriptors advanced 32 bytes along the
+// swizzled rows per step) under one elected lane: one warp-wide election per
+// k-block instead of one per MMA. `accumulate` applies to the first step; the
+// others always accumulate.
+__device__ __forceinline__ void mma4_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p, t;\n\t.reg .b64 a1, a2, a3, b1, b2, b3;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "setp.eq.b32 t, %4, %4;\n\t"
+      "add.s64 a1, %1, 2;\n\tadd.s64 a2, %1, 4;\n\tadd.s64 a3, %1, 6;\n\t"
+      "add.s64 b1, %2, 2;\n\tadd.s64 b2, %2, 4;\n\tadd.s64 b3, %2, 6;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], a1, b1, %3, t;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], a2, b2, %3, t;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], a3, b3, %3, t;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }

@@ -326,6 +326,17 @@ __device__ void run_producer(const Params& p, uint32_t tiles_base, uint32_t bars
   };
   const uint64_t pol_a = entry.pol_a;
   const uint64_t pol_b = entry.pol_b;
+  // AR/RS: the shard table in the warp's lanes (lane r holds shard r's first
+  // k-block, lanes past R the k-block count), read with shuffles, so the
+  // k-block loop loads nothing from the kernel's parameter space: a
+  // dynamically indexed parameter load per k-block cost about 60 ns of the
+  // loop's issue time (traced: about 320 ns per k-block before, which bound
+  // tiles narrower than 256 columns).
+  const int lane = static_cast<int>(threadIdx.x) & 31;
+  const int begins = p.shard_kb_begin[lane <= kMaxShards ? lane : kMaxShards];
+  // With a pair, every copy completes on the leader's full barrier: the
+  // barriers' addresses as seen from this CTA, mapped once.
+  const uint32_t lead_full0 = CG == 1 ? full0 : map_shared_to_rank(full0, 0);
   uint32_t issued = 0;
   uint32_t slot = 0, slot_parity = 1;   // ring slot of the next load; its free-wait parity
   uint32_t arrived = 0;   // AG with arrival flags: shards seen ready (bit r)
@@ -356,9 +367,15 @@ __device__ void run_producer(const Params& p, uint32_t tiles_base, uint32_t bars
     const int a_shard_b = shard_b >= 0 ? shard_b : p.ag_pad_shard;
     const int a_row_b = shard_b >= 0 ? m0b : p.shard_rows[p.ag_pad_shard];
     const int b_row = t.n0 + static_cast<int>(rank * (tile_mma_n<BN>(p, t) / CG));
-    int r = 0;
-    if (p.mode != kModeAG)
-      while (p.shard_kb_begin[r + 1] <= t.kb_begin) ++r;
+    // AR/RS: shard r holds k-blocks [r_begin, r_end). The search stops at a
+    // shard whose range holds kb_begin (< the k-block count, and every shard
+    // has at least one k-block).
+    int r = 0, r_begin = 0, r_end = 0;
+    if (p.mode != kModeAG) {
+      r_end = __shfl_sync(0xffffffffu, begins, 1);
+      while (r_end <= t.kb_begin) r_end = __shfl_sync(0xffffffffu, begins, ++r + 1);
+      r_begin = __shfl_sync(0xffffffffu, begins, r);
+    }
     // The k-block loop, in two compiled forms so that the usual one (one box of
     // A rows) carries no test for the second box: this loop alone feeds the
     // tensor pipe, and every instruction added to it per k-block costs.
@@ -385,10 +402,13 @@ __device__ void run_producer(const Params& p, uint32_t tiles_base, uint32_t bars
           mb = &p.tmap_b[0];
           kx = kb * BK;
         } else {
-          while (p.shard_kb_begin[r + 1] <= kb) ++r;
+          while (r_end <= kb) {
+            r_begin = r_end;
+            r_end = __shfl_sync(0xffffffffu, begins, ++r + 1);
+          }
           ma = &p.tmap_a[r];
           mb = &p.tmap_b[r];
-          kx = (kb - p.shard_kb_begin[r]) * BK;
+          kx = (kb - r_begin) * BK;
         }
         // With 64-row AG granules the A tile is two boxes of 64 rows (8 KB each,
         // a whole number of 128-byte swizzle atoms, so the layout is that of one
@@ -401,12 +421,19 @@ __device__ void run_producer(const Params& p, uint32_t tiles_base, uint32_t bars
           tma_load_2d_hint(sb, mb, full, kx, b_row, pol_b);
         } else {
           // Both CTAs' bytes are counted on the leader's full barrier, which the
-          // leader alone arms (for the pair's bytes).
-          if (rank == 0) mbar_arrive_expect_tx(full, CG * L::kStageBytes);
-          const uint32_t lead_full = map_shared_to_rank(full, 0);
-          tma_load_2d_pair(sa, ma, lead_full, kx, a_row, pol_a);
-          if constexpr (kTwo) tma_load_2d_pair(sa + kHalfA, ma_b, lead_full, kx, a_row_b, pol_a);
-          tma_load_2d_pair(sb, mb, lead_full, kx, b_row, pol_b);
+          // leader alone arms (for the pair's bytes). The expect_tx and the
+          // copies go out under one elected lane: an election per instruction
+          // measured as issue time on this loop.
+          const uint32_t lead_full = lead_full0 + 8 * stage;
+          if constexpr (kTwo) {
+            if (rank == 0) mbar_arrive_expect_tx(full, CG * L::kStageBytes);
+            tma_load_2d_pair(sa, ma, lead_full, kx, a_row, pol_a);
+            tma_load_2d_pair(sa + kHalfA, ma_b, lead_full, kx, a_row_b, pol_a);
+            tma_load_2d_pair(sb, mb, lead_full, kx, b_row, pol_b);
+          } else {
+            stage_copies_pair(rank == 0 ? 1u : 0u, full, CG * L::kStageBytes, lead_full, sa, ma,
+                              a_row, sb, mb, b_row, kx, pol_a, pol_b);
+          }
         }
         if (++issued == 1) prefetch_descriptors();
         if (++slot == STAGES) {
@@ -479,14 +506,17 @@ __device__ void run_mma(const Params& p, uint32_t tiles_base, uint32_t bars, uin
       ready = kb + 1 < t.kb_end && mbar_test_wait(full0 + 8 * stage, phase);
       const uint64_t a_desc = smem_desc_sw128(tiles_base + cur * L::kABytes);
       const uint64_t b_desc = smem_desc_sw128(tiles_base + STAGES * L::kABytes + cur * L::kBBytes);
+      if constexpr (CG == 1) {
 #pragma unroll
-      for (int k = 0; k < BK / 16; ++k) {
-        // advance 16 elements (32 bytes) along K inside the swizzled 128-byte rows
-        const uint32_t accumulate = (kb > t.kb_begin || k > 0) ? 1u : 0u;
-        if constexpr (CG == 1)
+        for (int k = 0; k < BK / 16; ++k) {
+          // advance 16 elements (32 bytes) along K inside the swizzled 128-byte rows
+          const uint32_t accumulate = (kb > t.kb_begin || k > 0) ? 1u : 0u;
           mma_bf16_ss(d_tmem, a_desc + 2 * k, b_desc + 2 * k, idesc, accumulate);
-        else
-          mma_bf16_ss_pair(d_tmem, a_desc + 2 * k, b_desc + 2 * k, idesc, accumulate);
+        }
+      } else {
+        // The k-block's four K=16 steps under one election (one per MMA
+        // measured as issue time on this loop).
+        mma4_bf16_pair(d_tmem, a_desc, b_desc, idesc, kb > t.kb_begin ? 1u : 0u);
       }
       issued_any = true;
       if constexpr (CG == 1)

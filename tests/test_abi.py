@@ -486,14 +486,16 @@ def test_raster_options_are_validated_and_leave_the_configuration(host):
 
 def test_192_column_tiles_only_where_they_fill_few_whole_waves(host):
     """On 152 SMs (76 pairs): AG with N = 3648 (19 x 192, not a multiple of
-    256) uses 192-column pair tiles at 2048 and 3072 rows (exactly two and
-    three waves, no cut tile), 256 columns otherwise and for other N."""
+    256) uses 192-column pair tiles at 2048, 3072 and 4096 rows (exactly two,
+    three and four waves, no cut tile), 256 columns otherwise (3584 rows in
+    64-row granules, 8192 rows: eight waves) and for other N."""
     h = Host(host.lib, sm=152)
     def bn(m_r, N):
         return h.describe(B.MODE_AG, 0, N, 7168, [m_r] * 8)["block_n"]
     assert bn(256, 3648) == 192 and bn(384, 3648) == 192
     assert h.describe(B.MODE_AG, 0, 3648, 7168, [256] * 8)["sk_iters"] == 0
-    assert bn(448, 3648) == 256 and bn(512, 3648) == 256 and bn(4096, 3648) == 256
+    assert bn(512, 3648) == 192
+    assert bn(448, 3648) == 256 and bn(1024, 3648) == 256 and bn(4096, 3648) == 256
     assert bn(256, 6288) == 256 and bn(256, 7168) == 256
     # AR and RS on the same shape get the same tiles
     d_ar = h.describe(B.MODE_AR, 2048, 3648, 0, [896] * 8)

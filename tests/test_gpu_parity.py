@@ -95,6 +95,7 @@ AR_SHAPES = [
     (300, 256, [8] * 16),
     (513, 640, [520]),
     (200, 7168, [896, 896]),
+    (131, 520, [128, 256]),
 ]
 
 
@@ -227,6 +228,7 @@ RS_SHAPES = [
     (5, 256, [64, 64, 64]),
     (64, 136, [8] * 16),           # 16 shards of 4 rows
     (300, 7168, [448] * 16),
+    (257, 264, [128, 256, 128]),   # M % R != 0
 ]
 
 
