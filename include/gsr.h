@@ -88,7 +88,10 @@ typedef enum {
                                2 = A evict-last / B evict-first,
                                3 = A evict-first / B evict-last                     */
     GSR_OPT_CTA_GROUP = 7,  /* CTAs per MMA tile: 0 = heuristic, 1 = one CTA per
-                               128-row tile, 2 = a CTA pair per 256-row tile        */
+                               128-row tile, 2 = a CTA pair per 256-row tile,
+                               4 = two CTA pairs per cluster on two 256-row
+                               tiles of the same columns, each copy of a B tile
+                               loaded once and multicast to both pairs        */
     GSR_OPT_SCHEDULE = 8,   /* work schedule: 0 = heuristic (uniform while there
                                are fewer single-CTA tiles than SMs; else whole
                                tiles for the full waves and, for a partial last

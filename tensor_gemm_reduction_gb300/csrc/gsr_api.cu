@@ -43,6 +43,7 @@ struct gemm_shard_plan {
   int opt_small;       // 0 = heuristic, 1 = never use the small-M kernel, 2 = always when it applies
   int opt_small_rows;  // small-M kernel: W rows per tile (0 = heuristic)
   int pair_clusters;   // CTA pairs that can be resident at once
+  int quad_clusters;   // clusters of two CTA pairs that can be resident at once
   uint64_t timeout_ns;
 };
 
@@ -358,7 +359,10 @@ Config choose_config(const gemm_shard_plan* P, int mode, int64_t M, int64_t N, i
   // (fewer partial tiles to sum than stream-K's pieces of every tile).
   const bool small = mt1 * c.n_tiles < P->sm_count;
   if (P->opt_cta_group) {
-    c.cta_group = (P->opt_cta_group == 2 && pairs_fit) ? 2 : 1;
+    const bool quads_fit = P->quad_clusters > 0 && cap >= 4;
+    c.cta_group = (P->opt_cta_group == 4 && quads_fit)   ? 4
+                  : (P->opt_cta_group >= 2 && pairs_fit) ? 2
+                                                         : 1;
   } else if (small) {
     c.cta_group = pairs_fit && c.block_n == 256 && !one_row_tile ? 2 : 1;
   } else {
@@ -367,14 +371,16 @@ Config choose_config(const gemm_shard_plan* P, int mode, int64_t M, int64_t N, i
     c.cta_group = (pairs_fit && eff2 >= 0.9 * eff1) ? 2 : 1;   // pairs measured 10-20 % faster
   }
   // 192-column tiles exist for CTA pairs only.
-  if (c.block_n == 192 && c.cta_group != 2) {
+  if (c.block_n == 192 && c.cta_group == 1) {
     c.block_n = 256;
     c.n_tiles = cdiv(N, c.block_n);
   }
-  c.m_tiles = c.cta_group == 2 ? mt2 : mt1;
+  c.m_tiles = c.cta_group == 4 ? count_m_tiles(4) : c.cta_group == 2 ? mt2 : mt1;
   c.tiles = c.m_tiles * c.n_tiles;
   const int64_t workers =
-      c.cta_group == 2 ? std::min<int64_t>(cap / 2, P->pair_clusters) : static_cast<int64_t>(cap);
+      c.cta_group == 4   ? std::min<int64_t>(cap / 4, P->quad_clusters)
+      : c.cta_group == 2 ? std::min<int64_t>(cap / 2, P->pair_clusters)
+                         : static_cast<int64_t>(cap);
   // 192-column pair tiles where 256 leaves a narrow last column of tiles (N a
   // multiple of 192 but not of 256, like N = 3648 = 19 x 192) and 192 fills at
   // most four whole waves, so no tile is cut. Measured at AG N = 3648 against
@@ -648,6 +654,7 @@ static gemm_shard_plan* new_plan(int device, int sm_count, int64_t max_M, int64_
   P->opt_small = 0;
   P->opt_small_rows = 0;
   P->pair_clusters = sm_count / 2;   // host plans: every SM pairs up
+  P->quad_clusters = sm_count / 4;
   P->timeout_ns = 2000000000ull;
   return P;
 }
@@ -677,7 +684,7 @@ gsr_status gemm_shard_plan_create(gemm_shard_plan** out, int device, int64_t max
     return fail(GSR_ERR_UNSUPPORTED, "device %d is compute capability %d.%d; this library is built for sm_103a",
                 device, prop.major, prop.minor);
   if (!encode_fn()) return fail(GSR_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled is unavailable");
-  int pair_clusters = 0;
+  int pair_clusters = 0, quad_clusters = 0;
   {
     DeviceScope scope(device);
     if (scope.err != cudaSuccess) return cuda_fail(scope.err, "cudaSetDevice");
@@ -685,13 +692,14 @@ gsr_status gemm_shard_plan_create(gemm_shard_plan** out, int device, int64_t max
     if (static_cast<size_t>(prop.sharedMemPerBlockOptin) < need)
       return fail(GSR_ERR_UNSUPPORTED, "device allows %zu bytes of shared memory per block; %zu needed",
                   static_cast<size_t>(prop.sharedMemPerBlockOptin), need);
-    e = gsr::prepare_kernels(device, &pair_clusters);
+    e = gsr::prepare_kernels(device, &pair_clusters, &quad_clusters);
     if (e == cudaSuccess) e = gsr::prepare_small_kernel();
     if (e == cudaSuccess) e = gsr::prepare_pack_kernel();
     if (e != cudaSuccess) return cuda_fail(e, "configuring the kernels");
   }
   *out = new_plan(device, prop.multiProcessorCount, max_M, max_N, max_K, max_R);
   (*out)->pair_clusters = pair_clusters;
+  (*out)->quad_clusters = quad_clusters;
   return ok();
 }
 
@@ -734,7 +742,8 @@ gsr_status gemm_shard_plan_set_option(gemm_shard_plan* plan, gsr_option option, 
       plan->opt_l2_hints = static_cast<int>(value);
       return ok();
     case GSR_OPT_CTA_GROUP:
-      if (value < 0 || value > 2) return fail(GSR_ERR_INVALID_VALUE, "cta_group must be 0..2");
+      if (value < 0 || value > 4 || value == 3)
+        return fail(GSR_ERR_INVALID_VALUE, "cta_group must be 0, 1, 2 or 4");
       plan->opt_cta_group = static_cast<int>(value);
       return ok();
     case GSR_OPT_SCHEDULE:

@@ -319,6 +319,23 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
+// tma_load_2d_pair whose data lands in the CTAs of `mask` (the same offset in
+// each), each completing on its own pair leader's barrier at the offset that
+// `bar_cluster` (a pair leader's barrier) has: two CTA pairs of a cluster of
+// four read one copy of a tile of B this way.
+__device__ __forceinline__ void tma_load_2d_pair_multicast(uint32_t dst, const CUtensorMap* map,
+                                                           uint32_t bar_cluster, int x, int y,
+                                                           uint16_t mask, uint64_t policy) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".multicast::cluster.cta_group::2.L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5, %6;\n\t}"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y),
+      "h"(mask), "l"(policy)
+      : "memory");
+}
+
 // A pair's stage of copies under one elected lane: the leader's expect_tx
 // (`arm`), then this CTA's A and B boxes completing on the leader's barrier.
 __device__ __forceinline__ void stage_copies_pair(uint32_t arm, uint32_t full, uint32_t bytes,

@@ -262,7 +262,9 @@ __host__ __device__ constexpr uint32_t acc_stride() { return tmem_cols<BN>() / 2
 template <int BN, int STAGES, int CG>
 struct Layout {
   static constexpr uint32_t kABytes = BM * BK * 2;            // this CTA's rows of A
-  static constexpr uint32_t kBBytes = (BN / CG) * BK * 2;     // this CTA's columns of B
+  // This CTA's columns of B: all of them, or its half of a pair's (with two
+  // pairs in a cluster, each pair loads half of that half and multicasts it).
+  static constexpr uint32_t kBBytes = (BN / (CG == 1 ? 1 : 2)) * BK * 2;
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
   static constexpr uint32_t kTiles = STAGES * kStageBytes;
   // barriers: full[S], empty[S], tmem_full[2], tmem_empty[2], drain
@@ -336,7 +338,8 @@ __device__ void run_producer(const Params& p, uint32_t tiles_base, uint32_t bars
   const int begins = p.shard_kb_begin[lane <= kMaxShards ? lane : kMaxShards];
   // With a pair, every copy completes on the leader's full barrier: the
   // barriers' addresses as seen from this CTA, mapped once.
-  const uint32_t lead_full0 = CG == 1 ? full0 : map_shared_to_rank(full0, 0);
+  // With two pairs in a cluster (CG = 4) the pairs are ranks {0, 1} and {2, 3}.
+  const uint32_t lead_full0 = CG == 1 ? full0 : map_shared_to_rank(full0, rank & ~1u);
   uint32_t issued = 0;
   uint32_t slot = 0, slot_parity = 1;   // ring slot of the next load; its free-wait parity
   uint32_t arrived = 0;   // AG with arrival flags: shards seen ready (bit r)
@@ -366,7 +369,12 @@ __device__ void run_producer(const Params& p, uint32_t tiles_base, uint32_t bars
     const int a_row = t.shard >= 0 ? t.m0 : p.shard_rows[p.ag_pad_shard];
     const int a_shard_b = shard_b >= 0 ? shard_b : p.ag_pad_shard;
     const int a_row_b = shard_b >= 0 ? m0b : p.shard_rows[p.ag_pad_shard];
-    const int b_row = t.n0 + static_cast<int>(rank * (tile_mma_n<BN>(p, t) / CG));
+    // CG = 4: this CTA's columns of B (its pair half) are loaded as two
+    // quarter boxes, one by each pair, and multicast to the CTA at the same
+    // place in both pairs; quarter p lands BN/4 rows into the half.
+    const int b_row = CG <= 2 ? t.n0 + static_cast<int>(rank * (tile_mma_n<BN>(p, t) / CG))
+                              : t.n0 + static_cast<int>((rank & 1u) * (tile_mma_n<BN>(p, t) / 2)) +
+                                    static_cast<int>(rank >> 1) * (BN / 4);
     // AR/RS: shard r holds k-blocks [r_begin, r_end). The search stops at a
     // shard whose range holds kb_begin (< the k-block count, and every shard
     // has at least one k-block).
@@ -425,13 +433,23 @@ __device__ void run_producer(const Params& p, uint32_t tiles_base, uint32_t bars
           // copies go out under one elected lane: an election per instruction
           // measured as issue time on this loop.
           const uint32_t lead_full = lead_full0 + 8 * stage;
-          if constexpr (kTwo) {
-            if (rank == 0) mbar_arrive_expect_tx(full, CG * L::kStageBytes);
+          const bool leader = (rank & 1u) == 0;
+          if constexpr (CG == 4) {
+            // The pair's bytes (its A rows and both halves of its B columns,
+            // whichever pair loaded them) complete on its leader's barrier.
+            if (leader) mbar_arrive_expect_tx(full, 2 * L::kStageBytes);
+            tma_load_2d_pair(sa, ma, lead_full, kx, a_row, pol_a);
+            if constexpr (kTwo) tma_load_2d_pair(sa + kHalfA, ma_b, lead_full, kx, a_row_b, pol_a);
+            const uint16_t both = static_cast<uint16_t>((1u << (rank & 1u)) | (4u << (rank & 1u)));
+            tma_load_2d_pair_multicast(sb + (rank >> 1) * (L::kBBytes / 2), mb, lead_full, kx, b_row,
+                                       both, pol_b);
+          } else if constexpr (kTwo) {
+            if (leader) mbar_arrive_expect_tx(full, CG * L::kStageBytes);
             tma_load_2d_pair(sa, ma, lead_full, kx, a_row, pol_a);
             tma_load_2d_pair(sa + kHalfA, ma_b, lead_full, kx, a_row_b, pol_a);
             tma_load_2d_pair(sb, mb, lead_full, kx, b_row, pol_b);
           } else {
-            stage_copies_pair(rank == 0 ? 1u : 0u, full, CG * L::kStageBytes, lead_full, sa, ma,
+            stage_copies_pair(leader ? 1u : 0u, full, CG * L::kStageBytes, lead_full, sa, ma,
                               a_row, sb, mb, b_row, kx, pol_a, pol_b);
           }
         }
@@ -447,7 +465,7 @@ __device__ void run_producer(const Params& p, uint32_t tiles_base, uint32_t bars
     else
       stream_kblocks(std::false_type{});
   }
-  if (!ok && (CG == 1 || rank == 0)) {
+  if (!ok && (CG == 1 || (rank & 1u) == 0)) {
     // Let every copy already issued land before the CTA's shared memory goes
     // away (with a pair, the leader's barriers count the peer's copies too).
     const uint32_t first = issued > STAGES ? issued - STAGES : 0;
@@ -458,11 +476,16 @@ __device__ void run_producer(const Params& p, uint32_t tiles_base, uint32_t bars
 
 template <int BN, int STAGES, int CG>
 __device__ void run_mma(const Params& p, uint32_t tiles_base, uint32_t bars, uint32_t tmem_base,
-                        const Ctl& ctl) {
+                        uint32_t rank, const Ctl& ctl) {
   using L = Layout<BN, STAGES, CG>;
   const uint32_t full0 = bars, tfull0 = bars + 16 * STAGES, tempty0 = tfull0 + 16;
   const uint32_t empty0 = bars + 8 * STAGES, drain = tempty0 + 16;
-  const uint32_t rank = 0;   // only the leader issues MMAs; tile k ranges do not depend on rank
+  // Only a pair's leader issues its MMAs (rank 0, or 0 and 2 with two pairs).
+  // A stage is freed in every CTA its copies wrote: both CTAs of the pair, or
+  // all four with two pairs (each CTA's empty barrier then counts both
+  // leaders' commits). The accumulator is the pair's.
+  constexpr uint16_t kFreeMask = CG == 4 ? 0xF : 0x3;
+  const uint16_t pair_mask = static_cast<uint16_t>(0x3u << (rank & ~1u));
   uint32_t stage = 0, phase = 0, local = 0;   // next ring slot and its fill phase
   bool ok = true, issued_any = false;
   Sched sch = sched_begin<CG>(p);
@@ -482,7 +505,7 @@ __device__ void run_mma(const Params& p, uint32_t tiles_base, uint32_t bars, uin
     }
     tc_fence_after_sync();
     const uint32_t d_tmem = tmem_base + acc * acc_stride<BN>();
-    const uint32_t idesc = make_idesc(BM * CG, tile_mma_n<BN>(p, t));
+    const uint32_t idesc = make_idesc(BM * (CG == 1 ? 1 : 2), tile_mma_n<BN>(p, t));
     // The next slot's barrier is tested (without blocking) before this slot's
     // MMAs are issued, so the test overlaps the tensor pipe's work instead of
     // sitting between the MMAs of two consecutive k-blocks. The slot's bytes
@@ -522,7 +545,7 @@ __device__ void run_mma(const Params& p, uint32_t tiles_base, uint32_t bars, uin
       if constexpr (CG == 1)
         mma_commit(empty0 + 8 * cur);
       else
-        mma_commit_pair(empty0 + 8 * cur, 0x3);     // frees the slot in both CTAs
+        mma_commit_pair(empty0 + 8 * cur, kFreeMask);   // frees the slot in every CTA it fed
       if (!looked_ahead) {
         have_next = sched_next<BN, CG>(p, sch, tn, rank);
         looked_ahead = true;
@@ -532,7 +555,7 @@ __device__ void run_mma(const Params& p, uint32_t tiles_base, uint32_t bars, uin
     if constexpr (CG == 1)
       mma_commit(tfull0 + 8 * acc);
     else
-      mma_commit_pair(tfull0 + 8 * acc, 0x3);       // both CTAs' epilogues may read
+      mma_commit_pair(tfull0 + 8 * acc, pair_mask);   // both CTAs' epilogues may read
     if (!looked_ahead) have_next = sched_next<BN, CG>(p, sch, tn, rank);
     t = tn;
     have = have_next;
@@ -542,7 +565,7 @@ __device__ void run_mma(const Params& p, uint32_t tiles_base, uint32_t bars, uin
     if constexpr (CG == 1)
       mma_commit(drain);
     else
-      mma_commit_pair(drain, 0x1);
+      mma_commit_pair(drain, static_cast<uint16_t>(1u << rank));
     wait_drain(drain, 0, 100000000ull);
   }
 }
@@ -632,7 +655,7 @@ __device__ void run_epilogue(const Params& p, uint32_t bars, uint32_t tmem_base,
         if constexpr (CG == 1)
           mbar_arrive(tempty0 + 8 * acc);
         else
-          mbar_arrive_cluster(map_shared_to_rank(tempty0 + 8 * acc, 0));
+          mbar_arrive_cluster(map_shared_to_rank(tempty0 + 8 * acc, rank & ~1u));
       }
     };
 
@@ -775,11 +798,11 @@ __global__ void __launch_bounds__(kThreads, 1) gsr_gemm_kernel(const __grid_cons
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(bars + 8 * i, 1);                 // full: the (leader's) expect_tx + TMA bytes
-      mbar_init(bars + 8 * (STAGES + i), 1);      // empty: one MMA commit
+      mbar_init(bars + 8 * (STAGES + i), CG == 4 ? 2 : 1);   // empty: each feeding leader's commit
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bars + 16 * STAGES + 8 * i, 1);               // tmem_full: MMA commit
-      mbar_init(bars + 16 * STAGES + 16 + 8 * i, 4 * CG);     // tmem_empty: one per epilogue warp
+      mbar_init(bars + 16 * STAGES + 16 + 8 * i, CG == 1 ? 4 : 8);   // tmem_empty: one per epilogue warp of the pair
     }
     mbar_init(bars + 16 * STAGES + 32, 1);  // drain
     *abort_flag = 0;
@@ -819,7 +842,7 @@ __global__ void __launch_bounds__(kThreads, 1) gsr_gemm_kernel(const __grid_cons
   } else if (warp == 1) {
     // The whole warp walks the MMA loop (its values stay warp-uniform); one
     // elected lane issues each MMA and commit.
-    if (rank == 0) run_mma<BN, STAGES, CG>(p, tiles_base, bars, tmem_base, ctl);
+    if ((rank & 1u) == 0) run_mma<BN, STAGES, CG>(p, tiles_base, bars, tmem_base, rank, ctl);
     __syncwarp();
   } else {
     run_epilogue<BN, STAGES, CG>(p, bars, tmem_base, rank, last_flag, ctl);
@@ -846,6 +869,10 @@ template <> struct Stages<128, 1> { static constexpr int value = 6; };   // 32 K
 template <> struct Stages<256, 2> { static constexpr int value = 7; };   // 32 KB per CTA
 template <> struct Stages<128, 2> { static constexpr int value = 8; };   // 24 KB per CTA
 template <> struct Stages<192, 2> { static constexpr int value = 8; };   // 28 KB per CTA
+// Two CTA pairs per cluster (B multicast between the pairs): the same stages.
+template <> struct Stages<256, 4> { static constexpr int value = 7; };
+template <> struct Stages<128, 4> { static constexpr int value = 8; };
+template <> struct Stages<192, 4> { static constexpr int value = 8; };
 
 template <int BN, int CG>
 using KernelLayout = Layout<BN, Stages<BN, CG>::value, CG>;
@@ -867,7 +894,7 @@ cudaError_t launch_instance(const Params& p, int ctas, cudaStream_t stream) {
   attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[n].val.programmaticStreamSerializationAllowed = 1;
   ++n;
-  if (CG == 2) {
+  if (CG >= 2) {
     attr[n].id = cudaLaunchAttributeClusterDimension;
     attr[n].val.clusterDim.x = CG;
     attr[n].val.clusterDim.y = 1;
@@ -886,21 +913,41 @@ cudaError_t launch_instance(const Params& p, int ctas, cudaStream_t stream) {
 }  // namespace
 
 size_t kernel_smem_bytes(int block_n, int cta_group) {
-  if (cta_group == 2)
+  if (cta_group >= 2)
     return block_n == 256   ? KernelLayout<256, 2>::kSmem
            : block_n == 192 ? KernelLayout<192, 2>::kSmem
                             : KernelLayout<128, 2>::kSmem;
   return block_n == 256 ? KernelLayout<256, 1>::kSmem : KernelLayout<128, 1>::kSmem;
 }
 
-cudaError_t prepare_kernels(int device, int* pair_clusters) {
+cudaError_t prepare_kernels(int device, int* pair_clusters, int* quad_clusters) {
   (void)device;  // the caller has made `device` current
   cudaError_t e = set_smem_limit<256, 1>();
   if (e == cudaSuccess) e = set_smem_limit<128, 1>();
   if (e == cudaSuccess) e = set_smem_limit<256, 2>();
   if (e == cudaSuccess) e = set_smem_limit<128, 2>();
   if (e == cudaSuccess) e = set_smem_limit<192, 2>();
+  if (e == cudaSuccess) e = set_smem_limit<256, 4>();
+  if (e == cudaSuccess) e = set_smem_limit<128, 4>();
+  if (e == cudaSuccess) e = set_smem_limit<192, 4>();
   if (e != cudaSuccess) return e;
+  {
+    // How many clusters of two CTA pairs can be resident at once.
+    cudaLaunchConfig_t cfg4 = {};
+    cudaLaunchAttribute attr4[1];
+    attr4[0].id = cudaLaunchAttributeClusterDimension;
+    attr4[0].val.clusterDim.x = 4;
+    attr4[0].val.clusterDim.y = 1;
+    attr4[0].val.clusterDim.z = 1;
+    cfg4.gridDim = dim3(4, 1, 1);
+    cfg4.blockDim = dim3(kThreads, 1, 1);
+    cfg4.dynamicSmemBytes = KernelLayout<256, 4>::kSmem;
+    cfg4.attrs = attr4;
+    cfg4.numAttrs = 1;
+    e = cudaOccupancyMaxActiveClusters(quad_clusters, gsr_gemm_kernel<256, Stages<256, 4>::value, 4>,
+                                       &cfg4);
+    if (e != cudaSuccess) return e;
+  }
   // How many CTA pairs can be resident at once (SMs pair up inside a GPC).
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -918,6 +965,10 @@ cudaError_t prepare_kernels(int device, int* pair_clusters) {
 }
 
 cudaError_t launch_gemm(const Params& p, int block_n, int cta_group, int ctas, cudaStream_t stream) {
+  if (cta_group == 4)
+    return block_n == 256   ? launch_instance<256, 4>(p, ctas, stream)
+           : block_n == 192 ? launch_instance<192, 4>(p, ctas, stream)
+                            : launch_instance<128, 4>(p, ctas, stream);
   if (cta_group == 2)
     return block_n == 256   ? launch_instance<256, 2>(p, ctas, stream)
            : block_n == 192 ? launch_instance<192, 2>(p, ctas, stream)

@@ -162,10 +162,13 @@ struct PackParams {
 
 // Host-side launcher (defined with the kernel).
 // cta_group 1: one CTA per 128-row tile; 2: a CTA pair (cluster of two) per
-// 256-row tile. block_n is 128 or 256. `ctas` counts CTAs (even for pairs).
+// 256-row tile; 4: two CTA pairs (a cluster of four) on two 256-row tiles of
+// the same columns, sharing each copy of B. block_n is 128, 192 (pairs) or
+// 256. `ctas` counts CTAs (a multiple of the cluster size).
 cudaError_t launch_gemm(const Params& p, int block_n, int cta_group, int ctas, cudaStream_t stream);
-// Sets shared-memory limits and reports how many CTA pairs can be resident.
-cudaError_t prepare_kernels(int device, int* pair_clusters);
+// Sets shared-memory limits and reports how many CTA pairs, and how many
+// clusters of two CTA pairs, can be resident.
+cudaError_t prepare_kernels(int device, int* pair_clusters, int* quad_clusters);
 size_t kernel_smem_bytes(int block_n, int cta_group);
 // The small-M kernel (gsr_small.cu): `ctas` is even (clusters of two).
 cudaError_t launch_small(const Params& p, int ctas, cudaStream_t stream);

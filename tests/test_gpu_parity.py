@@ -19,7 +19,8 @@ pytestmark = pytest.mark.gpu
 # the oracle): the heuristic; the uniform schedule; stream-K on only 8 CTAs (so
 # that even small shapes cut tiles into several pieces); CTA pairs with 128-
 # and 256-column whole tiles; CTA pairs with stream-K; CTA pairs with a
-# uniform 3-way split; CTA pairs with 192-column tiles.
+# uniform 3-way split; CTA pairs with 192-column tiles; clusters of two CTA
+# pairs that share each copy of B.
 VARIANTS = {
     "auto": {},
     "uniform": dict(schedule=1),
@@ -32,6 +33,11 @@ VARIANTS = {
     "pairsplit": dict(max_M=4096, max_N=8192, max_K=8192, max_R=16, cta_group=2, split_k=3),
     "rastern": dict(raster_n=3),
     "splittail": dict(cta_group=2, schedule=5, max_ctas=16),
+    # two CTA pairs per cluster sharing each copy of B (whole tiles, stream-K
+    # on four clusters, 192-column tiles)
+    "quad": dict(cta_group=4),
+    "quadsk": dict(cta_group=4, schedule=2, max_ctas=16),
+    "quad192": dict(cta_group=4, block_n=192),
 }
 
 
