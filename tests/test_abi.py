@@ -716,7 +716,7 @@ def test_last_error_string_is_per_thread(lib, host):
     ("RASTER_M", [0, 1, 64], [-1, 65]),
     ("RASTER_N", [0, 1, 64], [-1, 65]),
     ("L2_HINTS", [0, 3], [-1, 4]),
-    ("CTA_GROUP", [0, 1, 2], [-1, 3]),
+    ("CTA_GROUP", [0, 1, 2, 4], [-1, 3, 5]),
     ("SCHEDULE", [0, 5], [-1, 6]),
     ("SMALL_M", [0, 2], [-1, 3]),
     ("SMALL_TILE_ROWS", [0, 8, 128], [-8, 4, 136]),
@@ -816,3 +816,27 @@ def test_workspace_init_checks(host):
                                          None) == B.GSR_ERR_UNSUPPORTED
     assert lib.gemm_shard_workspace_init(None, ctypes.c_void_p(0x20000000), need, None) == \
         B.GSR_ERR_INVALID_VALUE
+
+
+def test_two_pairs_per_cluster_on_request(lib):
+    """GSR_OPT_CTA_GROUP = 4: clusters of two CTA pairs, each cluster on two
+    256-row tiles of the same columns (half as many work tiles), a grid of
+    whole clusters; the configuration still does not depend on the mode, and
+    every schedule fits the plan's workspace."""
+    h = Host(lib, sm=152)
+    B.gemm_shard_plan_set_option(h.plan, B.GSR_OPT_CTA_GROUP, 4)
+    pairs = Host(lib, sm=152)
+    B.gemm_shard_plan_set_option(pairs.plan, B.GSR_OPT_CTA_GROUP, 2)
+    for M in (300, 1000, 4096, 32768):
+        d = h.describe(B.MODE_AR, M, 7168, 0, [896] * 8)
+        d2 = pairs.describe(B.MODE_AR, M, 7168, 0, [896] * 8)
+        assert d["cta_group"] == 4 and d["ctas"] % 4 == 0 and d["ctas"] <= 152
+        assert d["tiles"] == -(-(-(-M // 256)) // 2) * 28 and d2["tiles"] == -(-M // 256) * 28
+        assert d == h.describe(B.MODE_RS, M, 7168, 0, [896] * 8)
+        assert d["workspace_bytes"] <= h.ws_bytes
+    d = h.describe(B.MODE_AG, 0, 6288, 7168, [4096] * 8)
+    assert d["cta_group"] == 4 and d["tiles"] == 64 * 25
+    # too few SMs for a cluster of four: CTA pairs
+    small = Host(lib, sm=2)
+    B.gemm_shard_plan_set_option(small.plan, B.GSR_OPT_CTA_GROUP, 4)
+    assert small.describe(B.MODE_AR, 1000, 7168, 0, [896] * 8)["cta_group"] == 2
