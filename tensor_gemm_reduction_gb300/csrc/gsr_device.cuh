@@ -245,6 +245,20 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_
                : "memory");
 }
 
+// The same 16-byte store into the peer's shared memory, asynchronous: its
+// arrival is counted (16 bytes of complete_tx) on the peer's mbarrier `bar`
+// (a shared::cluster address in the same CTA as `addr`), so a consumer that
+// armed that barrier with the expected byte count sees the data once the
+// phase completes, with no fence or arrive on the sender's side.
+__device__ __forceinline__ void st_async_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                            uint32_t d, uint32_t bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::
+          "r"(addr),
+      "r"(a), "r"(b), "r"(c), "r"(d), "r"(bar)
+      : "memory");
+}
+
 // Named barrier over the 128 epilogue threads.
 __device__ __forceinline__ void epilogue_bar_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kEpilogueThreads) : "memory");
@@ -297,6 +311,17 @@ __device__ __forceinline__ void cluster_arrive() {
 }
 __device__ __forceinline__ void cluster_wait() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// cluster_barrier without the release: prior global stores are not waited for
+// (a kernel's stores are visible to later work once it completes anyway), and
+// neither are operations on the peer's shared memory, so the caller must know
+// that the peer waits for each of those before it leaves.
+__device__ __forceinline__ void cluster_barrier_relaxed() {
+  asm volatile(
+      "barrier.cluster.arrive.relaxed.aligned;\n\t"
+      "barrier.cluster.wait.aligned;" ::
+          : "memory");
 }
 
 // Arrive on an mbarrier given by its shared::cluster address (possibly the peer's).

@@ -21,8 +21,9 @@
 // halves are then added in distributed shared memory instead of through global
 // memory: the output rows are cut into 16-row granules, the first half of the
 // granules is finished by rank 0 and the rest by rank 1, and each CTA writes
-// the granules its peer finishes straight into the peer's shared memory
-// (st.shared::cluster), then arrives on the peer's mbarrier. The owner adds the
+// the granules its peer finishes straight into the peer's shared memory with
+// asynchronous stores (st.async) whose bytes complete the peer's mbarrier,
+// which the peer armed with the byte count it expects. The owner adds the
 // peer's half to its own (one fp32 addition per output, commutative, so the
 // result does not depend on which CTA adds), rounds to bf16 (round to nearest
 // even) and transposes each 32 x 32 block through shared memory so that the
@@ -234,15 +235,26 @@ __device__ __forceinline__ uint16_t bf16_bits(float x) {
   return *reinterpret_cast<uint16_t*>(&h);
 }
 
-// Row m of the output (routed by mode).
-__device__ __forceinline__ uint16_t* out_row(const Params& p, int m, int rep) {
-  if (p.mode == kModeRS) {
-    const int s = m / p.rps;
-    return p.y_r[s] + static_cast<size_t>(m - s * p.rps) * p.N;
+// Row m of the output (routed by mode). The parameters it needs are read when
+// the epilogue starts: the first read of a parameter's line comes from memory,
+// and at the end of the stream it would delay the stores by a round trip.
+struct OutRows {
+  uint16_t* y;
+  int mode, rps, N;
+  __device__ explicit OutRows(const Params& p) : y(p.y), mode(p.mode), rps(p.rps), N(p.N) {
+    // Make these reads (and those of both lines of y_r) happen now.
+    asm volatile("" ::"l"(y), "r"(mode), "r"(rps), "r"(N), "l"(p.y_r[0]),
+                 "l"(p.y_r[kMaxShards - 1]));
   }
-  if (p.mode == kModeARRep) return p.y_r[rep] + static_cast<size_t>(m) * p.N;
-  return p.y + static_cast<size_t>(m) * p.N;
-}
+  __device__ __forceinline__ uint16_t* row(const Params& p, int m, int rep) const {
+    if (mode == kModeRS) {
+      const int s = m / rps;
+      return p.y_r[s] + static_cast<size_t>(m - s * rps) * N;
+    }
+    if (mode == kModeARRep) return p.y_r[rep] + static_cast<size_t>(m) * N;
+    return y + static_cast<size_t>(m) * N;
+  }
+};
 
 // Up to two consecutive granules (32 TMEM columns) of this thread's lane.
 __device__ __forceinline__ void load_granules(uint32_t taddr, int count, uint32_t (&v)[32]) {
@@ -277,10 +289,19 @@ __device__ void small_epilogue(const Params& p, const SmallLayout& L, uint32_t b
   // A quarter of TMEM lanes wholly past the tile (96-row tiles: lanes 96..127)
   // holds no output: its warps only take part in the handshakes.
   const bool live = quad * 32 < p.tile_rows;
+  const OutRows out(p);
+  const int m_rows = p.M;
+  // Bytes the peer sends this CTA per tile (its complete_tx on `staged`): 16
+  // fp32 per owned granule for every TMEM lane of a live quarter.
+  const uint32_t rx_bytes = static_cast<uint32_t>((own_hi - own_lo) * ((p.tile_rows + 31) / 32) *
+                                                  32 * kGranule * 4);
   uint32_t local = 0;
-  for (int tile = static_cast<int>(blockIdx.x) / 2; tile < p.n_tiles;
-       tile += static_cast<int>(gridDim.x) / 2, ++local) {
+  const int step = static_cast<int>(gridDim.x) / 2;
+  for (int tile = static_cast<int>(blockIdx.x) / 2; tile < p.n_tiles; tile += step, ++local) {
     const uint32_t acc = local & 1u;
+    // One arrive per tile, with the bytes to expect; the staged wait of the
+    // previous tile (same warp) has seen the previous phase complete.
+    if (ew == 0) mbar_arrive_expect_tx(b.staged, rx_bytes);
     bool ok = wait_bounded(b.tfull0 + 8 * acc, (local >> 1) & 1u, ctl, (kRoleEpilogue << 8) | 1);
     if (!epilogue_bar_and<kSmallEpiThreads>(ok)) break;
     tc_fence_after_sync();
@@ -289,7 +310,8 @@ __device__ void small_epilogue(const Params& p, const SmallLayout& L, uint32_t b
     const int n_end = min(n0 + p.tile_rows, p.N);   // TMEM lanes past the tile are not output
 
     // 1. The granules the peer finishes go into the peer's staging area, once
-    //    the peer has consumed what this CTA sent for the previous tile.
+    //    the peer has consumed what this CTA sent for the previous tile. The
+    //    stores are asynchronous and counted on the peer's staged barrier.
     if (local > 0) {
       ok = wait_bounded_cluster(b.drained, (local - 1) & 1u, ctl, (kRoleEpilogue << 8) | 2);
       if (!epilogue_bar_and<kSmallEpiThreads>(ok)) break;
@@ -302,10 +324,9 @@ __device__ void small_epilogue(const Params& p, const SmallLayout& L, uint32_t b
 #pragma unroll
       for (int c4 = 0; c4 < 8; ++c4)
         if (c4 < 4 * cnt)
-          st_cluster_v4(dst + c4 * kSmallTileN * 16, v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2],
-                        v[4 * c4 + 3]);
+          st_async_v4(dst + c4 * kSmallTileN * 16, v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2],
+                      v[4 * c4 + 3], peer_staged);
     }
-    mbar_arrive_cluster(peer_staged);   // release at cluster scope: the stores above first
 
     // 2. This CTA's granules: its own half plus the peer's, rounded to bf16,
     //    transposed and stored. The transpose goes back into the part of the
@@ -346,16 +367,21 @@ __device__ void small_epilogue(const Params& p, const SmallLayout& L, uint32_t b
         const int row = vi >> 2, part = vi & 3;
         const int m = g * kGranule + row;
         const int n = n0 + quad * 32 + part * 8;
-        if (row < kGranule * cnt && m < p.M && n < n_end) {
+        if (row < kGranule * cnt && m < m_rows && n < n_end) {
           const uint4 val = *reinterpret_cast<const uint4*>(blocks + t * (kSmallTileN * 16) +
                                                             (row & 7) * 64 + part * 16);
           for (int rep = 0; rep < reps; ++rep)
-            *reinterpret_cast<uint4*>(out_row(p, m, rep) + n) = val;
+            *reinterpret_cast<uint4*>(out.row(p, m, rep) + n) = val;
         }
       }
       __syncwarp();
     }
-    mbar_arrive_cluster(peer_drained);  // this CTA's staging may be written again
+    if (tile + step < p.n_tiles) {
+      // This CTA's staging may be written again (the peer waits for it only
+      // before a next tile; after the last one, no handshake and no wait for
+      // the stores above).
+      mbar_arrive_cluster(peer_drained);
+    }
 
     // 3. The TMEM accumulator goes back to the MMA issuer.
     tc_fence_before_sync();
@@ -388,7 +414,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) gsr_small_kernel(const __gri
       mbar_init(b.tfull0 + 8 * i, 1);                  // MMA commit
       mbar_init(b.tempty0 + 8 * i, kSmallEpiWarps);    // one per epilogue warp
     }
-    mbar_init(b.staged, kSmallEpiThreads);    // every epilogue thread of the peer
+    mbar_init(b.staged, 1);    // one expect_tx arrive per tile; the peer's bytes complete it
     mbar_init(b.drained, kSmallEpiThreads);
     mbar_init(b.drain, 1);
     *abort_flag = 0;
@@ -427,11 +453,23 @@ __global__ void __launch_bounds__(kSmallThreads, 1) gsr_small_kernel(const __gri
     small_epilogue(p, L, base, base_ptr, b, tmem_base, rank, ctl);
   }
 
+  // No CTA leaves while its peer may still write or signal it. On the normal
+  // path every write and arrive a CTA receives is one it waits for (the
+  // peer's staged bytes, and the drained arrive before a next tile; none
+  // follows the last tile), so the barrier needs no release, which would
+  // wait for the output stores.
   tc_fence_before_sync();
-  cluster_barrier();   // no CTA leaves while its peer may still write or signal it
+  cluster_barrier_relaxed();
   if (warp == 1) {
     tc_fence_after_sync();
     tmem_dealloc(tmem_base, L.tmem_cols);
+  }
+  // After a timed-out wait that is no longer so: the peer may have sent what
+  // this CTA stopped waiting for. Having passed the barrier, the peer has
+  // issued all of it; the CTA stays resident until it has surely landed.
+  if (threadIdx.x == 0 && *abort_flag) {
+    const uint64_t t0 = global_timer_ns();
+    while (global_timer_ns() - t0 < 20000ull) __nanosleep(1000);
   }
 }
 
