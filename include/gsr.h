@@ -112,21 +112,25 @@ typedef enum {
     GSR_OPT_SMALL_M = 9,    /* the small-M kernel (AR/RS, M <= 256): 0 = heuristic
                                (used when M <= 256 and no other option above
                                forces a configuration), 1 = never, 2 = whenever
-                               M <= 256 and the K range has at least two
-                               k-blocks of 64. It streams W in tiles of rows
-                               (GSR_OPT_SMALL_TILE_ROWS, at most 128) against
-                               all M rows at once (the activation rows
-                               are the MMA's N), each tile split over K between
-                               the two CTAs of a cluster and summed in
-                               distributed shared memory; it needs no workspace
-                               beyond the status word                            */
+                               M <= 256. It streams W in tiles of rows
+                               (GSR_OPT_SMALL_TILE_ROWS, at most 256), one CTA
+                               pair per tile over the whole K range, against
+                               all M rows at once (the activation rows are the
+                               pair MMA's M, the tile's rows its N); it needs
+                               no workspace beyond the status word               */
     GSR_OPT_SMALL_TILE_ROWS = 10, /* W rows per tile of the small-M kernel: 0 =
-                               heuristic (the fewest rows, in multiples of 8 up
-                               to 128, that spread N over every SM pair in the
-                               fewest waves), else a multiple of 8 in 8..128     */
-    GSR_OPT_RASTER_N = 11   /* main kernel: n-tiles per raster group, n running
+                               heuristic (the fewest rows, in multiples of 16 up
+                               to 256, that spread N over every SM pair in the
+                               fewest waves), else a multiple of 16 in 16..256   */
+    GSR_OPT_RASTER_N = 11,  /* main kernel: n-tiles per raster group, n running
                                fastest inside a group (0 = off: GSR_OPT_RASTER_M
                                applies), 1..64                                   */
+    GSR_OPT_SMALL_KBLOCKS = 12 /* small-M kernel: k-blocks of 64 per copy: 0 =
+                               heuristic (the largest of 4, 2, 1 that divides
+                               every shard's k-block count, with every K_r a
+                               multiple of 64), else 1, 2 or 4: the largest of
+                               that value and the smaller ones that divides as
+                               above                                             */
 } gsr_option;
 
 /*
@@ -385,11 +389,11 @@ const char *gsr_last_error_string(void);
 /* Kernel configuration of a call, as gemm_shard_describe reports it. */
 typedef struct {
     int block_n;            /* output tile width: 128, 192 or 256 (the small-M
-                               kernel: W rows per tile, a multiple of 8 <= 128)   */
+                               kernel: W rows per tile, a multiple of 16 <= 256)  */
     int cta_group;          /* 1: a CTA per 128-row tile; 2: a CTA pair per 256 rows */
     int schedule;           /* 1 = uniform pieces, 2 = stream-K hybrid, 3 = the
-                               small-M kernel (block_n W rows per tile, split = 2
-                               halves of K per tile on a cluster of two CTAs),
+                               small-M kernel (one CTA pair per tile of block_n
+                               W rows over the whole K range, split = 1),
                                4 = split tail (split = pieces per tail tile)      */
     int split;              /* uniform schedule: pieces per tile                    */
     int64_t tiles;          /* output tiles                                         */
@@ -397,6 +401,8 @@ typedef struct {
     int64_t sk_iters;       /* stream-K: k-blocks shared out over the workers       */
     int ctas;               /* persistent CTAs launched                             */
     size_t workspace_bytes; /* workspace this call needs                           */
+    int kblocks;            /* small-M kernel: k-blocks of 64 per copy (1, 2 or 4);
+                               1 for the main kernel                              */
 } gsr_config;
 
 /* The kernel configuration the plan chooses for a call, for logging and tests:

@@ -36,6 +36,7 @@ GSR_OPT_SCHEDULE = 8
 GSR_OPT_SMALL_M = 9
 GSR_OPT_SMALL_TILE_ROWS = 10
 GSR_OPT_RASTER_N = 11
+GSR_OPT_SMALL_KBLOCKS = 12
 
 MODE_AR, MODE_RS, MODE_AG = 0, 1, 2
 
@@ -63,7 +64,7 @@ class GsrConfig(ctypes.Structure):
                 ("schedule", ctypes.c_int), ("split", ctypes.c_int),
                 ("tiles", ctypes.c_int64), ("dp_tiles", ctypes.c_int64),
                 ("sk_iters", ctypes.c_int64), ("ctas", ctypes.c_int),
-                ("workspace_bytes", ctypes.c_size_t)]
+                ("workspace_bytes", ctypes.c_size_t), ("kblocks", ctypes.c_int)]
 
 
 class GsrError(RuntimeError):

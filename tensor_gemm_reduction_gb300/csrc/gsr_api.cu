@@ -42,6 +42,7 @@ struct gemm_shard_plan {
                        // last), 5 = split tail (GSR_OPT_SCHEDULE in gsr.h)
   int opt_small;       // 0 = heuristic, 1 = never use the small-M kernel, 2 = always when it applies
   int opt_small_rows;  // small-M kernel: W rows per tile (0 = heuristic)
+  int opt_small_kz;    // small-M kernel: k-blocks per copy (0 = heuristic)
   int pair_clusters;   // CTA pairs that can be resident at once
   int quad_clusters;   // clusters of two CTA pairs that can be resident at once
   uint64_t timeout_ns;
@@ -158,9 +159,11 @@ struct Config {
   int policy_a = gsr::kPolicyNormal;
   int policy_b = gsr::kPolicyNormal;
   size_t ws_bytes = 0;
-  int small = 0;      // the small-M kernel (K-pair clusters, operands swapped)
-  int m_pad = 0;      // small-M: activation rows rounded up to 16 (the MMA's N)
+  int small = 0;      // the small-M kernel (a CTA pair per tile of W rows)
+  int m_pad = 0;      // small-M: activation rows rounded up to 16
   int stages = 0;     // small-M: ring depth
+  int x_rows = 0;     // small-M: activation rows per CTA copy (the X box height)
+  int kz = 1;         // small-M: k-blocks per copy (3-D boxes when > 1)
 };
 
 
@@ -187,37 +190,56 @@ int ag_granule(int R, const int64_t* M_r) {
 
 // Small M (AR/RS, a decode-like batch of at most 256 rows): streaming W is
 // the whole cost, so the small-M kernel runs every activation row against
-// tiles of W rows, each tile split over K between the two CTAs of a cluster.
-// The tile height is the smallest multiple of 8 (up to 128) that covers N
-// with every cluster in the fewest waves, so that all SMs stream W (N = 7168
-// on 76 clusters: 96 rows, 75 tiles). Returns false when the kernel does not
-// apply (or an option forces the main kernel).
+// tiles of W rows, one CTA pair per tile over the whole K range. The tile
+// height (the pair MMA's N) is the smallest multiple of 16 (up to 256) that
+// covers N with every pair in the fewest waves, so that all SMs stream W
+// (N = 7168 on 76 pairs: 96 rows, 75 tiles). Returns false when the kernel
+// does not apply (or an option forces the main kernel).
 bool small_m_config(const gemm_shard_plan* P, int mode, int64_t M, int64_t N, int R,
                     const int64_t* sizes, Config& c) {
   if (mode == gsr::kModeAG || M < 1 || M > gsr::kSmallMaxM || P->opt_small == 1) return false;
   int64_t kb = 0;
   for (int r = 0; r < R; ++r) kb += cdiv(sizes[r], BK);
   const bool forced = P->opt_split || P->opt_block_n || P->opt_cta_group || P->opt_schedule;
-  if (kb < 2 || (P->opt_small != 2 && forced)) return false;
+  if (kb < 1 || (P->opt_small != 2 && forced)) return false;
   c.small = 1;
   c.m_pad = static_cast<int>(std::max<int64_t>(16, cdiv(M, 16) * 16));
-  c.stages = gsr::small_stages(c.m_pad);
   const int cap = P->opt_max_ctas ? std::min(P->opt_max_ctas, P->sm_count) : P->sm_count;
   const int64_t clusters = std::max(cap / 2, 1);
   int64_t rows = P->opt_small_rows;
   if (!rows) {
-    const int64_t waves = cdiv(N, gsr::kSmallTileN * clusters);
-    rows = std::min<int64_t>(gsr::kSmallTileN, cdiv(cdiv(N, waves * clusters), 8) * 8);
+    const int64_t waves = cdiv(N, gsr::kSmallMaxTileN * clusters);
+    rows = std::min<int64_t>(gsr::kSmallMaxTileN, cdiv(cdiv(N, waves * clusters), 16) * 16);
   }
   c.block_n = static_cast<int>(rows);
-  c.cta_group = 1;
-  c.sched = gsr::kSchedKPair;
-  c.splits = 2;
+  c.cta_group = 2;
+  c.sched = gsr::kSchedSmall;
+  c.splits = 1;
+  // k-blocks per copy: the largest of 4, 2, 1 (at most the option) that
+  // leaves a ring of at least four stages in shared memory, where no shard
+  // has a ragged k-block (a 3-D view of a shard would read the next row where
+  // a 2-D box reads zeros). A shard's last copy may run past its k-blocks:
+  // those are zero-filled (no memory read) and add nothing.
+  c.kz = 1;
+  bool whole = true;
+  for (int r = 0; r < R; ++r) whole = whole && sizes[r] % BK == 0;
+  for (int kz = P->opt_small_kz ? P->opt_small_kz : 4; whole && kz > 1 && c.kz == 1; kz /= 2) {
+    const int st = gsr::small_stages(static_cast<int>(M), c.block_n, kz);
+    if (st >= 4 &&
+        gsr::small_layout(static_cast<int>(M), c.block_n, st, kz).total <= gsr::kSmallSmemLimit)
+      c.kz = kz;
+  }
+  // The kernel walks stages of kz k-blocks: kb_total counts them.
+  kb = 0;
+  for (int r = 0; r < R; ++r) kb += cdiv(cdiv(sizes[r], BK), c.kz);
+  c.stages = gsr::small_stages(static_cast<int>(M), c.block_n, c.kz);
+  c.x_rows = static_cast<int>(
+      gsr::small_layout(static_cast<int>(M), c.block_n, c.stages, c.kz).x_rows);
   c.kb_total = kb;
   c.m_tiles = 1;
   c.n_tiles = cdiv(N, rows);
   c.tiles = c.n_tiles;
-  c.units = 2 * c.tiles;
+  c.units = c.tiles;
   c.ctas = static_cast<int>(2 * std::min<int64_t>(c.tiles, clusters));
   // Every cluster reads all of X and a disjoint slice of W.
   const int hints = P->opt_l2_hints;
@@ -431,6 +453,22 @@ Config choose_config(const gemm_shard_plan* P, int mode, int64_t M, int64_t N, i
   return c;
 }
 
+// The same rows viewed as {64 columns, rows, cols / 64 k-blocks} (cols a
+// multiple of 64), with a box of kz k-blocks: one copy lands kz consecutive
+// 128B-swizzled tiles of box_rows rows, one after the other.
+CUresult encode_kmajor_3d(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int box_rows,
+                          int kz) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(BK), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(cols / BK)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * 2, static_cast<cuuint64_t>(BK) * 2};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows),
+                       static_cast<cuuint32_t>(kz)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
 CUresult encode_kmajor(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int box_rows) {
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
@@ -503,6 +541,7 @@ void fill_common(gsr::Params& p, const gemm_shard_plan* P, const Config& c, int 
   p.m_pad = c.m_pad;
   p.stages = c.stages;
   p.tile_rows = c.small ? c.block_n : 0;
+  p.small_kz = c.kz;
   p.ag_gran = BM;   // AG sets its own
   p.timeout_ns = P->timeout_ns;
   uint8_t* w = static_cast<uint8_t*>(ws);
@@ -590,11 +629,14 @@ gsr_status run_ksharded(const gemm_shard_plan* P, int mode, int64_t M, int64_t N
   int kb = 0;
   for (int r = 0; r < R; ++r) {
     p.shard_kb_begin[r] = kb;
-    kb += static_cast<int>(cdiv(K_r[r], BK));
-    // The small-M kernel loads all m_pad activation rows at once.
-    CUresult cr = encode_kmajor(&p.tmap_a[r], X_r[r], M, K_r[r], c.small ? c.m_pad : BM);
+    // The small-M kernel counts stages of kz k-blocks (kz = 1 elsewhere).
+    kb += static_cast<int>(cdiv(cdiv(K_r[r], BK), c.kz));
+    // A small-M CTA loads up to x_rows activation rows at once, kz k-blocks a copy.
+    CUresult cr = c.kz > 1 ? encode_kmajor_3d(&p.tmap_a[r], X_r[r], M, K_r[r], c.x_rows, c.kz)
+                           : encode_kmajor(&p.tmap_a[r], X_r[r], M, K_r[r], c.small ? c.x_rows : BM);
     if (cr != CUDA_SUCCESS) return fail(GSR_ERR_CUDA, "encoding X_r[%d] descriptor failed (%d)", r, (int)cr);
-    cr = encode_kmajor(&p.tmap_b[r], W_r[r], N, K_r[r], c.block_n / c.cta_group);
+    cr = c.kz > 1 ? encode_kmajor_3d(&p.tmap_b[r], W_r[r], N, K_r[r], c.block_n / 2, c.kz)
+                  : encode_kmajor(&p.tmap_b[r], W_r[r], N, K_r[r], c.block_n / c.cta_group);
     if (cr != CUDA_SUCCESS) return fail(GSR_ERR_CUDA, "encoding W_r[%d] descriptor failed (%d)", r, (int)cr);
   }
   for (int r = R; r <= kMaxShards; ++r) p.shard_kb_begin[r] = kb;
@@ -653,6 +695,7 @@ static gemm_shard_plan* new_plan(int device, int sm_count, int64_t max_M, int64_
   P->opt_schedule = 0;
   P->opt_small = 0;
   P->opt_small_rows = 0;
+  P->opt_small_kz = 0;
   P->pair_clusters = sm_count / 2;   // host plans: every SM pairs up
   P->quad_clusters = sm_count / 4;
   P->timeout_ns = 2000000000ull;
@@ -754,10 +797,15 @@ gsr_status gemm_shard_plan_set_option(gemm_shard_plan* plan, gsr_option option, 
       if (value < 0 || value > 2) return fail(GSR_ERR_INVALID_VALUE, "small_m must be 0..2");
       plan->opt_small = static_cast<int>(value);
       return ok();
+    case GSR_OPT_SMALL_KBLOCKS:
+      if (value != 0 && value != 1 && value != 2 && value != 4)
+        return fail(GSR_ERR_INVALID_VALUE, "small_kblocks must be 0, 1, 2 or 4");
+      plan->opt_small_kz = static_cast<int>(value);
+      return ok();
     case GSR_OPT_SMALL_TILE_ROWS:
-      if (value < 0 || value > gsr::kSmallTileN || value % 8)
-        return fail(GSR_ERR_INVALID_VALUE, "small_tile_rows must be 0 or a multiple of 8 up to %d",
-                    gsr::kSmallTileN);
+      if (value < 0 || value > gsr::kSmallMaxTileN || value % 16)
+        return fail(GSR_ERR_INVALID_VALUE, "small_tile_rows must be 0 or a multiple of 16 up to %d",
+                    gsr::kSmallMaxTileN);
       plan->opt_small_rows = static_cast<int>(value);
       return ok();
   }
@@ -1056,6 +1104,7 @@ gsr_status gemm_shard_describe(const gemm_shard_plan* P, int mode, int64_t M, in
   out->sk_iters = c.sk_iters;
   out->ctas = c.ctas;
   out->workspace_bytes = c.ws_bytes;
+  out->kblocks = c.small ? c.kz : 1;
   return ok();
 }
 

@@ -57,21 +57,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return done != 0;
 }
 
-// The same wait with acquire semantics at cluster scope: for phases completed
-// by arrivals (with release at cluster scope) of the peer CTA, whose
-// distributed-shared-memory stores into this CTA must be visible afterwards.
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
-  uint32_t done;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(done)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return done != 0;
-}
-
 // Non-blocking test of the same phase condition.
 __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
   uint32_t done;
@@ -237,26 +222,17 @@ __device__ __forceinline__ void tmem_ld_16cols_wait(uint32_t taddr, uint32_t (&v
                : "memory");
 }
 
-// 16-byte store into the shared memory of a CTA of the cluster (address from mapa).
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                              uint32_t d) {
-  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b),
-               "r"(c), "r"(d)
+// Each thread reads 8 consecutive fp32 columns of its own TMEM lane, and waits.
+__device__ __forceinline__ void tmem_ld_8cols_wait(uint32_t taddr, uint32_t (&v)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+                 "=r"(v[7])
+               : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]), "+r"(v[6]),
+                 "+r"(v[7])
+               :
                : "memory");
-}
-
-// The same 16-byte store into the peer's shared memory, asynchronous: its
-// arrival is counted (16 bytes of complete_tx) on the peer's mbarrier `bar`
-// (a shared::cluster address in the same CTA as `addr`), so a consumer that
-// armed that barrier with the expected byte count sees the data once the
-// phase completes, with no fence or arrive on the sender's side.
-__device__ __forceinline__ void st_async_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                            uint32_t d, uint32_t bar) {
-  asm volatile(
-      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::
-          "r"(addr),
-      "r"(a), "r"(b), "r"(c), "r"(d), "r"(bar)
-      : "memory");
 }
 
 // Named barrier over the 128 epilogue threads.
@@ -309,6 +285,11 @@ __device__ __forceinline__ void cluster_barrier() {
 __device__ __forceinline__ void cluster_arrive() {
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }
+// An arrival that publishes nothing (no release): it does not wait for the
+// thread's earlier memory operations, such as cold descriptor prefetches.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
 __device__ __forceinline__ void cluster_wait() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
@@ -358,6 +339,40 @@ __device__ __forceinline__ void tma_load_2d_pair_multicast(uint32_t dst, const C
       ".multicast::cluster.cta_group::2.L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5, %6;\n\t}"
       ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y),
       "h"(mask), "l"(policy)
+      : "memory");
+}
+
+// tma_load_2d_pair over a 3-D view {x, row, z}: a box of several k-blocks.
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map,
+                                                 uint32_t bar_cluster, int y, int z,
+                                                 uint64_t policy) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;\n\t}" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(0), "r"(y), "r"(z), "l"(policy)
+      : "memory");
+}
+
+// stage_copies_pair with 3-D boxes: A at {0, a_row, z}, B at {0, b_row, z}.
+__device__ __forceinline__ void stage_copies_pair_3d(uint32_t arm, uint32_t full, uint32_t bytes,
+                                                     uint32_t lead_full, uint32_t sa,
+                                                     const CUtensorMap* ma, int a_row, uint32_t sb,
+                                                     const CUtensorMap* mb, int b_row, int z,
+                                                     uint64_t pol_a, uint64_t pol_b) {
+  asm volatile(
+      "{\n\t.reg .pred e, q;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.and.b32 q, %0, 0, e;\n\t"
+      "@q mbarrier.arrive.expect_tx.shared::cta.b64 _, [%1], %2;\n\t"
+      "@e cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%4], [%5, {%13, %6, %7}], [%3], %8;\n\t"
+      "@e cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%9], [%10, {%13, %11, %7}], [%3], %12;\n\t}" ::"r"(arm),
+      "r"(full), "r"(bytes), "r"(lead_full), "r"(sa), "l"(reinterpret_cast<uint64_t>(ma)),
+      "r"(a_row), "r"(z), "l"(pol_a), "r"(sb), "l"(reinterpret_cast<uint64_t>(mb)), "r"(b_row),
+      "l"(pol_b), "r"(0)
       : "memory");
 }
 
@@ -493,25 +508,6 @@ __device__ __noinline__ bool wait_bounded_slow(uint32_t bar, uint32_t parity, co
   const uint64_t limit = c.timeout_ns * (site >> 8);
   for (uint32_t spin = 1;; ++spin) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((spin & 31u) == 0) {
-      if (*c.abort) return false;
-      if (global_timer_ns() - t0 > limit) {
-        *c.abort = 1;
-        atomicCAS(c.status, 0u, kStatusTimeout | site);
-        return false;
-      }
-    }
-  }
-}
-
-// wait_bounded for a phase completed by the peer CTA of a cluster (acquire at
-// cluster scope).
-__device__ __noinline__ bool wait_bounded_cluster(uint32_t bar, uint32_t parity, const Ctl& c,
-                                                  uint32_t site) {
-  const uint64_t t0 = global_timer_ns();
-  const uint64_t limit = c.timeout_ns * (site >> 8);
-  for (uint32_t spin = 1;; ++spin) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
     if ((spin & 31u) == 0) {
       if (*c.abort) return false;
       if (global_timer_ns() - t0 > limit) {

@@ -21,10 +21,9 @@ enum Mode : int { kModeAR = 0, kModeRS = 1, kModeAG = 2, kModeARRep = 3 };
 // the remaining tiles, in tile order, are cut into one contiguous range per
 // worker (a CTA, or a CTA pair), and a tile cut by a worker boundary is
 // summed by the last of its pieces to finish, in k order.
-// K-pair (small-M kernel): each output tile is computed by the two CTAs of a
-// cluster, each over half of the k-blocks, and the two halves are added in
-// distributed shared memory.
-enum Sched : int { kSchedUniform = 0, kSchedStreamK = 1, kSchedKPair = 2, kSchedSplitTail = 3 };
+// Small (small-M kernel): one CTA pair per tile of W rows over the whole K
+// range, tiles dealt round-robin to the pairs.
+enum Sched : int { kSchedUniform = 0, kSchedStreamK = 1, kSchedSmall = 2, kSchedSplitTail = 3 };
 
 // L2 eviction priority requested for an operand's TMA loads.
 enum Policy : int { kPolicyNormal = 0, kPolicyEvictFirst = 1, kPolicyEvictLast = 2 };
@@ -62,7 +61,8 @@ struct Params {  // 128-byte aligned through its CUtensorMap members
   int m_tiles;                  // AR/RS: ceil(M/(BM*CG)); AG: ceil(halves/CG)
   int n_tiles;                  // ceil(N/BN)
   int tiles;                    // m_tiles * n_tiles
-  int kb_total;                 // k-blocks per tile (AR/RS: sum_r ceil(K_r/BK))
+  int kb_total;                 // k-blocks per tile (AR/RS: sum_r ceil(K_r/BK)); the
+                                // small-M kernel: stages of small_kz k-blocks
   int splits;                   // uniform schedule: pieces per tile (1 = none)
   int units;                    // uniform schedule: tiles * splits
   int sched;                    // kSchedUniform, kSchedStreamK or kSchedSplitTail
@@ -74,7 +74,7 @@ struct Params {  // 128-byte aligned through its CUtensorMap members
   int policy_a;                 // L2 policy of A-operand loads (kPolicy*)
   int policy_b;                 // L2 policy of B-operand loads (kPolicy*)
   int rps;                      // RS: rows per shard = ceil(M/R)
-  int shard_kb_begin[kMaxShards + 1];  // AR/RS: first k-block of shard r
+  int shard_kb_begin[kMaxShards + 1];  // AR/RS: first k-block (small-M: stage) of shard r
   int shard_mt_begin[kMaxShards + 1];  // AG: first row granule of shard r
   int ag_halves;                // AG: row granules over all shards
   int ag_gran;                  // AG: rows per granule, 128 (one per CTA tile) or 64
@@ -83,62 +83,85 @@ struct Params {  // 128-byte aligned through its CUtensorMap members
                                 // by the idle half of an odd last pair tile
   int shard_row_begin[kMaxShards + 1]; // AG: first output row of shard r
   int shard_rows[kMaxShards];          // AG: M_r
-  int m_pad;                    // small-M kernel: activation rows rounded up to 16
-                                // (the MMA's N); 0 for the main kernel
+  int m_pad;                    // small-M kernel: activation rows rounded up to 16;
+                                // 0 for the main kernel
   int stages;                   // small-M kernel: depth of the shared-memory ring
-  int tile_rows;                // small-M kernel: W rows per tile (a multiple of 8,
-                                // at most kSmallTileN; TMEM lanes past it unused)
+  int tile_rows;                // small-M kernel: W rows per tile (the pair MMA's N:
+                                // a multiple of 16, at most kSmallMaxTileN)
+  int small_kz;                 // small-M kernel: k-blocks per copy (1: 2-D copies;
+                                // 2 or 4: 3-D copies of that many k-blocks)
 };
 
 // ---------------------------------------------------------------- small M
-// The small-M kernel (M <= kSmallMaxM, AR/RS) swaps the operands: a tile is
-// up to kSmallTileN rows of W (output columns, the MMA's M, always 128: rows
-// past the tile are stale shared memory whose TMEM lanes are never stored)
-// against all m_pad activation rows (the MMA's N). Its shared memory, from a 1024-aligned base:
-// the W ring, the X ring, the staging area that receives the peer CTA's
-// partial for the output rows this CTA finishes (and, once read, the bf16
-// transposes of the finished rows), the mbarriers and a few words. Host and device share
-// this layout.
-constexpr int kSmallTileN = 128;
+// The small-M kernel (M <= kSmallMaxM, AR/RS) runs one CTA pair (a cluster of
+// two) per tile of tile_rows rows of W (output columns; a multiple of 16, at
+// most kSmallMaxTileN) over the whole K range, with every activation row in
+// the tile: tcgen05.mma.cta_group::2 with the activation rows as the MMA's M
+// (each CTA holds h = ceil(M / 2) rows rounded up to 16: an MMA of 128 rows,
+// 64 per CTA, when h <= 64, else of 256, 128 per CTA) and the tile's W rows
+// as its N (each CTA holds half of them). A ring stage holds kz consecutive
+// k-blocks of each operand (one copy each: kz = 1 is a 2-D box, kz = 2 or 4
+// a 3-D box over a {64, rows, K_r / 64} view of the shard, whose last stage
+// may run past the shard's k-blocks into zero fill). Its shared memory, from a
+// 1024-aligned base: the X ring, the W ring, the mbarriers and a few words.
+// Host and device share this layout.
 constexpr int kSmallMaxM = 256;
-constexpr int kSmallEpiWarps = 8;            // two per TMEM lane quarter
-constexpr int kSmallEpiThreads = 32 * kSmallEpiWarps;
-constexpr int kSmallThreads = 64 + kSmallEpiThreads;  // warp 0 TMA, warp 1 MMA, the rest epilogue
-constexpr int kGranule = 16;                 // output rows per exchange granule
-constexpr int kSmallMaxStages = 16;
-constexpr uint32_t kSmallSmemLimit = 232448; // 227 KB per CTA
+constexpr int kSmallMaxTileN = 256;
+constexpr int kSmallEpiWarps = 4;                 // one per TMEM lane quarter
+constexpr int kSmallThreads = 64 + 32 * kSmallEpiWarps;  // warp 0 TMA, warp 1 MMA, the rest epilogue
+constexpr int kSmallMaxStages = 32;
+constexpr uint32_t kSmallSmemLimit = 232448;     // 227 KB per CTA
 
 struct SmallLayout {
-  uint32_t w_bytes, x_bytes, stages;
-  uint32_t x_off, staging_off, bars_off, misc_off, total;  // total includes 1024 of alignment slack
-  uint32_t tmem_cols, acc_stride;
+  uint32_t mma_m;        // 128 (x_rows <= 64) or 256
+  uint32_t x_rows;       // h: activation rows per CTA (rank r holds rows r*h ..
+                         // r*h + h); the X box height
+  uint32_t kz;           // k-blocks per stage
+  uint32_t x_bytes, w_bytes;    // one k-block of X, of W
+  uint32_t x_stage, w_stage;    // one stage: kz k-blocks
+  uint32_t stages;
+  uint32_t w_off, bars_off, misc_off, total;  // total includes 1024 of alignment slack
+  uint32_t acc_cols;     // TMEM columns one accumulator uses
+  uint32_t acc_stride;   // columns between the two accumulators
+  uint32_t tmem_cols;    // allocated: a power of two, at least 32
 };
 
-__host__ __device__ inline uint32_t small_owned_granules(int m_pad) {
-  return static_cast<uint32_t>((m_pad / kGranule + 1) / 2);
-}
-
-__host__ __device__ inline SmallLayout small_layout(int m_pad, int stages) {
+__host__ __device__ inline SmallLayout small_layout(int M, int tile_rows, int stages, int kz) {
   SmallLayout L;
-  L.w_bytes = kSmallTileN * BK * 2;
-  L.x_bytes = static_cast<uint32_t>(m_pad) * BK * 2;
+  // The rows are split evenly over the pair, so that both CTAs stream the same
+  // bytes; the MMA reads mma_m / 2 rows from each, of which rows past h are
+  // stale shared memory (TMEM lanes that are never stored) and rows past M
+  // are zero-filled by the copy (or, when a CTA has none, never loaded).
+  const int half = (M + 1) / 2;
+  L.x_rows = static_cast<uint32_t>(half <= 16 ? 16 : (half + 15) / 16 * 16);
+  L.mma_m = L.x_rows <= 64 ? 128u : 256u;
+  L.x_bytes = L.x_rows * BK * 2;
+  L.w_bytes = static_cast<uint32_t>(tile_rows / 2) * BK * 2;
+  L.kz = static_cast<uint32_t>(kz);
+  L.x_stage = L.kz * L.x_bytes;
+  L.w_stage = L.kz * L.w_bytes;
   L.stages = static_cast<uint32_t>(stages);
-  L.x_off = L.stages * L.w_bytes;
-  L.staging_off = L.x_off + L.stages * L.x_bytes;
-  L.bars_off = L.staging_off + small_owned_granules(m_pad) * kGranule * kSmallTileN * 4;
-  L.misc_off = L.bars_off + (2 * L.stages + 7) * 8;
+  L.w_off = L.stages * L.x_stage;
+  // The MMA reads mma_m / 2 rows from an X k-block: the last one's read runs
+  // past the X ring into the W ring (or, if that is shorter, into padding).
+  uint32_t end = L.w_off + L.stages * L.w_stage;
+  const uint32_t x_read_end = L.w_off - L.x_bytes + L.mma_m / 2 * BK * 2;
+  if (x_read_end > end) end = x_read_end;
+  L.bars_off = end;
+  L.misc_off = L.bars_off + (2 * L.stages + 5) * 8;   // full, empty, tfull[2], tempty[2], drain
   L.total = 1024 + L.misc_off + 16;
+  L.acc_cols = L.mma_m == 256 ? static_cast<uint32_t>(tile_rows) : static_cast<uint32_t>(tile_rows / 2);
+  L.acc_stride = (L.acc_cols + 31) / 32 * 32;
   uint32_t cols = 32;
-  while (cols < 2u * static_cast<uint32_t>(m_pad)) cols *= 2;
+  while (cols < 2 * L.acc_stride) cols *= 2;
   L.tmem_cols = cols;
-  L.acc_stride = cols / 2;
   return L;
 }
 
-// Deepest ring that fits the shared-memory limit for m_pad activation rows.
-__host__ __device__ inline int small_stages(int m_pad) {
+// Deepest ring that fits the shared-memory limit.
+__host__ __device__ inline int small_stages(int M, int tile_rows, int kz) {
   int s = kSmallMaxStages;
-  while (s > 2 && small_layout(m_pad, s).total > kSmallSmemLimit) --s;
+  while (s > 2 && small_layout(M, tile_rows, s, kz).total > kSmallSmemLimit) --s;
   return s;
 }
 
@@ -170,7 +193,7 @@ cudaError_t launch_gemm(const Params& p, int block_n, int cta_group, int ctas, c
 // clusters of two CTA pairs, can be resident.
 cudaError_t prepare_kernels(int device, int* pair_clusters, int* quad_clusters);
 size_t kernel_smem_bytes(int block_n, int cta_group);
-// The small-M kernel (gsr_small.cu): `ctas` is even (clusters of two).
+// The small-M kernel (gsr_small.cu): `ctas` is even (CTA pairs).
 cudaError_t launch_small(const Params& p, int ctas, cudaStream_t stream);
 cudaError_t prepare_small_kernel();
 // The packed gather (gsr_pack.cu): one warp per CTA.

@@ -7,37 +7,40 @@
 // for the shapes where the work is streaming W from HBM: with few activation
 // rows, W (N x K) is the only large operand.
 //
-// Operands are swapped so that no tensor-core row is wasted on a short batch:
-// a tile is tile_rows rows of W (output columns; the MMA's M) against all m_pad
-// activation rows (M rounded up to 16; the MMA's N), Y^T[n, m] accumulated in
-// TMEM with TMEM lane = output column and TMEM column = output row. The MMA is
-// always 128 rows tall; with tile_rows < 128 (a multiple of 8, chosen so that
-// N spreads over every pair of SMs) the rows past the tile read stale shared
-// memory into TMEM lanes that are never stored.
+// One CTA pair (a cluster of two) owns a tile of tile_rows rows of W (output
+// columns) over the whole K range (every shard's k-blocks, in shard order),
+// against every activation row: tcgen05.mma.cta_group::2 with the activation
+// rows as the MMA's M and the tile's W rows as its N, so the pair streams a
+// disjoint slice of W and nothing is reduced between CTAs. Each CTA holds
+// half of the tile's W rows and h = ceil(M / 2) activation rows (rounded up
+// to 16; rank r holds rows r*h .. r*h + h, so both stream the same bytes):
+// - h <= 64: the MMA's M is 128, 64 rows per CTA. The accumulator of a CTA
+//   holds its 64 rows twice over in TMEM: lanes 0-63 the tile's first
+//   tile_rows/2 columns, lanes 64-127 the others (columns 0 .. tile_rows/2).
+// - h > 64: the MMA's M is 256, 128 rows per CTA, lane i = row i of the
+//   CTA's half, every column of the tile.
+// The MMA's rows past h read stale shared memory into TMEM lanes that are
+// never stored; a CTA whose rows are all past M loads no activations.
+// The MMA is always the same size for a given M: each output element is the
+// same chain of fp32 additions over k (k-blocks in shard order, four K = 16
+// steps each) whatever the tile height, so every tile height gives the same
+// bits, and RS rows equal AR rows.
 //
-// Each tile belongs to a cluster of two CTAs. CTA rank k accumulates the
-// k-blocks of its half of the K range (over every shard's k-blocks, in shard
-// order), so both stream disjoint halves of the tile's W rows. The two fp32
-// halves are then added in distributed shared memory instead of through global
-// memory: the output rows are cut into 16-row granules, the first half of the
-// granules is finished by rank 0 and the rest by rank 1, and each CTA writes
-// the granules its peer finishes straight into the peer's shared memory with
-// asynchronous stores (st.async) whose bytes complete the peer's mbarrier,
-// which the peer armed with the byte count it expects. The owner adds the
-// peer's half to its own (one fp32 addition per output, commutative, so the
-// result does not depend on which CTA adds), rounds to bf16 (round to nearest
-// even) and transposes each 32 x 32 block through shared memory so that the
-// global stores are 16-byte vectors, four per 64-byte row segment (a thread
-// holds one output column; storing its 2-byte values row by row measured an
-// order of magnitude slower). RS routes output row m to
-// shard m / rps; the configuration depends only on the shape, so RS rows equal
-// AR rows bit for bit.
+// A ring stage holds kz consecutive k-blocks of each operand, one copy each
+// (kz > 1: a 3-D box over a {64, rows, K_r / 64} view of the shard; a
+// shard's last stage may run past its k-blocks, which the copy zero-fills and
+// the MMAs add as zeros). The stream runs at a roughly fixed number of stages
+// per unit time per SM, whatever their size: 48-row W boxes of one k-block
+// streamed W at 2.2 TB/s, of two k-blocks at 3.6 TB/s.
 //
-// Roles (320 threads): warp 0 TMA producer, warp 1 MMA issuer, warps 2..9
-// epilogue, two per quarter of the TMEM lanes (a warp reads only the lanes of
-// its own quarter), taking alternate 32-row chunks of the output rows: the
-// epilogue is latency-bound inside each warp, so two warps per quarter halve
-// it. Every wait is bounded by %globaltimer like the main kernel's.
+// Both CTAs' copies of a stage complete on the leader's (rank 0's) barrier;
+// the leader issues the MMAs and its commits free the slot in both CTAs. The
+// epilogue of each CTA reads its own rows from TMEM and stores each thread's
+// columns of its row as 16-byte vectors (no exchange, no transpose).
+//
+// Roles (192 threads): warp 0 TMA producer, warp 1 MMA issuer (leader only),
+// warps 2..5 epilogue, one per quarter of the TMEM lanes. Every wait is
+// bounded by %globaltimer like the main kernel's.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -49,40 +52,47 @@
 namespace gsr {
 namespace {
 
+// Named barrier 2: warp 1 (which allocates the TMEM) and the epilogue warps.
+__device__ __forceinline__ void tmem_handoff_sync() {
+  asm volatile("bar.sync 2, %0;" ::"n"(32 + 32 * kSmallEpiWarps) : "memory");
+}
+
+// Named barrier 3: warp 1 (which creates the mbarriers) and the producer.
+__device__ __forceinline__ void barriers_ready_arrive() {
+  asm volatile("bar.arrive 3, 64;" ::: "memory");
+}
+__device__ __forceinline__ void barriers_ready_sync() {
+  asm volatile("bar.sync 3, 64;" ::: "memory");
+}
+
 // Barrier offsets of the small kernel (bytes from the barrier base).
 struct SmallBars {
-  uint32_t full0, empty0, tfull0, tempty0, staged, drained, drain;
+  uint32_t full0, empty0, tfull0, tempty0, drain;
   __device__ explicit SmallBars(uint32_t bars, uint32_t stages)
       : full0(bars),
         empty0(bars + 8 * stages),
         tfull0(bars + 16 * stages),
         tempty0(bars + 16 * stages + 16),
-        staged(bars + 16 * stages + 32),
-        drained(bars + 16 * stages + 40),
-        drain(bars + 16 * stages + 48) {}
+        drain(bars + 16 * stages + 32) {}
 };
 
-// The k-blocks of CTA `rank` of the pair: the first or the second half.
-__device__ __forceinline__ void kpair_range(const Params& p, uint32_t rank, int& lo, int& hi) {
-  const int half = p.kb_total / 2;
-  lo = rank ? half : 0;
-  hi = rank ? p.kb_total : half;
-}
-
-// Walks the k-blocks this CTA loads, in order: its tiles in turn, each over
-// this CTA's half of the K range. The whole producer warp runs it with
-// warp-uniform values; lane r holds shard r's first k-block (`begins`), read
-// with a shuffle, so the loop issues no load from the kernel's parameter space
-// (dynamically indexed parameter loads measured several hundred ns each and
-// throttled the TMA stream when made per k-block).
+// Walks the k-blocks of this pair's tiles, in order: each tile over the whole
+// K range. The whole producer warp runs it with warp-uniform values; lane r
+// holds shard r's first k-block (`begins`), read with a shuffle, so the loop
+// issues no load from the kernel's parameter space (dynamically indexed
+// parameter loads measured several hundred ns each and throttled the TMA
+// stream when made per k-block).
 static_assert(kMaxShards + 1 <= 32, "the shard table must fit in the lanes of a warp");
 
+// `kb` counts stages (kz k-blocks each; one k-block when kz = 1).
 struct KCursor {
-  int n0, n_step, kb, shard, shard_begin, next_begin;
-  __device__ void start(int begins, int kb_lo, int tile_rows) {
+  int n0, n_step, kb, kb_end, kz, shard, shard_begin, next_begin;
+  __device__ void start(int begins, int stages_per_tile, int tile_rows, int kblocks) {
     n0 = static_cast<int>(blockIdx.x) / 2 * tile_rows;
     n_step = static_cast<int>(gridDim.x) / 2 * tile_rows;
-    kb = kb_lo;
+    kb = 0;
+    kb_end = stages_per_tile;
+    kz = kblocks;
     seek(begins, 0);
   }
   __device__ __forceinline__ void seek(int begins, int from) {
@@ -91,10 +101,12 @@ struct KCursor {
     while (next_begin <= kb) next_begin = __shfl_sync(0xffffffffu, begins, ++shard + 1);
     shard_begin = __shfl_sync(0xffffffffu, begins, shard);
   }
+  // The stage's first k-block within its shard (the 3-D box's z), and its column (2-D).
+  __device__ __forceinline__ int kz_index() const { return (kb - shard_begin) * kz; }
   __device__ __forceinline__ int kx() const { return (kb - shard_begin) * BK; }
-  __device__ __forceinline__ void advance(int begins, int kb_lo, int kb_hi) {
-    if (++kb == kb_hi) {
-      kb = kb_lo;
+  __device__ __forceinline__ void advance(int begins) {
+    if (++kb == kb_end) {
+      kb = 0;
       n0 += n_step;
       seek(begins, 0);
     } else if (next_begin <= kb) {
@@ -103,8 +115,8 @@ struct KCursor {
   }
 };
 
-// Number of tiles this cluster walks.
-__device__ __forceinline__ int small_tiles_of_cluster(const Params& p) {
+// Number of tiles this pair walks.
+__device__ __forceinline__ int small_tiles_of_pair(const Params& p) {
   const int c = static_cast<int>(blockIdx.x) / 2, step = static_cast<int>(gridDim.x) / 2;
   return c < p.n_tiles ? (p.n_tiles - 1 - c) / step + 1 : 0;
 }
@@ -116,39 +128,44 @@ __device__ __forceinline__ int small_tiles_of_cluster(const Params& p) {
 struct ProducerStart {
   uint64_t pol_x, pol_w;
   uint32_t stage_tx;
-  int kb_lo, kb_hi, total, begins;
+  int total, begins, x_row, w_row_off;
+  bool load_x;
   KCursor kc;
   // Called by the whole producer warp.
   __device__ void init(const Params& p, const SmallLayout& L, uint32_t rank) {
     pol_x = make_l2_policy(p.policy_a);
     pol_w = make_l2_policy(p.policy_b);
-    // A slot's barrier counts both tiles: tile_rows rows of W and m_pad rows of X.
-    stage_tx = static_cast<uint32_t>(p.tile_rows) * BK * 2 + L.x_bytes;
+    x_row = static_cast<int>(rank * L.x_rows);
+    load_x = x_row < p.M;
+    w_row_off = static_cast<int>(rank) * (p.tile_rows / 2);
+    // The leader's barrier counts both CTAs' copies: two W halves, the
+    // leader's activation rows and, if it has any, the peer's.
+    stage_tx = 2 * L.w_stage + L.x_stage * (static_cast<int>(L.x_rows) < p.M ? 2u : 1u);
     // shard_kb_begin[0..kMaxShards] in lanes 0..16 (kMaxShards + 1 <= 32)
     const int lane = static_cast<int>(threadIdx.x) & 31;
     begins = p.shard_kb_begin[lane <= kMaxShards ? lane : kMaxShards];
-    kpair_range(p, rank, kb_lo, kb_hi);
-    total = (kb_hi - kb_lo) * small_tiles_of_cluster(p);
-    kc.start(begins, kb_lo, p.tile_rows);
+    total = p.kb_total * small_tiles_of_pair(p);
+    kc.start(begins, p.kb_total, p.tile_rows, p.small_kz);
     prefetch_tensormap(&p.tmap_b[kc.shard]);
-    prefetch_tensormap(&p.tmap_a[kc.shard]);
+    if (load_x) prefetch_tensormap(&p.tmap_a[kc.shard]);
   }
 };
 
 __device__ void small_producer(const Params& p, const SmallLayout& L, uint32_t base,
-                               const SmallBars& b, ProducerStart& st, const Ctl& ctl) {
+                               const SmallBars& b, ProducerStart& st, uint32_t rank,
+                               const Ctl& ctl) {
   const uint64_t pol_x = st.pol_x, pol_w = st.pol_w;
   const uint32_t stage_tx = st.stage_tx;
-  const int kb_lo = st.kb_lo, kb_hi = st.kb_hi, total = st.total, begins = st.begins;
+  const int total = st.total, begins = st.begins, x_row = st.x_row, w_row_off = st.w_row_off;
+  const bool load_x = st.load_x;
+  const uint32_t arm = rank == 0 ? 1u : 0u;
+  // This loop alone feeds the tensor pipe: its critical path is kept short
+  // (slot and parity advance incrementally; no division or search per k-block).
   KCursor& kc = st.kc;
-  // This loop alone feeds the tensor pipe and shares its scheduler with a
-  // waiting warp: its critical path is kept short (slot and parity advance
-  // incrementally; no division or search per k-block). Each added operation
-  // per k-block measured as lost HBM bandwidth.
   uint32_t slot = 0, slot_parity = 1, issued = 0;
   bool ok = true;
   for (int i = 0; i < total; ++i) {
-    // Slot `slot` is free once the MMAs of k-block i - stages are done.
+    // Slot `slot` is free once the pair's MMAs of stage i - stages are done.
     const bool free_slot = wait_bounded(b.empty0 + 8 * slot, slot_parity, ctl, (kRoleProducer << 8) | 1);
     __syncwarp();
     if (!free_slot) {
@@ -156,15 +173,27 @@ __device__ void small_producer(const Params& p, const SmallLayout& L, uint32_t b
       break;
     }
     const uint32_t full = b.full0 + 8 * slot;
-    mbar_arrive_expect_tx(full, stage_tx);
-    // W rows past N and activation rows past M (up to m_pad) are zero-filled.
-    tma_load_2d_hint(base + slot * L.w_bytes, &p.tmap_b[kc.shard], full, kc.kx(), kc.n0, pol_w);
-    tma_load_2d_hint(base + L.x_off + slot * L.x_bytes, &p.tmap_a[kc.shard], full, kc.kx(), 0, pol_x);
-    kc.advance(begins, kb_lo, kb_hi);
+    const uint32_t lead_full = map_shared_to_rank(full, 0);
+    const uint32_t xs = base + slot * L.x_stage, ws = base + L.w_off + slot * L.w_stage;
+    // W rows past N and activation rows past M are zero-filled.
+    if (L.kz == 1) {
+      if (load_x)
+        stage_copies_pair(arm, full, stage_tx, lead_full, xs, &p.tmap_a[kc.shard], x_row, ws,
+                          &p.tmap_b[kc.shard], kc.n0 + w_row_off, kc.kx(), pol_x, pol_w);
+      else
+        tma_load_2d_pair(ws, &p.tmap_b[kc.shard], lead_full, kc.kx(), kc.n0 + w_row_off, pol_w);
+    } else {
+      if (load_x)
+        stage_copies_pair_3d(arm, full, stage_tx, lead_full, xs, &p.tmap_a[kc.shard], x_row, ws,
+                             &p.tmap_b[kc.shard], kc.n0 + w_row_off, kc.kz_index(), pol_x, pol_w);
+      else
+        tma_load_3d_pair(ws, &p.tmap_b[kc.shard], lead_full, kc.n0 + w_row_off, kc.kz_index(), pol_w);
+    }
+    kc.advance(begins);
     if (++issued == 1) {
       // The other shards' descriptors, once the first copies are on their way.
       for (int r = 0; r < p.R; ++r) {
-        prefetch_tensormap(&p.tmap_a[r]);
+        if (load_x) prefetch_tensormap(&p.tmap_a[r]);
         prefetch_tensormap(&p.tmap_b[r]);
       }
     }
@@ -173,19 +202,29 @@ __device__ void small_producer(const Params& p, const SmallLayout& L, uint32_t b
       slot_parity ^= 1u;
     }
   }
-  if (!ok) {
-    // Let the copies already issued land before the shared memory goes away.
+  if (ok) {
+    // The leader's commits for the last ring's worth of stages land here
+    // too; nothing else waits for them, and they must land before this CTA
+    // leaves (its exit barrier does not order them).
+    const uint32_t first = issued > L.stages ? issued - L.stages : 0;
+    for (uint32_t i = first; i < issued && ok; ++i) {
+      ok = wait_bounded(b.empty0 + 8 * (i % L.stages), (i / L.stages) & 1u, ctl, (kRoleProducer << 8) | 2);
+      __syncwarp();
+    }
+  } else {
+    // Let the copies already issued land before the shared memory goes away
+    // (they complete on the leader's barrier; this CTA cannot see them, so it
+    // waits for the pair's MMAs to have freed the slots, or gives up).
     const uint32_t first = issued > L.stages ? issued - L.stages : 0;
     for (uint32_t i = first; i < issued; ++i)
-      wait_drain(b.full0 + 8 * (i % L.stages), (i / L.stages) & 1u, 100000000ull);
+      wait_drain(b.empty0 + 8 * (i % L.stages), (i / L.stages) & 1u, 100000000ull);
   }
 }
 
+// The pair's MMAs (rank 0 only).
 __device__ void small_mma(const Params& p, const SmallLayout& L, uint32_t base, const SmallBars& b,
-                          uint32_t tmem_base, uint32_t rank, const Ctl& ctl) {
-  int kb_lo, kb_hi;
-  kpair_range(p, rank, kb_lo, kb_hi);
-  const uint32_t idesc = make_idesc(kSmallTileN, static_cast<uint32_t>(p.m_pad));
+                          uint32_t tmem_base, const Ctl& ctl) {
+  const uint32_t idesc = make_idesc(L.mma_m, static_cast<uint32_t>(p.tile_rows));
   uint32_t stage = 0, phase = 0, local = 0;
   bool ok = true, issued_any = false;
   for (int tile = static_cast<int>(blockIdx.x) / 2; ok && tile < p.n_tiles;
@@ -200,7 +239,7 @@ __device__ void small_mma(const Params& p, const SmallLayout& L, uint32_t base, 
     }
     tc_fence_after_sync();
     const uint32_t d_tmem = tmem_base + acc * L.acc_stride;
-    for (int kb = kb_lo; kb < kb_hi; ++kb) {
+    for (int kb = 0; kb < p.kb_total; ++kb) {   // stages of kz k-blocks
       const bool got = wait_bounded(b.full0 + 8 * stage, phase, ctl, (kRoleMma << 8) | 2);
       __syncwarp();
       if (!got) {
@@ -208,31 +247,24 @@ __device__ void small_mma(const Params& p, const SmallLayout& L, uint32_t base, 
         break;
       }
       tc_fence_after_sync();
-      const uint64_t w_desc = smem_desc_sw128(base + stage * L.w_bytes);
-      const uint64_t x_desc = smem_desc_sw128(base + L.x_off + stage * L.x_bytes);
-#pragma unroll
-      for (int k = 0; k < BK / 16; ++k)
-        mma_bf16_ss(d_tmem, w_desc + 2 * k, x_desc + 2 * k, idesc,
-                    (kb > kb_lo || k > 0) ? 1u : 0u);
+      const uint32_t xs = base + stage * L.x_stage, ws = base + L.w_off + stage * L.w_stage;
+      for (uint32_t j = 0; j < L.kz; ++j)
+        mma4_bf16_pair(d_tmem, smem_desc_sw128(xs + j * L.x_bytes),
+                       smem_desc_sw128(ws + j * L.w_bytes), idesc, (kb > 0 || j > 0) ? 1u : 0u);
       issued_any = true;
-      mma_commit(b.empty0 + 8 * stage);
+      mma_commit_pair(b.empty0 + 8 * stage, 0x3);   // frees the slot in both CTAs
       if (++stage == L.stages) {
         stage = 0;
         phase ^= 1u;
       }
     }
     if (!ok) break;
-    mma_commit(b.tfull0 + 8 * acc);
+    mma_commit_pair(b.tfull0 + 8 * acc, 0x3);       // both CTAs' epilogues may read
   }
   if (!ok && issued_any) {
-    mma_commit(b.drain);
+    mma_commit_pair(b.drain, 0x1);
     wait_drain(b.drain, 0, 100000000ull);
   }
-}
-
-__device__ __forceinline__ uint16_t bf16_bits(float x) {
-  __nv_bfloat16 h = __float2bfloat16_rn(x);
-  return *reinterpret_cast<uint16_t*>(&h);
 }
 
 // Row m of the output (routed by mode). The parameters it needs are read when
@@ -256,137 +288,63 @@ struct OutRows {
   }
 };
 
-// Up to two consecutive granules (32 TMEM columns) of this thread's lane.
-__device__ __forceinline__ void load_granules(uint32_t taddr, int count, uint32_t (&v)[32]) {
-  if (count == 2) {
-    tmem_ld_32cols(taddr, v);
-    tmem_ld_wait(v);
-  } else {
-    tmem_ld_16cols_wait(taddr, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
-  }
-}
-
-__device__ void small_epilogue(const Params& p, const SmallLayout& L, uint32_t base,
-                               uint8_t* base_ptr, const SmallBars& b, uint32_t tmem_base,
-                               uint32_t rank, const Ctl& ctl) {
+__device__ void small_epilogue(const Params& p, const SmallLayout& L, const SmallBars& b,
+                               uint32_t tmem_base, uint32_t rank, const Ctl& ctl) {
   const int lane = static_cast<int>(threadIdx.x) & 31;
-  const int ew = (static_cast<int>(threadIdx.x) >> 5) - 2;     // epilogue warp 0..7
   const int quad = (static_cast<int>(threadIdx.x) >> 5) & 3;  // TMEM lanes this warp may read
-  const int first = 2 * (ew >> 2);   // this warp's first granule pair: chunks alternate
+  const int idx = quad * 32 + lane;                            // this thread's TMEM lane
   const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
-  const int granules = p.m_pad / kGranule;
-  const int g_split = static_cast<int>(small_owned_granules(p.m_pad));  // rank 0 owns [0, g_split)
-  const int own_lo = rank ? g_split : 0, own_hi = rank ? granules : g_split;
-  const int peer_lo = rank ? 0 : g_split, peer_hi = rank ? g_split : granules;
-  const uint32_t peer = rank ^ 1u;
-  // Staging: [granule of the owner's range][column group of 4][TMEM lane][4] fp32.
-  const uint32_t peer_staging = map_shared_to_rank(base + L.staging_off, peer);
-  const float4* my_staging = reinterpret_cast<const float4*>(base_ptr + L.staging_off);
-  const uint32_t peer_staged = map_shared_to_rank(b.staged, peer);
-  const uint32_t peer_drained = map_shared_to_rank(b.drained, peer);
-  const int col_lane = quad * 32 + lane;   // this thread's TMEM lane = column in the tile
-  const int reps = p.mode == kModeARRep ? p.R : 1;
-  // A quarter of TMEM lanes wholly past the tile (96-row tiles: lanes 96..127)
-  // holds no output: its warps only take part in the handshakes.
-  const bool live = quad * 32 < p.tile_rows;
+  const int half = p.tile_rows / 2;
+  // This thread's row among the CTA's activation rows, its output row and its
+  // columns within the tile (see the layouts at the top of the file).
+  const int a_row = L.mma_m == 256 ? idx : (idx & 63);
+  const int row = static_cast<int>(rank * L.x_rows) + a_row;
+  const int col0 = L.mma_m == 256 ? 0 : (idx >> 6) * half;
+  const int ncols = static_cast<int>(L.acc_cols);
   const OutRows out(p);
-  const int m_rows = p.M;
-  // Bytes the peer sends this CTA per tile (its complete_tx on `staged`): 16
-  // fp32 per owned granule for every TMEM lane of a live quarter.
-  const uint32_t rx_bytes = static_cast<uint32_t>((own_hi - own_lo) * ((p.tile_rows + 31) / 32) *
-                                                  32 * kGranule * 4);
-  uint32_t local = 0;
+  const bool live = a_row < static_cast<int>(L.x_rows) && row < p.M;
+  const int reps = p.mode == kModeARRep ? p.R : 1;
+  const uint32_t lead_tempty = map_shared_to_rank(b.tempty0, 0);
   const int step = static_cast<int>(gridDim.x) / 2;
+  uint32_t local = 0;
   for (int tile = static_cast<int>(blockIdx.x) / 2; tile < p.n_tiles; tile += step, ++local) {
     const uint32_t acc = local & 1u;
-    // One arrive per tile, with the bytes to expect; the staged wait of the
-    // previous tile (same warp) has seen the previous phase complete.
-    if (ew == 0) mbar_arrive_expect_tx(b.staged, rx_bytes);
-    bool ok = wait_bounded(b.tfull0 + 8 * acc, (local >> 1) & 1u, ctl, (kRoleEpilogue << 8) | 1);
-    if (!epilogue_bar_and<kSmallEpiThreads>(ok)) break;
+    const bool ok = wait_bounded(b.tfull0 + 8 * acc, (local >> 1) & 1u, ctl, (kRoleEpilogue << 8) | 1);
+    if (!epilogue_bar_and<32 * kSmallEpiWarps>(ok)) break;
     tc_fence_after_sync();
     const uint32_t taddr = tmem_base + lane_addr + acc * L.acc_stride;
-    const int n0 = tile * p.tile_rows;
-    const int n_end = min(n0 + p.tile_rows, p.N);   // TMEM lanes past the tile are not output
-
-    // 1. The granules the peer finishes go into the peer's staging area, once
-    //    the peer has consumed what this CTA sent for the previous tile. The
-    //    stores are asynchronous and counted on the peer's staged barrier.
-    if (local > 0) {
-      ok = wait_bounded_cluster(b.drained, (local - 1) & 1u, ctl, (kRoleEpilogue << 8) | 2);
-      if (!epilogue_bar_and<kSmallEpiThreads>(ok)) break;
-    }
-    for (int g = peer_lo + first; live && g < peer_hi; g += 4) {
-      const int cnt = min(2, peer_hi - g);
-      uint32_t v[32];
-      load_granules(taddr + g * kGranule, cnt, v);
-      const uint32_t dst = peer_staging + ((g - peer_lo) * 4 * kSmallTileN + col_lane) * 16;
+    const int n_base = tile * p.tile_rows + col0;
+    for (int c = 0; c < ncols; c += 16) {
+      // 16 columns per TMEM load; an 8-column load for a ragged last chunk
+      // (never past the accumulator's columns).
+      uint32_t v[16];
+      const int cnt = ncols - c >= 16 ? 16 : 8;
+      if (cnt == 16)
+        tmem_ld_16cols_wait(taddr + c, v);
+      else
+        tmem_ld_8cols_wait(taddr + c, *reinterpret_cast<uint32_t(*)[8]>(&v[0]));
+      if (live) {
 #pragma unroll
-      for (int c4 = 0; c4 < 8; ++c4)
-        if (c4 < 4 * cnt)
-          st_async_v4(dst + c4 * kSmallTileN * 16, v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2],
-                      v[4 * c4 + 3], peer_staged);
-    }
-
-    // 2. This CTA's granules: its own half plus the peer's, rounded to bf16,
-    //    transposed and stored. The transpose goes back into the part of the
-    //    staging area this warp has just read (its 32 lanes of the granules'
-    //    column groups, 512 bytes each, 2048 bytes apart): 8 rows of 32 bf16
-    //    columns per block, so no separate buffer is needed.
-    ok = wait_bounded_cluster(b.staged, local & 1u, ctl, (kRoleEpilogue << 8) | 3);
-    if (!epilogue_bar_and<kSmallEpiThreads>(ok)) break;
-    for (int g = own_lo + first; live && g < own_hi; g += 4) {
-      const int cnt = min(2, own_hi - g);
-      uint32_t v[32];
-      load_granules(taddr + g * kGranule, cnt, v);
-      const float4* src = my_staging + (g - own_lo) * 4 * kSmallTileN + col_lane;
-      uint8_t* const blocks = base_ptr + L.staging_off +
-                              static_cast<size_t>((g - own_lo) * 4 * kSmallTileN + quad * 32) * 16;
-      float4 f[8];
-#pragma unroll
-      for (int c4 = 0; c4 < 8; ++c4)
-        if (c4 < 4 * cnt) f[c4] = src[c4 * kSmallTileN];
-      __syncwarp();   // every lane has read its staging before the blocks are overwritten
-      // rows 16g .. 16g + 16 cnt of this warp's 32 columns: row r at block r / 8
-#pragma unroll
-      for (int c4 = 0; c4 < 8; ++c4) {
-        if (c4 >= 4 * cnt) break;
-        const float a[4] = {f[c4].x, f[c4].y, f[c4].z, f[c4].w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int r = 4 * c4 + j;
-          reinterpret_cast<uint16_t*>(blocks + (r >> 3) * (kSmallTileN * 16) + (r & 7) * 64)[lane] =
-              bf16_bits(__uint_as_float(v[r]) + a[j]);
+        for (int j = 0; j < 2; ++j) {
+          const int n = n_base + c + 8 * j;
+          if (8 * j < cnt && n < out.N) {
+            uint4 w;
+            w.x = pack_bf16x2(v[8 * j + 0], v[8 * j + 1]);
+            w.y = pack_bf16x2(v[8 * j + 2], v[8 * j + 3]);
+            w.z = pack_bf16x2(v[8 * j + 4], v[8 * j + 5]);
+            w.w = pack_bf16x2(v[8 * j + 6], v[8 * j + 7]);
+            for (int rep = 0; rep < reps; ++rep)
+              *reinterpret_cast<uint4*>(out.row(p, row, rep) + n) = w;
+          }
         }
       }
-      __syncwarp();
-      // 16-byte vectors: 8 rows x 4 parts of 8 columns per instruction
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const int vi = lane + 32 * t;
-        const int row = vi >> 2, part = vi & 3;
-        const int m = g * kGranule + row;
-        const int n = n0 + quad * 32 + part * 8;
-        if (row < kGranule * cnt && m < m_rows && n < n_end) {
-          const uint4 val = *reinterpret_cast<const uint4*>(blocks + t * (kSmallTileN * 16) +
-                                                            (row & 7) * 64 + part * 16);
-          for (int rep = 0; rep < reps; ++rep)
-            *reinterpret_cast<uint4*>(out.row(p, m, rep) + n) = val;
-        }
-      }
-      __syncwarp();
     }
-    if (tile + step < p.n_tiles) {
-      // This CTA's staging may be written again (the peer waits for it only
-      // before a next tile; after the last one, no handshake and no wait for
-      // the stores above).
-      mbar_arrive_cluster(peer_drained);
-    }
-
-    // 3. The TMEM accumulator goes back to the MMA issuer.
+    // The accumulator goes back to the leader's MMA issuer, which waits for it
+    // only before a tile two further on (none after the last two tiles: no
+    // arrive that nothing waits for, so the exit barrier need not order it).
     tc_fence_before_sync();
     __syncwarp();
-    if (lane == 0) mbar_arrive(b.tempty0 + 8 * acc);
+    if (lane == 0 && tile + 2 * step < p.n_tiles) mbar_arrive_cluster(lead_tempty + 8 * acc);
   }
 }
 
@@ -395,7 +353,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) gsr_small_kernel(const __gri
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* base_ptr = smem_raw + (base - raw);
-  const SmallLayout L = small_layout(p.m_pad, p.stages);
+  const SmallLayout L = small_layout(p.M, p.tile_rows, p.stages, p.small_kz);
   const SmallBars b(base + L.bars_off, L.stages);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + L.misc_off);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + L.misc_off + 4);
@@ -405,34 +363,39 @@ __global__ void __launch_bounds__(kSmallThreads, 1) gsr_small_kernel(const __gri
   ProducerStart start;
   if (warp == 0) start.init(p, L, rank);
 
-  if (threadIdx.x == 0) {
+  // Thread 32 (warp 1) creates the barriers and publishes them to the peer
+  // with its (releasing) arrival on the cluster barrier, and to this CTA's
+  // producer through named barrier 3. The other warps arrive without a
+  // release: the producer's arrival would otherwise wait for its cold
+  // descriptor prefetches (measured 1.6 us). Each role waits for the peer's
+  // barriers only before its first access to the peer; the leader's producer,
+  // which starts the stream, waits after its loop. The TMEM allocation
+  // (collective over the pair) comes after the arrival, off the producers'
+  // path: the MMA issuer and the epilogue get its address through named
+  // barrier 2.
+  if (threadIdx.x == 32) {
     for (uint32_t i = 0; i < L.stages; ++i) {
-      mbar_init(b.full0 + 8 * i, 1);    // expect_tx + the W and X bytes of a k-block
-      mbar_init(b.empty0 + 8 * i, 1);   // one MMA commit
+      mbar_init(b.full0 + 8 * i, 1);    // the leader's expect_tx + both CTAs' bytes
+      mbar_init(b.empty0 + 8 * i, 1);   // one MMA commit (the leader's, in both CTAs)
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(b.tfull0 + 8 * i, 1);                  // MMA commit
-      mbar_init(b.tempty0 + 8 * i, kSmallEpiWarps);    // one per epilogue warp
+      mbar_init(b.tfull0 + 8 * i, 1);                     // MMA commit
+      mbar_init(b.tempty0 + 8 * i, 2 * kSmallEpiWarps);   // every epilogue warp of the pair
     }
-    mbar_init(b.staged, 1);    // one expect_tx arrive per tile; the peer's bytes complete it
-    mbar_init(b.drained, kSmallEpiThreads);
     mbar_init(b.drain, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), L.tmem_cols);
-    tmem_relinquish();
+    __syncwarp();
+    cluster_arrive();
+    barriers_ready_arrive();
+  } else if (warp == 0) {
+    barriers_ready_sync();
+    cluster_arrive_relaxed();
+  } else {
+    cluster_arrive_relaxed();
   }
-  tc_fence_before_sync();
-  __syncthreads();
-  tc_fence_after_sync();
-  const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
-  // Only the epilogue touches the peer CTA (its staging area and barriers), so
-  // only the epilogue waits here for the peer's barriers to exist; the
-  // producer and the MMA issuer start at once and wait after their loops.
-  cluster_arrive();
 
   // Programmatic dependent launch, as in the main kernel: nothing above
   // touches global memory.
@@ -440,33 +403,44 @@ __global__ void __launch_bounds__(kSmallThreads, 1) gsr_small_kernel(const __gri
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   Ctl ctl{abort_flag, p.status, p.timeout_ns};
+  uint32_t tmem_base = 0;
   if (warp == 0) {
-    small_producer(p, L, base, b, start, ctl);
+    if (rank != 0) cluster_wait();
+    small_producer(p, L, base, b, start, rank, ctl);
     __syncwarp();
-    cluster_wait();
+    if (rank == 0) cluster_wait();
   } else if (warp == 1) {
-    small_mma(p, L, base, b, tmem_base, rank, ctl);
+    tmem_alloc_pair(smem_u32(tmem_slot), L.tmem_cols);
+    tmem_relinquish_pair();
+    tc_fence_before_sync();
+    tmem_handoff_sync();
+    tc_fence_after_sync();
+    tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+    cluster_wait();
+    if (rank == 0) small_mma(p, L, base, b, tmem_base, ctl);
     __syncwarp();
-    cluster_wait();
   } else {
+    tmem_handoff_sync();
+    tc_fence_after_sync();
+    tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
     cluster_wait();
-    small_epilogue(p, L, base, base_ptr, b, tmem_base, rank, ctl);
+    small_epilogue(p, L, b, tmem_base, rank, ctl);
   }
 
   // No CTA leaves while its peer may still write or signal it. On the normal
-  // path every write and arrive a CTA receives is one it waits for (the
-  // peer's staged bytes, and the drained arrive before a next tile; none
-  // follows the last tile), so the barrier needs no release, which would
-  // wait for the output stores.
+  // path every copy, commit and arrive a CTA receives is one it waits for (the
+  // producers drain the last commits; no accumulator hand-back follows the
+  // last two tiles), so the barrier needs no release, which would wait for
+  // the output stores.
   tc_fence_before_sync();
   cluster_barrier_relaxed();
   if (warp == 1) {
     tc_fence_after_sync();
-    tmem_dealloc(tmem_base, L.tmem_cols);
+    tmem_dealloc_pair(tmem_base, L.tmem_cols);
   }
-  // After a timed-out wait that is no longer so: the peer may have sent what
-  // this CTA stopped waiting for. Having passed the barrier, the peer has
-  // issued all of it; the CTA stays resident until it has surely landed.
+  // After a timed-out wait: the peer may have sent what this CTA stopped
+  // waiting for. Having passed the barrier, the peer has issued all of it;
+  // the CTA stays resident until it has surely landed.
   if (threadIdx.x == 0 && *abort_flag) {
     const uint64_t t0 = global_timer_ns();
     while (global_timer_ns() - t0 < 20000ull) __nanosleep(1000);
@@ -491,7 +465,7 @@ cudaError_t launch_small(const Params& p, int ctas, cudaStream_t stream) {
   attr[1].val.clusterDim.z = 1;
   cfg.gridDim = dim3(ctas, 1, 1);
   cfg.blockDim = dim3(kSmallThreads, 1, 1);
-  cfg.dynamicSmemBytes = small_layout(p.m_pad, p.stages).total;
+  cfg.dynamicSmemBytes = small_layout(p.M, p.tile_rows, p.stages, p.small_kz).total;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 2;

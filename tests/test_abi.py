@@ -234,45 +234,58 @@ def test_config_is_independent_of_mode(host):
             assert a == r
 
 
-def test_small_m_uses_the_k_pair_kernel(host):
-    # M <= 256 (AR/RS): the small-M kernel, tiles of W rows (block_n) against
-    # all rows, each tile split over K between the two CTAs of a cluster. The
-    # tile height is the smallest multiple of 8 that spreads N over every
-    # cluster in the fewest waves: N = 7168 on 148 SMs (74 clusters) gives
-    # 104-row tiles, 69 tiles on 138 CTAs, whatever M up to 256; on 152 SMs, 96
-    # rows and 75 tiles on 150 CTAs.
+def test_small_m_uses_the_pair_tile_kernel(host):
+    # M <= 256 (AR/RS): the small-M kernel, one CTA pair per tile of W rows
+    # (block_n, the pair MMA's N) over the whole K range, against all rows.
+    # The tile height is the smallest multiple of 16 that spreads N over every
+    # pair in the fewest waves: N = 7168 on 148 SMs (74 pairs) gives 112-row
+    # tiles, 64 tiles on 128 CTAs, whatever M up to 256; on 152 SMs, 96 rows
+    # and 75 tiles on 150 CTAs.
     for M in (1, 16, 127, 128, 129, 200, 256):
         d = host.describe(B.MODE_AR, M, 7168, 0, [896] * 8)
         assert (d["cta_group"], d["block_n"], d["schedule"], d["split"], d["tiles"], d["ctas"]) == \
-            (1, 104, 3, 2, 69, 138), M
+            (2, 112, 3, 1, 64, 128), M
         # no split-K partials or counters: the workspace is the fixed minimum
         assert d["workspace_bytes"] <= host.describe(B.MODE_AR, 4096, 7168, 0, [896] * 8)["workspace_bytes"]
     d = Host(host.lib, sm=152).describe(B.MODE_AR, 64, 7168, 0, [896] * 8)
     assert (d["block_n"], d["tiles"], d["ctas"]) == (96, 75, 150)
-    # more tiles than clusters: one cluster per SM pair, tiles walked in turn;
-    # N = 32640 needs four waves of at most 128 rows: 112-row tiles
+    # more tiles than pairs: tiles walked in turn; N = 32640 needs two waves
+    # of at most 256 rows: 224-row tiles
     d = host.describe(B.MODE_AR, 64, 32768 - 128, 0, [896] * 8)
-    assert (d["schedule"], d["block_n"], d["tiles"], d["ctas"]) == (3, 112, 292, 148)
-    # small N: one tile of 8 rows
+    assert (d["schedule"], d["block_n"], d["tiles"], d["ctas"]) == (3, 224, 146, 148)
+    # small N: one tile of 16 rows
     d = host.describe(B.MODE_AR, 64, 8, 0, [896] * 8)
-    assert (d["block_n"], d["tiles"], d["ctas"]) == (8, 1, 2)
+    assert (d["block_n"], d["tiles"], d["ctas"]) == (16, 1, 2)
     # the tile height as an option: 128 rows, 56 tiles on 112 CTAs
     h = Host(host.lib)
     B.gemm_shard_plan_set_option(h.plan, B.GSR_OPT_SMALL_TILE_ROWS, 128)
     d = h.describe(B.MODE_AR, 128, 7168, 0, [896] * 8)
     assert (d["schedule"], d["block_n"], d["tiles"], d["ctas"]) == (3, 128, 56, 112)
-    for bad in (-8, 4, 20, 136):
+    for bad in (-16, 8, 20, 136, 272):
         with pytest.raises(B.GsrError):
             B.gemm_shard_plan_set_option(h.plan, B.GSR_OPT_SMALL_TILE_ROWS, bad)
-    # a capped grid keeps whole clusters
+    # k-blocks per copy: the largest of 4, 2, 1 that leaves a ring of four
+    # stages, unless a shard has a ragged k-block; a shard's last copy may run
+    # past its k-blocks (14 per shard of 896: four copies of 4)
+    assert host.describe(B.MODE_AR, 1, 7168, 0, [896] * 8)["kblocks"] == 4       # 4 x 9 KB stages
+    assert host.describe(B.MODE_AR, 64, 7168, 0, [896] * 8)["kblocks"] == 4     # 32 rows a CTA
+    assert host.describe(B.MODE_AR, 128, 7168, 0, [896] * 8)["kblocks"] == 2    # 4 x 15 KB: 3 fit
+    assert Host(host.lib, sm=152).describe(B.MODE_AR, 128, 7168, 0, [896] * 8)["kblocks"] == 4
+    assert host.describe(B.MODE_AR, 1, 7168, 0, [1024] * 7)["kblocks"] == 4
+    assert host.describe(B.MODE_AR, 200, 7168, 0, [1024] * 7)["kblocks"] == 2   # 128 rows a CTA
+    assert host.describe(B.MODE_AR, 64, 7168, 0, [8, 72, 136])["kblocks"] == 1  # ragged
+    assert host.describe(B.MODE_AR, 4096, 7168, 0, [1024] * 7)["kblocks"] == 1  # the main kernel
+    h = Host(host.lib)
+    B.gemm_shard_plan_set_option(h.plan, B.GSR_OPT_SMALL_KBLOCKS, 1)
+    assert h.describe(B.MODE_AR, 64, 7168, 0, [896] * 8)["kblocks"] == 1
+    # a capped grid keeps whole pairs
     h = Host(host.lib)
     B.gemm_shard_plan_set_option(h.plan, B.GSR_OPT_MAX_CTAS, 9)
     assert h.describe(B.MODE_AR, 64, 7168, 0, [896] * 8)["ctas"] == 8
-    # above 256 rows, or with a single k-block, or in AG mode: the main kernel
+    # above 256 rows, or in AG mode: the main kernel; a single k-block is fine
     assert host.describe(B.MODE_AR, 257, 7168, 0, [896] * 8)["schedule"] != 3
-    assert host.describe(B.MODE_AR, 64, 7168, 0, [64])["schedule"] != 3
-    assert host.describe(B.MODE_AR, 64, 7168, 0, [8])["schedule"] != 3
-    # two shards of one (ragged) k-block each: one per CTA of the pair
+    assert host.describe(B.MODE_AR, 64, 7168, 0, [64])["schedule"] == 3
+    assert host.describe(B.MODE_AR, 64, 7168, 0, [8])["schedule"] == 3
     assert host.describe(B.MODE_AR, 64, 7168, 0, [8, 8])["schedule"] == 3
     assert host.describe(B.MODE_AG, 0, 7168, 7168, [16] * 8)["schedule"] != 3
     # a forced configuration option selects the main kernel unless small_m = 2
@@ -719,7 +732,8 @@ def test_last_error_string_is_per_thread(lib, host):
     ("CTA_GROUP", [0, 1, 2, 4], [-1, 3, 5]),
     ("SCHEDULE", [0, 5], [-1, 6]),
     ("SMALL_M", [0, 2], [-1, 3]),
-    ("SMALL_TILE_ROWS", [0, 8, 128], [-8, 4, 136]),
+    ("SMALL_TILE_ROWS", [0, 16, 256], [-16, 8, 136, 272]),
+    ("SMALL_KBLOCKS", [0, 1, 2, 4], [-1, 3, 8]),
 ])
 def test_every_option_checks_its_range(host, name, good, bad):
     opt = getattr(B, "GSR_OPT_" + name)

@@ -321,13 +321,13 @@ def test_split_k_ag_and_block_n_128():
 
 
 def test_heuristic_split_small_m_matches_oracle():
-    """M=128, N=7168, 8 shards of 896: the plan cuts every tile's k range into
-    pieces summed in k order."""
-    p, ws = plan()
+    """M=128, N=7168, 8 shards of 896 on the main kernel (the small-M kernel
+    off): the plan cuts every tile's k range into pieces summed in k order."""
+    p, ws = plan(small_m=1)
     d = B.gemm_shard_describe(p, B.MODE_AR, 128, 7168, 0, [896] * 8)
     assert d["split"] > 1 or d["sk_iters"] > 0
     inp = gi.gaussian_ar(128, 7168, [896] * 8, seed=99)
-    Y, _, _ = run_ar(inp)
+    Y, _, _ = run_ar(inp, (p, ws))
     assert_close(to_f64(Y.out), oracle.ar(inp.X_r, inp.W_r), "ar m128 split")
 
 
