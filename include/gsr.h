@@ -126,11 +126,10 @@ typedef enum {
                                fastest inside a group (0 = off: GSR_OPT_RASTER_M
                                applies), 1..64                                   */
     GSR_OPT_SMALL_KBLOCKS = 12 /* small-M kernel: k-blocks of 64 per copy: 0 =
-                               heuristic (the largest of 4, 2, 1 that divides
-                               every shard's k-block count, with every K_r a
-                               multiple of 64), else 1, 2 or 4: the largest of
-                               that value and the smaller ones that divides as
-                               above                                             */
+                               heuristic (the largest of 4, 3, 2 that leaves a
+                               ring of four stages, where every K_r is a
+                               multiple of 64; else 1), else 1..4: at most that
+                               many, by the same rule                            */
 } gsr_option;
 
 /*
@@ -401,7 +400,7 @@ typedef struct {
     int64_t sk_iters;       /* stream-K: k-blocks shared out over the workers       */
     int ctas;               /* persistent CTAs launched                             */
     size_t workspace_bytes; /* workspace this call needs                           */
-    int kblocks;            /* small-M kernel: k-blocks of 64 per copy (1, 2 or 4);
+    int kblocks;            /* small-M kernel: k-blocks of 64 per copy (1 to 4);
                                1 for the main kernel                              */
 } gsr_config;
 

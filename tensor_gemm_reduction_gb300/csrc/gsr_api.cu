@@ -215,7 +215,7 @@ bool small_m_config(const gemm_shard_plan* P, int mode, int64_t M, int64_t N, in
   c.cta_group = 2;
   c.sched = gsr::kSchedSmall;
   c.splits = 1;
-  // k-blocks per copy: the largest of 4, 2, 1 (at most the option) that
+  // k-blocks per copy: the largest of 4, 3, 2, 1 (at most the option) that
   // leaves a ring of at least four stages in shared memory, where no shard
   // has a ragged k-block (a 3-D view of a shard would read the next row where
   // a 2-D box reads zeros). A shard's last copy may run past its k-blocks:
@@ -223,7 +223,7 @@ bool small_m_config(const gemm_shard_plan* P, int mode, int64_t M, int64_t N, in
   c.kz = 1;
   bool whole = true;
   for (int r = 0; r < R; ++r) whole = whole && sizes[r] % BK == 0;
-  for (int kz = P->opt_small_kz ? P->opt_small_kz : 4; whole && kz > 1 && c.kz == 1; kz /= 2) {
+  for (int kz = P->opt_small_kz ? P->opt_small_kz : 4; whole && kz > 1 && c.kz == 1; --kz) {
     const int st = gsr::small_stages(static_cast<int>(M), c.block_n, kz);
     if (st >= 4 &&
         gsr::small_layout(static_cast<int>(M), c.block_n, st, kz).total <= gsr::kSmallSmemLimit)
@@ -798,8 +798,8 @@ gsr_status gemm_shard_plan_set_option(gemm_shard_plan* plan, gsr_option option, 
       plan->opt_small = static_cast<int>(value);
       return ok();
     case GSR_OPT_SMALL_KBLOCKS:
-      if (value != 0 && value != 1 && value != 2 && value != 4)
-        return fail(GSR_ERR_INVALID_VALUE, "small_kblocks must be 0, 1, 2 or 4");
+      if (value < 0 || value > 4)
+        return fail(GSR_ERR_INVALID_VALUE, "small_kblocks must be 0..4");
       plan->opt_small_kz = static_cast<int>(value);
       return ok();
     case GSR_OPT_SMALL_TILE_ROWS:

@@ -89,7 +89,7 @@ struct Params {  // 128-byte aligned through its CUtensorMap members
   int tile_rows;                // small-M kernel: W rows per tile (the pair MMA's N:
                                 // a multiple of 16, at most kSmallMaxTileN)
   int small_kz;                 // small-M kernel: k-blocks per copy (1: 2-D copies;
-                                // 2 or 4: 3-D copies of that many k-blocks)
+                                // 2..4: 3-D copies of that many k-blocks)
 };
 
 // ---------------------------------------------------------------- small M
@@ -100,7 +100,7 @@ struct Params {  // 128-byte aligned through its CUtensorMap members
 // (each CTA holds h = ceil(M / 2) rows rounded up to 16: an MMA of 128 rows,
 // 64 per CTA, when h <= 64, else of 256, 128 per CTA) and the tile's W rows
 // as its N (each CTA holds half of them). A ring stage holds kz consecutive
-// k-blocks of each operand (one copy each: kz = 1 is a 2-D box, kz = 2 or 4
+// k-blocks of each operand (one copy each: kz = 1 is a 2-D box, kz = 2..4
 // a 3-D box over a {64, rows, K_r / 64} view of the shard, whose last stage
 // may run past the shard's k-blocks into zero fill). Its shared memory, from a
 // 1024-aligned base: the X ring, the W ring, the mbarriers and a few words.

@@ -264,15 +264,16 @@ def test_small_m_uses_the_pair_tile_kernel(host):
     for bad in (-16, 8, 20, 136, 272):
         with pytest.raises(B.GsrError):
             B.gemm_shard_plan_set_option(h.plan, B.GSR_OPT_SMALL_TILE_ROWS, bad)
-    # k-blocks per copy: the largest of 4, 2, 1 that leaves a ring of four
+    # k-blocks per copy: the largest of 4, 3, 2, 1 that leaves a ring of four
     # stages, unless a shard has a ragged k-block; a shard's last copy may run
     # past its k-blocks (14 per shard of 896: four copies of 4)
     assert host.describe(B.MODE_AR, 1, 7168, 0, [896] * 8)["kblocks"] == 4       # 4 x 9 KB stages
     assert host.describe(B.MODE_AR, 64, 7168, 0, [896] * 8)["kblocks"] == 4     # 32 rows a CTA
-    assert host.describe(B.MODE_AR, 128, 7168, 0, [896] * 8)["kblocks"] == 2    # 4 x 15 KB: 3 fit
+    assert host.describe(B.MODE_AR, 128, 7168, 0, [896] * 8)["kblocks"] == 3    # 4 x 15 KB: 3 fit
     assert Host(host.lib, sm=152).describe(B.MODE_AR, 128, 7168, 0, [896] * 8)["kblocks"] == 4
     assert host.describe(B.MODE_AR, 1, 7168, 0, [1024] * 7)["kblocks"] == 4
-    assert host.describe(B.MODE_AR, 200, 7168, 0, [1024] * 7)["kblocks"] == 2   # 128 rows a CTA
+    assert host.describe(B.MODE_AR, 129, 7168, 0, [896] * 8)["kblocks"] == 3    # 80 rows a CTA
+    assert host.describe(B.MODE_AR, 200, 7168, 0, [1024] * 7)["kblocks"] == 2   # 112 rows a CTA
     assert host.describe(B.MODE_AR, 64, 7168, 0, [8, 72, 136])["kblocks"] == 1  # ragged
     assert host.describe(B.MODE_AR, 4096, 7168, 0, [1024] * 7)["kblocks"] == 1  # the main kernel
     h = Host(host.lib)
@@ -733,7 +734,7 @@ def test_last_error_string_is_per_thread(lib, host):
     ("SCHEDULE", [0, 5], [-1, 6]),
     ("SMALL_M", [0, 2], [-1, 3]),
     ("SMALL_TILE_ROWS", [0, 16, 256], [-16, 8, 136, 272]),
-    ("SMALL_KBLOCKS", [0, 1, 2, 4], [-1, 3, 8]),
+    ("SMALL_KBLOCKS", [0, 1, 3, 4], [-1, 5, 8]),
 ])
 def test_every_option_checks_its_range(host, name, good, bad):
     opt = getattr(B, "GSR_OPT_" + name)

@@ -121,7 +121,7 @@ def test_small_repeat_calls_and_main_kernel_agree():
 @pytest.mark.parametrize("M,K_r", [(1, [512, 256, 1024]), (64, [896, 192]), (100, [512, 256, 1024]),
                                    (200, [896, 192, 64])])
 def test_small_kblocks_per_copy_agree_bitwise(M, K_r):
-    """Copies of 1, 2 or 4 k-blocks (a 2-D box, or a 3-D box over a strided
+    """Copies of 1 to 4 k-blocks (a 2-D box, or a 3-D box over a strided
     {64, rows, K_r / 64} view of each shard) feed the same MMAs in the same
     order, so the outputs are bit-identical. Shards of 14, 3 and 1 k-blocks
     end in a copy that runs past the shard: its zero-filled k-blocks add
@@ -129,7 +129,7 @@ def test_small_kblocks_per_copy_agree_bitwise(M, K_r):
     inp = gi.gaussian_ar(M, 1000, K_r, seed=41)
     ref = oracle.ar(inp.X_r, inp.W_r)
     seen, bits = set(), None
-    for kz in (1, 2, 4):
+    for kz in (1, 2, 3, 4):
         p = small_plan(small_kblocks=kz)
         seen.add(B.gemm_shard_describe(p[0], B.MODE_AR, M, 1000, 0, K_r)["kblocks"])
         Y = run(inp, p)
