@@ -84,7 +84,9 @@ typedef enum {
     GSR_OPT_MAX_CTAS = 4,   /* cap on persistent CTAs: 0 = one per SM               */
     GSR_OPT_RASTER_M = 5,   /* m-tiles per raster group (m runs fastest inside a
                                group): 0 = heuristic, 1..64                         */
-    GSR_OPT_L2_HINTS = 6,   /* TMA L2 eviction hints: 0 = heuristic, 1 = none,
+    GSR_OPT_L2_HINTS = 6,   /* TMA L2 eviction hints: 0 = heuristic (main kernel:
+                               2 where both operands together fit in the L2,
+                               else none; small-M kernel: 2), 1 = none,
                                2 = A evict-last / B evict-first,
                                3 = A evict-first / B evict-last                     */
     GSR_OPT_CTA_GROUP = 7,  /* CTAs per MMA tile: 0 = heuristic, 1 = one CTA per
@@ -154,7 +156,8 @@ gsr_status gemm_shard_plan_create(gemm_shard_plan **out, int device, int64_t max
  * Create a plan bound to no device, for a machine without a GPU: it describes
  * a device with `sm_count` SMs. Calls made with it check their arguments and
  * workspace exactly as on a device, then return GSR_ERR_UNSUPPORTED instead of
- * launching (no device pointer is touched). gemm_shard_describe and
+ * launching (no device pointer is touched). It takes a GB300's L2 size (126
+ * MiB) where the configuration depends on it. gemm_shard_describe and
  * gemm_shard_workspace_size work as for a device plan. Errors as
  * gemm_shard_plan_create, plus GSR_ERR_INVALID_VALUE for sm_count < 1.
  */
@@ -402,6 +405,8 @@ typedef struct {
     size_t workspace_bytes; /* workspace this call needs                           */
     int kblocks;            /* small-M kernel: k-blocks of 64 per copy (1 to 4);
                                1 for the main kernel                              */
+    int l2_hints;           /* the TMA L2 hints taken: 1 = none, 2 = A evict-last /
+                               B evict-first, 3 = A evict-first / B evict-last    */
 } gsr_config;
 
 /* The kernel configuration the plan chooses for a call, for logging and tests:

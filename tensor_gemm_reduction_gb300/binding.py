@@ -64,7 +64,8 @@ class GsrConfig(ctypes.Structure):
                 ("schedule", ctypes.c_int), ("split", ctypes.c_int),
                 ("tiles", ctypes.c_int64), ("dp_tiles", ctypes.c_int64),
                 ("sk_iters", ctypes.c_int64), ("ctas", ctypes.c_int),
-                ("workspace_bytes", ctypes.c_size_t), ("kblocks", ctypes.c_int)]
+                ("workspace_bytes", ctypes.c_size_t), ("kblocks", ctypes.c_int),
+                ("l2_hints", ctypes.c_int)]
 
 
 class GsrError(RuntimeError):

@@ -299,6 +299,25 @@ def test_small_m_uses_the_pair_tile_kernel(host):
         B.gemm_shard_plan_set_option(h.plan, B.GSR_OPT_SMALL_M, 3)
 
 
+def test_l2_hints_where_both_operands_fit_in_l2(host):
+    # The main kernel asks for A evict-last / B evict-first where A and W fit
+    # in the L2 together (126 MiB on a host plan), else for no hints; the
+    # option overrides; the small-M kernel always takes them.
+    assert host.describe(B.MODE_AG, 0, 3648, 7168, [256] * 8)["l2_hints"] == 2    # 81 MB
+    assert host.describe(B.MODE_AG, 0, 3648, 7168, [512] * 8)["l2_hints"] == 2    # 111 MB
+    assert host.describe(B.MODE_AG, 0, 3648, 7168, [1024] * 8)["l2_hints"] == 1   # 170 MB
+    assert host.describe(B.MODE_AG, 0, 6288, 7168, [4096] * 8)["l2_hints"] == 1
+    assert host.describe(B.MODE_AR, 1000, 7168, 0, [896] * 8)["l2_hints"] == 2    # 117 MB
+    assert host.describe(B.MODE_RS, 1000, 7168, 0, [896] * 8)["l2_hints"] == 2
+    assert host.describe(B.MODE_AR, 4096, 7168, 0, [896] * 8)["l2_hints"] == 1    # 162 MB
+    assert host.describe(B.MODE_AR, 64, 7168, 0, [896] * 8)["l2_hints"] == 2      # small-M
+    for v, want in ((1, 1), (2, 2), (3, 3)):
+        h = Host(host.lib)
+        B.gemm_shard_plan_set_option(h.plan, B.GSR_OPT_L2_HINTS, v)
+        assert h.describe(B.MODE_AG, 0, 3648, 7168, [256] * 8)["l2_hints"] == want
+        assert h.describe(B.MODE_AR, 4096, 7168, 0, [896] * 8)["l2_hints"] == want
+
+
 def test_small_m_off_splits_tiles(lib):
     h = Host(lib)
     B.gemm_shard_plan_set_option(h.plan, B.GSR_OPT_SMALL_M, 1)
