@@ -379,3 +379,26 @@ def test_ar_replicated_outputs_equal_ar_bitwise(M, N, K_r, variant):
         assert np.array_equal(bits_of(g.out), ref)
         assert g.guards_intact()
     assert_close(to_f64(reps[-1].out), oracle.ar(inp.X_r, inp.W_r), "replicated")
+
+
+@pytest.mark.parametrize("mode", ["ar", "ag"])
+def test_l2_hints_change_no_bit(mode):
+    """The TMA L2 eviction hints (none, A evict-last / B evict-first, the
+    reverse) change only what the L2 keeps: the configuration and the
+    summation order are the same, so the outputs are bit-identical. The shapes
+    fit in L2, where the heuristic takes the hints."""
+    if mode == "ar":
+        inp = gi.gaussian_ar(700, 1032, [512, 384], seed=61)
+        outs = [run_ar(inp, p=plan(l2_hints=h))[0] for h in (1, 2, 3)]
+        ref = oracle.ar(inp.X_r, inp.W_r)
+    else:
+        inp = gi.gaussian_ag([300, 0, 448, 129], 1032, 512, seed=62)
+        outs = [run_ag(inp, p=plan(l2_hints=h)) for h in (1, 2, 3)]
+        ref = oracle.ag(inp.A_r, inp.W)
+    assert B.gemm_shard_describe(plan()[0], B.MODE_AR if mode == "ar" else B.MODE_AG,
+                                 700 if mode == "ar" else 0, 1032, 0 if mode == "ar" else 512,
+                                 [512, 384] if mode == "ar" else [300, 0, 448, 129])["l2_hints"] == 2
+    for y in outs:
+        assert y.guards_intact()
+        assert np.array_equal(bits_of(y.out), bits_of(outs[0].out))
+    assert_close(to_f64(outs[0].out), ref, f"{mode} with L2 hints")
