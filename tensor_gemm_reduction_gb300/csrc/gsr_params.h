@@ -97,7 +97,7 @@ struct Params {  // 128-byte aligned through its CUtensorMap members
 // two) per tile of tile_rows rows of W (output columns; a multiple of 16, at
 // most kSmallMaxTileN) over the whole K range, with every activation row in
 // the tile: tcgen05.mma.cta_group::2 with the activation rows as the MMA's M
-// (each CTA holds h = ceil(M / 2) rows rounded up to 16: an MMA of 128 rows,
+// (each CTA holds h = ceil(M / 2) rows rounded up to 8: an MMA of 128 rows,
 // 64 per CTA, when h <= 64, else of 256, 128 per CTA) and the tile's W rows
 // as its N (each CTA holds half of them). A ring stage holds kz consecutive
 // k-blocks of each operand (one copy each: kz = 1 is a 2-D box, kz = 2..4
@@ -114,7 +114,7 @@ constexpr uint32_t kSmallSmemLimit = 232448;     // 227 KB per CTA
 
 struct SmallLayout {
   uint32_t mma_m;        // 128 (x_rows <= 64) or 256
-  uint32_t x_rows;       // h: activation rows per CTA (rank r holds rows r*h ..
+  uint32_t x_rows;       // h: activation rows per CTA, a multiple of 8 (rank r holds rows r*h ..
                          // r*h + h); the X box height
   uint32_t kz;           // k-blocks per stage
   uint32_t x_bytes, w_bytes;    // one k-block of X, of W
@@ -133,7 +133,7 @@ __host__ __device__ inline SmallLayout small_layout(int M, int tile_rows, int st
   // stale shared memory (TMEM lanes that are never stored) and rows past M
   // are zero-filled by the copy (or, when a CTA has none, never loaded).
   const int half = (M + 1) / 2;
-  L.x_rows = static_cast<uint32_t>(half <= 16 ? 16 : (half + 15) / 16 * 16);
+  L.x_rows = static_cast<uint32_t>(half <= 8 ? 8 : (half + 7) / 8 * 8);   // whole 8-row swizzle atoms
   L.mma_m = L.x_rows <= 64 ? 128u : 256u;
   L.x_bytes = L.x_rows * BK * 2;
   L.w_bytes = static_cast<uint32_t>(tile_rows / 2) * BK * 2;

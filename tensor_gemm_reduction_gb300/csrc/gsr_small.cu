@@ -13,7 +13,7 @@
 // rows as the MMA's M and the tile's W rows as its N, so the pair streams a
 // disjoint slice of W and nothing is reduced between CTAs. Each CTA holds
 // half of the tile's W rows and h = ceil(M / 2) activation rows (rounded up
-// to 16; rank r holds rows r*h .. r*h + h, so both stream the same bytes):
+// to 8; rank r holds rows r*h .. r*h + h, so both stream the same bytes):
 // - h <= 64: the MMA's M is 128, 64 rows per CTA. The accumulator of a CTA
 //   holds its 64 rows twice over in TMEM: lanes 0-63 the tile's first
 //   tile_rows/2 columns, lanes 64-127 the others (columns 0 .. tile_rows/2).
