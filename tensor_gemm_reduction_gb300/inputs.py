@@ -234,10 +234,12 @@ AR_OPROJ = [Workload(f"ar_oproj_m{m}", "ar", N=7168, K=7168, R=8, M=m)
 # Decode batches below 128 rows, where the pages' fused AR was slower than the
 # unfused path (GEMM-RS/AR page, risks and impact): the same projection.
 AR_DECODE = [Workload(f"ar_oproj_m{m}", "ar", N=7168, K=7168, R=8, M=m) for m in (1, 16, 64)]
+# The largest batch the small-M kernel serves (its 256-row MMA form).
+AR_SMALL_TOP = [Workload("ar_oproj_m256", "ar", N=7168, K=7168, R=8, M=256)]
 # RS shares its seed with AR o_proj M=32768, so one set of inputs serves both.
 RS_ALL = [Workload(f"rs_r{r}", "rs", N=7168, K=7168, R=r, M=32768,
                    seed=default_seed(32768, 7168)) for r in (2, 4, 8, 16)]
-ALL_WORKLOADS = [AR_TINY] + AG_KDA + AG_MLA + AR_DECODE + AR_OPROJ + RS_ALL
+ALL_WORKLOADS = [AR_TINY] + AG_KDA + AG_MLA + AR_DECODE + AR_OPROJ[:2] + AR_SMALL_TOP + AR_OPROJ[2:] + RS_ALL
 
 
 def make_inputs(w: Workload, device: str | torch.device = "cpu"):

@@ -22,7 +22,7 @@ def test_workload_table_has_the_pages_projection_shapes():
             assert (w.mode, w.N, w.K, w.R, w.M) == ("ag", n, 7168, 8, 8 * local)
             assert w.shard_sizes() == [local] * 8
     # GEMM-RS/AR page, o_proj: N = K = 7168, K split over 8 ranks.
-    for m in (1, 16, 64, 128, 129, 1000, 4096, 32768):
+    for m in (1, 16, 64, 128, 129, 256, 1000, 4096, 32768):
         w = names[f"ar_oproj_m{m}"]
         assert (w.mode, w.N, w.K, w.R, w.M) == ("ar", 7168, 7168, 8, m)
         assert w.shard_sizes() == [896] * 8

@@ -80,7 +80,7 @@ def test_ag_full_size_every_element(w):
     st.finish(expect_elements=w.M * w.N)
 
 
-@pytest.mark.parametrize("w", [x for x in gi.AR_DECODE + gi.AR_OPROJ if x.M != 32768],
+@pytest.mark.parametrize("w", [x for x in gi.AR_DECODE + gi.AR_SMALL_TOP + gi.AR_OPROJ if x.M != 32768],
                          ids=lambda w: w.name)
 def test_ar_full_size_every_element(w):
     p, ws = plan()
