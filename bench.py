@@ -35,6 +35,7 @@ sys.path.insert(0, ROOT)
 METRIC = "BF16 TFLOP/s per mode vs M on 1 GB300; % of dense BF16 peak; oracle time"
 ROW_PAUSE_S = 0.3   # idle pause before each per-workload row (see sweep)
 L2_BYTES = 126 * 1024 * 1024
+DECODE_LAYERS = 4   # o_proj weight sets of the decode-step rows: 4 x 103 MB, more than L2
 # GB300 datasheet figures (dense bf16 tensor throughput, HBM3e bandwidth). The
 # roofline's `peak` is the measured one (a cuBLAS GEMM and a device copy on
 # this machine); these give the second fraction, against the nominal part.
@@ -554,9 +555,68 @@ def sweep(plan, ws, dev, pk, names):
                              w.bytes / (NOMINAL_HBM_GBS * 1e9)) / t, 3),
                      "bound": "tensor" if w.flops / (pk["bf16_burst"] * 1e12) >= w.bytes / (pk["hbm_gbs"] * 1e9) else "hbm",
                      "split": d["split"], "block_n": d["block_n"],
-                     "kernel": "small_m" if d["schedule"] == 3 else "main"})
+                     "kernel": "small_m" if d["schedule"] == 3 else "main",
+                     "timing": "single launches, L2 flushed before each"})
         del r
         torch.cuda.empty_cache()
+    return rows
+
+
+def sweep_decode_layers(plan, ws, dev, pk, names):
+    """Decode-size AR as a decode step runs it: calls back to back, each on the
+    next of DECODE_LAYERS o_proj weight sets (a model's successive layers), so
+    that W always streams from HBM with no L2 flush (the weight sets together
+    are larger than the L2). Time per call: CUDA-event time of a region of
+    20 x DECODE_LAYERS calls over their number, the median of five regions.
+    Programmatic dependent launch lets each call start while the previous one
+    ends, as in a decode step; the flushed rows time single launches instead."""
+    import statistics
+    import torch
+    from tensor_gemm_reduction_gb300 import binding as B
+    from tensor_gemm_reduction_gb300 import inputs as gi
+    # the o_proj workloads of the small-M kernel's range (M <= 256)
+    ws_list = [w for w in gi.ALL_WORKLOADS
+               if w.name.startswith("ar_oproj_m") and w.M <= 256
+               and (not names or w.name in names or f"{w.name}_layers{DECODE_LAYERS}" in names)]
+    if not ws_list:
+        return []
+    w0 = ws_list[0]
+    layers = [gi.gaussian_ar(1, w0.N, w0.shard_sizes(), seed=1000 + l, device=dev).W_r
+              for l in range(DECODE_LAYERS)]
+    rows = []
+    for w in ws_list:
+        assert (w.N, w.shard_sizes()) == (w0.N, w0.shard_sizes())
+        X_r = gi.make_inputs(w, device=dev).X_r
+        Y = torch.empty(w.M, w.N, dtype=torch.bfloat16, device=dev)
+        calls = [B.prepare_ar(plan, X_r, W_r, Y, ws) for W_r in layers]
+        n = 20 * DECODE_LAYERS
+        torch.cuda.synchronize()
+        time.sleep(ROW_PAUSE_S)
+        for i in range(2 * DECODE_LAYERS):
+            calls[i % DECODE_LAYERS]()
+        per_call = []
+        for _ in range(5):
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record()
+            for i in range(n):
+                calls[i % DECODE_LAYERS]()
+            e.record()
+            torch.cuda.synchronize()
+            per_call.append(s.elapsed_time(e) * 1e-3 / n)
+        B.gemm_shard_check_status(plan, ws)     # raises if an in-kernel wait ran out
+        t = statistics.median(per_call)
+        d = B_describe(plan, w)
+        rows.append({"workload": f"{w.name}_layers{DECODE_LAYERS}", "mode": "ar", "M": w.M, "N": w.N,
+                     "K": w.K, "R": w.R, "us": round(t * 1e6, 2),
+                     "hbm_gbs": round(w.bytes / t / 1e9, 1),
+                     "roofline_frac": round(w.bytes / (pk["hbm_gbs"] * 1e9) / t, 3),
+                     "roofline_frac_nominal": round(w.bytes / (NOMINAL_HBM_GBS * 1e9) / t, 3),
+                     "bound": "hbm", "kernel": "small_m" if d["schedule"] == 3 else "main",
+                     "timing": f"back-to-back calls over {DECODE_LAYERS} weight sets "
+                               f"({DECODE_LAYERS * 2 * w.N * w.K / 1e6:.0f} MB, more than L2), no flush"})
+        del X_r, Y, calls
+    del layers
+    torch.cuda.empty_cache()
     return rows
 
 
@@ -754,6 +814,7 @@ def main():
         torch.cuda.empty_cache()
         names = [s for s in args.sweep_only.split(",") if s]
         result["per_config"] = [sweep_floor(dev)] + sweep(plan, ws, dev, pk, names)
+        result["per_config"] += sweep_decode_layers(plan, ws, dev, pk, names)
         if not names or "pack_sp_t4" in names:
             result["per_config"].append(sweep_pack(plan, ws, dev, pk))
     if rank == 0:

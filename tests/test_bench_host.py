@@ -50,6 +50,14 @@ def test_algorithmic_work_closed_forms():
     assert p.bytes == 2 * 2 * (8 * 4096 - 5) * 4 * 7168
 
 
+def test_decode_layer_rows_stream_more_weights_than_the_l2_holds():
+    # The decode-step rows run without an L2 flush. A weight set is used again
+    # only after the three others (3 x 103 MB) have streamed through the L2,
+    # so every call reads its W from HBM.
+    w = bench.workload_by_name("ar_oproj_m1")
+    assert (bench.DECODE_LAYERS - 1) * 2 * w.N * w.K > bench.L2_BYTES
+
+
 def test_unknown_workload_is_rejected():
     with pytest.raises(SystemExit):
         bench.workload_by_name("no_such_workload")
