@@ -34,6 +34,14 @@
  *   - Streams: calls are stream-ordered and asynchronous. Nothing synchronises
  *     except gemm_shard_check_status. One workspace must not be used by two
  *     calls that may run at the same time.
+ *   - Graphs: gemm_ar, gemm_rs and gemm_ag may be recorded in a CUDA graph
+ *     (stream capture). A call's tensor maps and kernel parameters are built
+ *     on the host when the call is made, so the graph holds that call's
+ *     pointers and shapes, and a replay reads the buffers' current contents.
+ *     The workspace's split-K counters are back at zero after every launch,
+ *     so replays need no re-initialisation. gemm_shard_check_status
+ *     synchronises and cannot be captured. gemm_ar_noalloc allocates its
+ *     built-in scratch at its first call, which must not be captured.
  *   - Errors: argument errors are detected before any launch and return
  *     GSR_ERR_INVALID_VALUE / GSR_ERR_WORKSPACE without touching the GPU. A
  *     failed launch returns GSR_ERR_CUDA. Every wait inside the kernel is
