@@ -40,8 +40,7 @@
  *     pointers and shapes, and a replay reads the buffers' current contents.
  *     The workspace's split-K counters are back at zero after every launch,
  *     so replays need no re-initialisation. gemm_shard_check_status
- *     synchronises and cannot be captured. gemm_ar_noalloc allocates its
- *     built-in scratch at its first call, which must not be captured.
+ *     synchronises and cannot be captured.
  *   - Errors: argument errors are detected before any launch and return
  *     GSR_ERR_INVALID_VALUE / GSR_ERR_WORKSPACE without touching the GPU. A
  *     failed launch returns GSR_ERR_CUDA. Every wait inside the kernel is
