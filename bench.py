@@ -562,6 +562,16 @@ def sweep(plan, ws, dev, pk, names):
     return rows
 
 
+def decode_layer_workloads(names=()):
+    """The workloads of the decode-step rows: the o_proj shapes in the small-M
+    kernel's range (M <= 256), all of them, or those named (by workload or by
+    row name)."""
+    from tensor_gemm_reduction_gb300 import inputs as gi
+    return [w for w in gi.ALL_WORKLOADS
+            if w.name.startswith("ar_oproj_m") and w.M <= 256
+            and (not names or w.name in names or f"{w.name}_layers{DECODE_LAYERS}" in names)]
+
+
 def sweep_decode_layers(plan, ws, dev, pk, names):
     """Decode-size AR as a decode step runs it: calls back to back, each on the
     next of DECODE_LAYERS o_proj weight sets (a model's successive layers), so
@@ -574,10 +584,7 @@ def sweep_decode_layers(plan, ws, dev, pk, names):
     import torch
     from tensor_gemm_reduction_gb300 import binding as B
     from tensor_gemm_reduction_gb300 import inputs as gi
-    # the o_proj workloads of the small-M kernel's range (M <= 256)
-    ws_list = [w for w in gi.ALL_WORKLOADS
-               if w.name.startswith("ar_oproj_m") and w.M <= 256
-               and (not names or w.name in names or f"{w.name}_layers{DECODE_LAYERS}" in names)]
+    ws_list = decode_layer_workloads(names)
     if not ws_list:
         return []
     w0 = ws_list[0]

@@ -58,6 +58,14 @@ def test_decode_layer_rows_stream_more_weights_than_the_l2_holds():
     assert (bench.DECODE_LAYERS - 1) * 2 * w.N * w.K > bench.L2_BYTES
 
 
+def test_decode_layer_rows_cover_the_small_m_o_proj_shapes():
+    assert [w.M for w in bench.decode_layer_workloads()] == [1, 16, 64, 128, 129, 256]
+    assert {w.K for w in bench.decode_layer_workloads()} == {7168}
+    assert [w.M for w in bench.decode_layer_workloads(["ar_oproj_m129", "ag_kda_m2048"])] == [129]
+    assert [w.M for w in bench.decode_layer_workloads(["ar_oproj_m1_layers4"])] == [1]
+    assert bench.decode_layer_workloads(["ar_oproj_m1000"]) == []
+
+
 def test_unknown_workload_is_rejected():
     with pytest.raises(SystemExit):
         bench.workload_by_name("no_such_workload")
