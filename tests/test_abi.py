@@ -595,6 +595,9 @@ def test_workspace_and_schedule_invariants_over_shapes(lib, sm, schedule):
         d = h.describe(B.MODE_AR, M, N, 0, K_r)
         assert d["workspace_bytes"] <= h.ws_bytes, (M, N, K_r)
         assert 1 <= d["ctas"] <= sm
+        # RS rows equal AR rows bit for bit only because the configuration
+        # never depends on the mode.
+        assert h.describe(B.MODE_RS, M, N, 0, K_r) == d, (M, N, K_r)
         kb = sum((k + 63) // 64 for k in K_r)
         workers = d["ctas"] // d["cta_group"]
         if d["schedule"] == 4:
@@ -602,6 +605,32 @@ def test_workspace_and_schedule_invariants_over_shapes(lib, sm, schedule):
             assert 0 < tail * d["split"] <= workers and 1 <= d["split"] <= min(3, kb), (M, N, K_r, d)
         if d["schedule"] in (2, 4) and d["dp_tiles"] == d["tiles"]:
             assert d["sk_iters"] == 0
+
+
+@pytest.mark.parametrize("sm", [16, 148, 152])
+@pytest.mark.parametrize("opts", [{}, {"cta_group": 4}, {"block_n": 192}, {"schedule": 5}],
+                         ids=["heuristic", "cta_group4", "block_n192", "split_tail"])
+def test_ag_workspace_and_grid_invariants_over_shapes(lib, sm, opts):
+    """AG over random shard sizes (empty shards included), N and K: every
+    configuration fits the plan's workspace, the grid fits the SMs in whole
+    clusters, and the call reaches the launch point."""
+    h = Host(lib, sm=sm, max_M=34816)
+    for name, value in opts.items():
+        B.gemm_shard_plan_set_option(h.plan, getattr(B, f"GSR_OPT_{name.upper()}"), value)
+    rng = np.random.default_rng(sm + 7 * len(opts))
+    shapes = [([4096] * 8, 6288, 7168), ([448] * 8, 3648, 7168), ([0, 0, 130], 136, 64)]
+    for _ in range(40):
+        R = int(rng.integers(1, 17))
+        M_r = [int(rng.integers(0, 4097)) if rng.random() > 0.2 else 0 for _ in range(R)]
+        if sum(M_r) > 34816 or sum(M_r) == 0:
+            M_r = [int(rng.integers(1, 2049))]
+        shapes.append((M_r, int(rng.integers(1, 1025)) * 8, int(rng.integers(1, 1025)) * 8))
+    for M_r, N, K in shapes:
+        d = h.describe(B.MODE_AG, 0, N, K, M_r)
+        assert d["workspace_bytes"] <= h.ws_bytes, (M_r, N, K, d)
+        assert 1 <= d["ctas"] <= sm and d["ctas"] % d["cta_group"] == 0, (M_r, N, K, d)
+        assert d["dp_tiles"] <= d["tiles"] and d["sk_iters"] >= 0, (M_r, N, K, d)
+        assert h.ag(N, K, M_r) == B.GSR_ERR_UNSUPPORTED, B.gsr_last_error_string()
 
 
 def _build_in_child(q):
